@@ -1,0 +1,27 @@
+"""Float64 CPU oracle (test infrastructure only).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
+``bench.py`` may import this package.  It is independent of the CUDA library:
+neither imports the other.  See ``oracle/attention.py`` for the passages each
+function follows.
+"""
+
+from .attention import (  # noqa: F401
+    NEG_INF,
+    Layout,
+    block_means,
+    chunk_summary,
+    dense_attention,
+    finalise,
+    logical_positions,
+    lse_merge,
+    make_layout,
+    merge_summaries,
+    moba_attention,
+    moba_block_gate,
+    neutral_summary,
+    sequence_index,
+    sparse_attention,
+    sparse_key_list,
+    summarised_attention,
+)

@@ -1,0 +1,35 @@
+// Host-side declarations shared by the API layer and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "cpattn.h"
+
+namespace cpattn {
+
+// Selection of keys for the general (warp-per-row) kernel.
+enum KeyMode { kDense = 0, kTokens = 1, kBlocks = 2 };
+
+struct SparseArgs {
+  const int32_t* indices;  // [Tq, index_heads, topk]
+  int32_t topk;
+  int32_t index_heads;
+  int32_t block_size;
+};
+
+// Launchers return the cudaError_t of the launch (no synchronisation).
+cudaError_t launch_rowwise(const cpattn_attn_args& a, KeyMode mode, const SparseArgs& sp,
+                           cudaStream_t stream);
+cudaError_t launch_lse_merge(int32_t n_parts, const float* part_o, const float* part_lse,
+                             int32_t Tq, int32_t H, int32_t Dv, void* o, int32_t o_dtype,
+                             int64_t o_stride_t, int64_t o_stride_h, float* lse,
+                             cudaStream_t stream);
+size_t block_gate_workspace(const cpattn_attn_args& a, int32_t block_size);
+size_t block_gate_smem(int n_blocks, int D);
+cudaError_t launch_block_gate(const cpattn_attn_args& a, int32_t block_size, int32_t topk,
+                              int32_t* sel, void* workspace, cudaStream_t stream);
+
+}  // namespace cpattn

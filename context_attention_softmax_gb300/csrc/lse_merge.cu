@@ -1,0 +1,106 @@
+// Merge of finalised per-chunk results (O_c, LSE_c) into the global result.
+//
+// "Context parallel attention: exchange keys and merge softmax globally",
+// para 3: rescale every chunk to the larger maximum, add, divide at the end.
+// In LSE form a finalised chunk (O_c, LSE_c) is its summary up to a common
+// factor (l_c = exp(LSE_c - m_c), z_c = l_c O_c), so the merge reads
+//   L = max_c LSE_c,  w_c = exp(LSE_c - L),  O = sum w_c O_c / sum w_c,
+//   LSE = L + ln sum w_c.
+// Para 4: a neutral chunk has LSE_c = -inf and weight 0 (never -inf - -inf);
+// all chunks neutral gives O = 0, LSE = -inf.
+//
+// Memory-bound: each (row, head) reads n_parts * (Dv + 1) floats once and
+// writes Dv outputs.  One warp per (row, head); lanes own 4 consecutive
+// channels per step so each part is read with 16-byte coalesced loads.
+#include "common.cuh"
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+constexpr int kWarps = 8;
+
+template <typename TO>
+__device__ __forceinline__ void store4(TO* p, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(kWarps * 32)
+lse_merge_kernel(int n_parts, const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                 int64_t rows, int H, int Dv, TO* __restrict__ o, int64_t ost, int64_t osh,
+                 float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int64_t t = row / H;
+  const int h = (int)(row - t * H);
+
+  float L = -CUDART_INF_F;
+  for (int c = lane; c < n_parts; c += 32) L = fmaxf(L, __ldg(part_lse + (int64_t)c * rows + row));
+  L = warp_max(L);
+
+  TO* orow = o + t * ost + h * osh;
+  if (L == -CUDART_INF_F) {
+    for (int d = lane * 4; d < Dv; d += 128) store4<TO>(orow + d, make_float4(0.f, 0.f, 0.f, 0.f));
+    if (lane == 0 && lse != nullptr) lse[row] = -CUDART_INF_F;
+    return;
+  }
+  float W = 0.f;
+  for (int d0 = 0; d0 < Dv; d0 += 128) {
+    const int d = d0 + lane * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    for (int c = 0; c < n_parts; ++c) {
+      const float lc = __ldg(part_lse + (int64_t)c * rows + row);
+      const float w = (lc == -CUDART_INF_F) ? 0.f : expf(lc - L);
+      wsum += w;
+      if (w != 0.f && d < Dv) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(part_o + ((int64_t)c * rows + row) * Dv + d));
+        acc.x = fmaf(w, x.x, acc.x);
+        acc.y = fmaf(w, x.y, acc.y);
+        acc.z = fmaf(w, x.z, acc.z);
+        acc.w = fmaf(w, x.w, acc.w);
+      }
+    }
+    W = wsum;
+    if (d < Dv) {
+      const float inv = 1.f / wsum;
+      store4<TO>(orow + d, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    }
+  }
+  if (lane == 0 && lse != nullptr) lse[row] = L + logf(W);
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(int32_t n_parts, const float* part_o, const float* part_lse,
+                             int32_t Tq, int32_t H, int32_t Dv, void* o, int32_t o_dtype,
+                             int64_t o_stride_t, int64_t o_stride_h, float* lse,
+                             cudaStream_t stream) {
+  const int64_t rows = (int64_t)Tq * H;
+  if (rows == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((rows + kWarps - 1) / kWarps);
+  if (o_dtype == CPATTN_BF16)
+    lse_merge_kernel<__nv_bfloat16><<<blocks, kWarps * 32, 0, stream>>>(
+        n_parts, part_o, part_lse, rows, H, Dv, reinterpret_cast<__nv_bfloat16*>(o), o_stride_t,
+        o_stride_h, lse);
+  else
+    lse_merge_kernel<float><<<blocks, kWarps * 32, 0, stream>>>(
+        n_parts, part_o, part_lse, rows, H, Dv, reinterpret_cast<float*>(o), o_stride_t,
+        o_stride_h, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

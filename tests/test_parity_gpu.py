@@ -1,0 +1,263 @@
+"""GPU parity: every entry point through the C ABI against the float64 oracle.
+
+Small cases span several tiles with ragged tails and are compared element by
+element on every output; the full-size workloads run in the launch
+configuration the bench times and are compared on sampled rows (all heads,
+all channels of each sampled row).  Block selections are compared bit-exactly.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from context_attention_softmax_gb300 import (cpattn_block_gate, cpattn_chunk_fwd,
+                                             cpattn_lse_merge, cpattn_topk_sparse_fwd, inputs)
+
+from helpers import assert_matches, f64, layout_of, sample_rows, to_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from context_attention_softmax_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _chunk(w, **kw):
+    q, k, v = to_gpu(w)
+    return cpattn_chunk_fwd(q, k, v, scale=w.scale, causal=w.causal, causal_offset=w.causal_offset,
+                            cu_seqlens=w.cu_seqlens, q_chunk_map=w.q_chunk_map,
+                            kv_chunk_map=w.kv_chunk_map, chunk_len=w.chunk_len, **kw)
+
+
+# ---------------------------------------------------------------------------
+# dense chunk attention
+# ---------------------------------------------------------------------------
+
+def test_tiny_fp32_two_summaries_then_merge():
+    w = inputs.tiny_fp32()
+    o, lse, po, pl = _chunk(w, kv_chunk_len=w.kv_chunk_len)
+    q, k, v = f64(w)
+    O, L, PO, PL = orc.summarised_attention(q, k, v, w.scale, layout_of(w), w.kv_chunk_len)
+    assert_matches(o, lse, O, L, "fp32", "final")
+    for c in range(2):
+        assert_matches(po[c], pl[c], PO[c], PL[c], "fp32", f"summary {c}")
+    om, lm = cpattn_lse_merge(po, pl, out_dtype=torch.float32)
+    assert_matches(om, lm, O, L, "fp32", "lse_merge")
+    o2, l2 = _chunk(w)
+    assert_matches(o2, l2, O, L, "fp32", "single pass")
+
+
+@pytest.mark.parametrize("Tq,Tk,off,Hq,Hkv,kvc", [
+    (300, 1000, 700, 4, 2, 256),     # ragged tails on both sides
+    (257, 1300, 700, 4, 1, 256),     # keys 1000.. never permitted: chunk 4 is neutral
+    (128, 640, 0, 2, 2, 0),          # offset 0: the first query sees one key
+])
+def test_dense_gqa_small(Tq, Tk, off, Hq, Hkv, kvc):
+    rng_w = inputs.dense_gqa(seed=1, global_seq=Tq, cp_size=1, rank=0, Hq=Hq, Hkv=Hkv, Tk=Tk,
+                             kv_chunks=0)
+    rng_w.causal_offset = off
+    w = rng_w
+    q, k, v = f64(w)
+    O, L, PO, PL = orc.summarised_attention(q, k, v, w.scale, layout_of(w), kvc or Tk)
+    if kvc:
+        o, lse, po, pl = _chunk(w, kv_chunk_len=kvc)
+        for c in range(po.shape[0]):
+            assert_matches(po[c], pl[c], PO[c], PL[c], "bf16", f"summary {c}")
+        if Tk == 1300:
+            assert torch.isneginf(pl[4]).all() and (po[4] == 0).all()
+    else:
+        o, lse = _chunk(w)
+    assert_matches(o, lse, O, L, "bf16", "final")
+
+
+def test_dense_gqa_full_size_sampled():
+    w = inputs.dense_gqa()
+    o, lse = _chunk(w)
+    rows = sample_rows(w.Tq, 48, edges=(1, 127, 128, 1023, 2047))
+    q, k, v = f64(w)
+    O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w), rows=rows)
+    assert_matches(o[rows.tolist()], lse[rows.tolist()], O, L, "bf16", "cfg full")
+    # the four-chunk summary form reaches the same result
+    o4, l4, po, pl = _chunk(w, kv_chunk_len=w.kv_chunk_len)
+    assert torch.isneginf(pl[3]).all()          # chunk 3 (keys 6144..) is fully masked
+    assert_matches(o4[rows.tolist()], l4[rows.tolist()], O, L, "bf16", "cfg 4 chunks")
+
+
+def test_noncausal_and_queries_outside_sequences():
+    w = inputs.dense_gqa(seed=3, global_seq=200, cp_size=1, rank=0, Hq=2, Hkv=2, Tk=333, kv_chunks=0)
+    w.causal = False
+    w.causal_offset = 150
+    w.cu_seqlens = np.array([0, 100, 160, 290], dtype=np.int32)   # positions >= 290 in no sequence
+    q, k, v = f64(w)
+    O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w))
+    assert np.isneginf(L[140:]).all()
+    o, lse = _chunk(w)
+    assert_matches(o, lse, O, L, "bf16", "non-causal varlen")
+
+
+def test_empty_inputs():
+    d = torch.device("cuda")
+    q = torch.randn(0, 4, 128, device=d, dtype=torch.bfloat16)
+    k = torch.randn(64, 2, 128, device=d, dtype=torch.bfloat16)
+    o, lse = cpattn_chunk_fwd(q, k, k, causal_offset=3)
+    assert o.shape == (0, 4, 128)
+    q = torch.randn(16, 4, 128, device=d, dtype=torch.bfloat16)
+    k0 = torch.randn(0, 2, 128, device=d, dtype=torch.bfloat16)
+    o, lse = cpattn_chunk_fwd(q, k0, k0)
+    torch.cuda.synchronize()
+    assert (o == 0).all() and torch.isneginf(lse).all()
+    o, lse, po, pl = cpattn_chunk_fwd(q, k0, k0, kv_chunk_len=32)
+    assert po.shape[0] == 0 and (o == 0).all() and torch.isneginf(lse).all()
+
+
+# ---------------------------------------------------------------------------
+# packed THD varlen + zigzag
+# ---------------------------------------------------------------------------
+
+def _zigzag_check(z, rows_per_rank=None):
+    qg, kg, vg = (inputs.as_f64(t) for t in (z.q_global, z.k_global, z.v_global))
+    lay_full = orc.make_layout(qg.shape[0], qg.shape[0], True, 0, z.cu_seqlens)
+    L = z.chunk_len
+    for r in range(z.cp_size):
+        w = z.rank_workload(r)
+        o, lse = _chunk(w)
+        if rows_per_rank is None:
+            rows = np.arange(w.Tq)
+        else:
+            rows = sample_rows(w.Tq, rows_per_rank, seed=r, edges=(L - 1, L, 2 * L - 1))
+        logical = np.concatenate([np.arange(c * L, (c + 1) * L) for c in z.rank_chunks(r)])[rows]
+        # the oracle's full logical run, rows scattered back by ownership
+        O, LSE = orc.dense_attention(qg, kg, vg, z.scale, lay_full, rows=logical)
+        assert_matches(o[rows.tolist()], lse[rows.tolist()], O, LSE, "bf16", f"rank {r}")
+        # and the oracle on the rank's own physical layout agrees too
+        if rows_per_rank is None and r == 0:
+            q, k, v = f64(w)
+            O2, L2 = orc.dense_attention(q, k, v, w.scale, layout_of(w), rows=rows)
+            assert_matches(o, lse, O2, L2, "bf16", "rank 0 physical")
+
+
+def test_zigzag_varlen_small():
+    z = inputs.zigzag_varlen(seed=2, total=2048, n_seqs=4, len_lo=128, len_hi=1024, cp_size=4, H=4)
+    _zigzag_check(z)
+
+
+def test_zigzag_varlen_full_size_sampled():
+    z = inputs.zigzag_varlen()
+    _zigzag_check(z, rows_per_rank=12)
+
+
+# ---------------------------------------------------------------------------
+# DSA top-k token indices (absorbed MLA: v aliases the first 512 channels of k)
+# ---------------------------------------------------------------------------
+
+def _dsa_run(w, dev_status=None):
+    q, k, v = to_gpu(w)
+    return cpattn_topk_sparse_fwd(q, k, v, w.indices, block_size=1, scale=w.scale,
+                                  causal_offset=w.causal_offset, dev_status=dev_status)
+
+
+def test_dsa_small_with_padding_and_bad_indices():
+    w = inputs.dsa_absorbed(seed=4, Tq=70, Tk=2100, offset=1000, Hq=16, topk=256)
+    idx = w.indices.clone()
+    idx[3, 0, 100:] = -1                 # fewer than topk selected
+    idx[5, 0, :] = -1                    # nothing selected -> (0, -inf)
+    idx[7, 0, 10] = 5000                 # out of range: skipped, flagged
+    idx[8, 0, 11] = idx[8, 0, 12]        # duplicate counts twice
+    idx[9, 0, 20] = 2050                 # in range but after the query: masked again
+    w.indices = idx
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = _dsa_run(w, status)
+    q, k, v = f64(w)
+    O, L, bad = orc.sparse_attention(q, k, v, w.scale, layout_of(w), idx.numpy())
+    assert bad == 1
+    assert int(status.item()) == 6       # CPATTN_ERR_BAD_INDEX
+    assert_matches(o, lse, O, L, "bf16", "dsa small")
+
+
+def test_dsa_full_size_sampled():
+    w = inputs.dsa_absorbed(device="cuda")
+    o, lse = _dsa_run(w)
+    rows = sample_rows(w.Tq, 10, edges=(4095,))
+    q, k, v = f64(w)
+    O, L, _ = orc.sparse_attention(q, k, v, w.scale, layout_of(w), w.indices.numpy(), rows=rows)
+    assert_matches(o[rows.tolist()], lse[rows.tolist()], O, L, "bf16", "dsa full")
+
+
+# ---------------------------------------------------------------------------
+# MoBA block gate + block-sparse attention
+# ---------------------------------------------------------------------------
+
+def _moba_gpu(w):
+    q, k, v = to_gpu(w)
+    sel = cpattn_block_gate(q, k, w.block_size, w.topk, causal_offset=w.causal_offset)
+    o, lse = cpattn_topk_sparse_fwd(q, k, v, sel, block_size=w.block_size, scale=w.scale,
+                                    causal_offset=w.causal_offset)
+    return sel, o, lse
+
+
+def test_moba_small():
+    w = inputs.moba(seed=5, Tq=700, Tk=4096, offset=3300, H=4, block_size=256, topk=3)
+    sel, o, lse = _moba_gpu(w)
+    q, k, v = f64(w)
+    lay = layout_of(w)
+    ref_sel = orc.moba_block_gate(q, k, lay.qpos, w.block_size, w.topk)
+    np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)
+    O, L = orc.moba_attention(q, k, v, w.scale, lay, ref_sel, w.block_size)
+    assert_matches(o, lse, O, L, "bf16", "moba small")
+
+
+def test_moba_gate_ties_and_few_candidates():
+    w = inputs.moba(seed=6, Tq=64, Tk=2048, offset=0, H=2, block_size=128, topk=3)
+    k = w.k.clone()
+    k[5 * 128:6 * 128] = k[2 * 128:3 * 128]        # blocks 2 and 5 have equal means
+    k[9 * 128:10 * 128] = k[2 * 128:3 * 128]       # and block 9
+    w.k = k
+    w.causal_offset = 2048 - 64                    # own block 15; candidates 0..14
+    q = w.q.clone()
+    q[:] = (k[2 * 128:3 * 128].float().mean(0) * 50).to(torch.bfloat16)  # favour the tied blocks
+    w.q = q
+    sel, o, lse = _moba_gpu(w)
+    qq, kk, _ = f64(w)
+    ref = orc.moba_block_gate(qq, kk, layout_of(w).qpos, w.block_size, w.topk)
+    np.testing.assert_array_equal(sel.cpu().numpy(), ref)
+    assert (ref[:, :, :3] == [2, 5, 9]).all()
+    # a query in block 1 has one candidate: [0, 1, -1, -1]
+    w2 = inputs.moba(seed=7, Tq=8, Tk=1024, offset=130, H=2, block_size=128, topk=3)
+    sel2, _, _ = _moba_gpu(w2)
+    assert sel2[0, 0].tolist() == [0, 1, -1, -1]
+
+
+def test_moba_full_size():
+    w = inputs.moba()
+    sel, o, lse = _moba_gpu(w)
+    q, k, v = f64(w)
+    lay = layout_of(w)
+    ref_sel = orc.moba_block_gate(q, k, lay.qpos, w.block_size, w.topk)
+    np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)   # every (query, head), bit-exact
+    rows = sample_rows(w.Tq, 24, edges=(511, 512, 8191))
+    O, L, _ = orc.sparse_attention(q, k, v, w.scale, lay, ref_sel, w.block_size, rows=rows)
+    assert_matches(o[rows.tolist()], lse[rows.tolist()], O, L, "bf16", "moba full")
+
+
+# ---------------------------------------------------------------------------
+# lse_merge on its own
+# ---------------------------------------------------------------------------
+
+def test_lse_merge_neutral_parts():
+    d = torch.device("cuda")
+    rng = np.random.default_rng(8)
+    po = rng.standard_normal((3, 37, 5, 64))
+    pl = rng.standard_normal((3, 37, 5)) * 3
+    pl[1, :10] = -np.inf
+    pl[:, 20] = -np.inf                           # every part neutral for row 20
+    po[np.isneginf(pl)] = 0
+    O, L = orc.lse_merge(po, pl)
+    o, lse = cpattn_lse_merge(torch.tensor(po, dtype=torch.float32, device=d),
+                              torch.tensor(pl, dtype=torch.float32, device=d),
+                              out_dtype=torch.float32)
+    assert_matches(o, lse, O, L, "fp32", "lse_merge")
+    assert (o[20] == 0).all() and torch.isneginf(lse[20]).all()

@@ -115,7 +115,7 @@ cpattn_status cpattn_chunk_fwd(const cpattn_attn_args* a, void* workspace, size_
   (void)workspace_bytes;
   TRY(check_attn(a, true, true));
   CHECK(a->kv_chunk_len >= 0, CPATTN_ERR_INVALID_ARG, "kv_chunk_len=%d must be >= 0", a->kv_chunk_len);
-  if (a->kv_chunk_len > 0)
+  if (a->kv_chunk_len > 0 && a->Tk > 0 && (int64_t)a->Tq * a->Hq > 0)
     CHECK(a->partial_o != nullptr && a->partial_lse != nullptr, CPATTN_ERR_INVALID_ARG,
           "kv_chunk_len > 0 needs partial_o and partial_lse");
   SparseArgs none{nullptr, 0, 1, 1};

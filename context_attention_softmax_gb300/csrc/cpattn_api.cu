@@ -118,9 +118,14 @@ cpattn_status cpattn_chunk_fwd(const cpattn_attn_args* a, void* workspace, size_
   if (a->kv_chunk_len > 0 && a->Tk > 0 && (int64_t)a->Tq * a->Hq > 0)
     CHECK(a->partial_o != nullptr && a->partial_lse != nullptr, CPATTN_ERR_INVALID_ARG,
           "kv_chunk_len > 0 needs partial_o and partial_lse");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dense_tc_supported(*a)) {
+    bool launched = false;
+    cudaError_t e = launch_dense_tc(*a, st, &launched);
+    if (e != cudaSuccess || launched) return cuda_status(e, "cpattn_chunk_fwd tensor-core launch");
+  }
   SparseArgs none{nullptr, 0, 1, 1};
-  return cuda_status(launch_rowwise(*a, kDense, none, reinterpret_cast<cudaStream_t>(stream)),
-                     "cpattn_chunk_fwd launch");
+  return cuda_status(launch_rowwise(*a, kDense, none, st), "cpattn_chunk_fwd launch");
 }
 
 cpattn_status cpattn_lse_merge(int32_t n_parts, const float* part_o, const float* part_lse,

@@ -27,6 +27,11 @@ cudaError_t launch_lse_merge(int32_t n_parts, const float* part_o, const float* 
                              int32_t Tq, int32_t H, int32_t Dv, void* o, int32_t o_dtype,
                              int64_t o_stride_t, int64_t o_stride_h, float* lse,
                              cudaStream_t stream);
+// tcgen05 dense kernel (bf16, d = 128): supported() says whether the
+// arguments fit it; launch sets *launched = false when the layout cannot be
+// described by TMA tensor maps (the caller then uses the general kernel).
+bool dense_tc_supported(const cpattn_attn_args& a);
+cudaError_t launch_dense_tc(const cpattn_attn_args& a, cudaStream_t stream, bool* launched);
 size_t block_gate_workspace(const cpattn_attn_args& a, int32_t block_size);
 size_t block_gate_smem(int n_blocks, int D);
 cudaError_t launch_block_gate(const cpattn_attn_args& a, int32_t block_size, int32_t topk,

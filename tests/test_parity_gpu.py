@@ -55,6 +55,9 @@ def test_tiny_fp32_two_summaries_then_merge():
     (300, 1000, 700, 4, 2, 256),     # ragged tails on both sides
     (257, 1300, 700, 4, 1, 256),     # keys 1000.. never permitted: chunk 4 is neutral
     (128, 640, 0, 2, 2, 0),          # offset 0: the first query sees one key
+    (300, 1000, 700, 4, 2, 0),       # single pass (tensor-core path), ragged tails
+    (257, 1300, 700, 4, 1, 0),
+    (1, 129, 128, 1, 1, 0),          # one query, one key past a tile edge
 ])
 def test_dense_gqa_small(Tq, Tk, off, Hq, Hkv, kvc):
     rng_w = inputs.dense_gqa(seed=1, global_seq=Tq, cp_size=1, rank=0, Hq=Hq, Hkv=Hkv, Tk=Tk,
@@ -85,6 +88,18 @@ def test_dense_gqa_full_size_sampled():
     o4, l4, po, pl = _chunk(w, kv_chunk_len=w.kv_chunk_len)
     assert torch.isneginf(pl[3]).all()          # chunk 3 (keys 6144..) is fully masked
     assert_matches(o4[rows.tolist()], l4[rows.tolist()], O, L, "bf16", "cfg 4 chunks")
+
+
+@pytest.mark.parametrize("factor", [3.0, 8.0])
+def test_dense_large_logits_rescale(factor):
+    # score spread of tens of units: the running max grows by more than 2^8
+    # between tiles, so the accumulator is rescaled mid-row
+    w = inputs.dense_gqa(seed=9, global_seq=512, cp_size=2, rank=1, Hq=2, Hkv=1, Tk=1536,
+                         factor=factor, kv_chunks=0)
+    q, k, v = f64(w)
+    O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w))
+    o, lse = _chunk(w)
+    assert_matches(o, lse, O, L, "bf16", f"factor {factor}")
 
 
 def test_noncausal_and_queries_outside_sequences():

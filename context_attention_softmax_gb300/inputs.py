@@ -88,7 +88,7 @@ def tiny_fp32(seed=0, Tq=128, Tk=256, D=64, offset=128, kv_chunk_len=128):
 
 
 def dense_gqa(seed=0, global_seq=8192, cp_size=4, rank=2, Hq=16, Hkv=4, D=128,
-              factor=0.5, kv_chunks=4, Tk=None):
+              factor=0.5, kv_chunks=4, Tk=None, v_factor=None):
     """Dense causal CP chunk, GQA, bf16: rank ``rank`` of ``cp_size``.
 
     Default: 2048 queries at causal_offset 4096 against 8192 keys, 16 query
@@ -100,7 +100,7 @@ def dense_gqa(seed=0, global_seq=8192, cp_size=4, rank=2, Hq=16, Hkv=4, D=128,
     Tk = global_seq if Tk is None else Tk
     q = _draw(rng, (local, Hq, D), factor)
     k = _draw(rng, (Tk, Hkv, D), factor)
-    v = _draw(rng, (Tk, Hkv, D), factor)
+    v = _draw(rng, (Tk, Hkv, D), factor if v_factor is None else v_factor)
     return Workload(f"dense_causal_gqa_{local}x{Tk}_h{Hq}/{Hkv}_d{D}", "bf16",
                     to_device_dtype(q, "bf16"), to_device_dtype(k, "bf16"),
                     to_device_dtype(v, "bf16"), scale=1.0 / np.sqrt(D), causal=True,

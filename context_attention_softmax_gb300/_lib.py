@@ -32,6 +32,7 @@ EXPORTS = (
     "cpattn_lse_merge",
     "cpattn_topk_sparse_fwd",
     "cpattn_block_gate",
+    "cpattn_block_gate_static",
     "cpattn_workspace_size",
     "cpattn_last_error",
     "cpattn_version",
@@ -84,10 +85,11 @@ def load(path: str = LIB_PATH):
                                      c_i64, c_p, c_p]
     lib.cpattn_topk_sparse_fwd.argtypes = [P, c_p, c_i32, c_i32, c_i32, c_p, ctypes.c_size_t, c_p]
     lib.cpattn_block_gate.argtypes = [P, c_i32, c_i32, c_p, c_p, ctypes.c_size_t, c_p]
+    lib.cpattn_block_gate_static.argtypes = [P, c_i32, c_i32, c_p, c_p]
     lib.cpattn_workspace_size.argtypes = [c_i32, P, c_i32, c_i32]
     lib.cpattn_workspace_size.restype = ctypes.c_size_t
     for name in ("cpattn_chunk_fwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd",
-                 "cpattn_block_gate"):
+                 "cpattn_block_gate", "cpattn_block_gate_static"):
         getattr(lib, name).restype = c_i32
     lib.cpattn_last_error.argtypes = []
     lib.cpattn_last_error.restype = ctypes.c_char_p

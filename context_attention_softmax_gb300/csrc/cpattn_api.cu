@@ -103,6 +103,12 @@ cpattn_status check_attn(const cpattn_attn_args* a, bool need_v, bool need_o) {
 }
 
 }  // namespace
+
+cpattn_status report_error(cpattn_status s, const char* msg) {
+  g_last_error = msg;
+  return s;
+}
+
 }  // namespace cpattn
 
 using namespace cpattn;

@@ -20,6 +20,9 @@ struct SparseArgs {
   int32_t block_size;
 };
 
+// Sets the calling thread's cpattn_last_error() message and returns s.
+cpattn_status report_error(cpattn_status s, const char* msg);
+
 // Launchers return the cudaError_t of the launch (no synchronisation).
 cudaError_t launch_rowwise(const cpattn_attn_args& a, KeyMode mode, const SparseArgs& sp,
                            cudaStream_t stream);

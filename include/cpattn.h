@@ -207,6 +207,31 @@ cpattn_status cpattn_block_gate(const cpattn_attn_args* args, int32_t block_size
                                 int32_t* sel, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/*
+ * cpattn_block_gate_static - cpattn_block_gate for callers that cannot
+ * allocate device memory.  The pages have no counterpart; this is a
+ * deployment convenience of this library.
+ * Some callers cannot call cudaMalloc or grow a memory pool when they make
+ * this call: a plugin handed only its input and output buffers, code running
+ * inside a host callback, or a runtime that owns every allocation.  This
+ * variant takes no workspace: the block means live in a fixed 8 MiB array
+ * compiled into the library, which every GPU that loads the library holds
+ * until the process exits.  Arguments, output and selection are those of
+ * cpattn_block_gate.  The call allocates nothing.
+ * Limits and behaviour:
+ *   - shapes whose workspace (cpattn_workspace_size(CPATTN_OP_BLOCK_GATE,
+ *     ...)) exceeds 8 MiB are rejected with CPATTN_ERR_UNSUPPORTED and a
+ *     message; nothing is launched;
+ *   - the first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture;
+ *   - every call on a device shares the array and it keeps the last call's
+ *     contents (each call rewrites all it reads, so nothing needs clearing);
+ *     calls whose work overlaps on the GPU race - keep them in stream order.
+ */
+cpattn_status cpattn_block_gate_static(const cpattn_attn_args* args, int32_t block_size,
+                                       int32_t topk, int32_t* sel, void* stream);
+
 /* Bytes of device workspace the call needs (0 if none).  `args` supplies the
  * shapes; topk and block_size as passed to the call. */
 size_t cpattn_workspace_size(int32_t op, const cpattn_attn_args* args, int32_t topk,

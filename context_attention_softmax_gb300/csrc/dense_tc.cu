@@ -262,7 +262,10 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ softmax + epilogue
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in exp2 units
-    float m2 = -CUDART_INF_F, l = 0.f;
+    // l: fp32 sum of the weights (for LSE); lb: sum of the same weights as
+    // rounded to bf16 for the PV product, so O = z / lb is a consistent
+    // weighted average of V.
+    float m2 = -CUDART_INF_F, l = 0.f, lb = 0.f;
     int jt = 0;
     bool ok = true;
     for (int kt = 0; kt < p.n_ktiles; ++kt) {
@@ -311,7 +314,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       const float mref = (m2 == -CUDART_INF_F) ? 0.f : m2;
-      float rs = 0.f;
+      float rs = 0.f, rsb = 0.f;
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
@@ -319,8 +322,10 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float p1 = exp2f(sv[2 * c + 1] - mref);
         rs += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
+        rsb += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
       }
       l = l * alpha + rs;
+      lb = lb * alpha + rsb;
       // O and the P buffer are free once the previous tile's PV has finished.
       if (jt > 0) {
         ok = __all_sync(kFullMask, mbar_wait(&s.o_ready, (jt - 1) & 1, abort_flag));
@@ -360,7 +365,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // epilogue: O = z / l, LSE = m + ln l (natural log); no key -> (0, -inf)
     const int64_t tok = (int64_t)q0 + r;
     const bool live = ok && jt > 0 && l > 0.f;
-    const float inv = live ? 1.f / l : 0.f;
+    const float inv = (live && lb > 0.f) ? 1.f / lb : 0.f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + tok * a.o_stride_t + (int64_t)h * a.o_stride_h;
 #pragma unroll
     for (int c4 = 0; c4 < HD / 32; ++c4) {

@@ -1,27 +1,44 @@
-// Dense CP-chunk attention on the 5th-generation tensor cores (sm_103a):
-// TMA loads Q/K/V tiles into 128-byte-swizzled shared memory, one thread
-// issues tcgen05.mma (bf16 x bf16 -> fp32 in tensor memory), four softmax
-// warps read S from TMEM, apply the permitted relation, and fold each KV
-// tile into the running summary (m, l, z) of "Context parallel attention:
-// exchange keys and merge softmax globally" para 3 - z lives in TMEM as the
-// PV accumulator, m and l in registers, one query row per thread.
+// Dense CP-chunk attention on the 5th-generation tensor cores (sm_103a).
 //
-// Tile: 128 queries (one head) x 128 keys x d 128.  Roles per CTA (192
-// threads): warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner), warps
-// 2-5 softmax + epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// TMA loads Q/K/V tiles into 128-byte-swizzled shared memory; one thread
+// issues tcgen05.mma (bf16 x bf16 -> fp32 accumulators in tensor memory);
+// softmax warps read S from TMEM, apply the permitted relation and fold each
+// KV tile into the running summary (m, l, z) of "Context parallel attention:
+// exchange keys and merge softmax globally" para 3: z is the PV accumulator
+// in TMEM, m and l live in registers, one query row per thread.
 //
-// Per KV tile j:  S_j = Q K_j^T (TMEM buffer j%2) -> softmax_j writes P_j
-// (bf16) to shared memory -> O += P_j V_j.  S_{j+1} runs on the tensor core
-// while softmax_j runs.  The running max is refreshed lazily: O is rescaled
-// only when a row's max grows by more than 2^8 (in exp2 units), otherwise
-// the stale max is kept (values stay <= 256, exact in the final division).
+// Each CTA owns two 128-row blocks A and B that read the same KV head: two
+// query heads of one GQA group at the same query tile, or (one KV head per
+// query head) two adjacent query tiles of one head.  The blocks ping-pong on
+// the tensor core so that each softmax warpgroup has the other block's MMAs
+// to hide behind:
 //
-// Masking ("... merge softmax globally" para 1-2, para 5): a row's permitted
-// keys are one interval of logical positions; KV tiles never straddle a
-// chunk of the chunk map (chunk_len % 128 == 0), so a tile's keys are
-// contiguous logical positions and the mask of a row is two column bounds.
-// Tiles outside every row's interval are skipped by all roles alike, so an
-// all-masked chunk costs nothing and leaves the neutral summary.
+//   tensor core:  S_A(j) S_B(j) | PV_A(j) S_A(j+1) | PV_B(j) S_B(j+1) | ...
+//   softmax A:           [ softmax A(j) ]            [ softmax A(j+1) ]
+//   softmax B:                     [ softmax B(j) ]           ...
+//
+// TMEM (512 columns): S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
+// P_X (bf16, two per column) is written back over the first 64 columns of
+// S_X and read from there by the PV MMA (A operand in tensor memory).  MMAs
+// from one thread execute in issue order, so S_X(j+1), issued after PV_X(j),
+// never overwrites P_X(j) early, and its commit also certifies that PV_X(j)
+// has finished before softmax X(j+1) touches O_X.
+//
+// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer + TMEM owner,
+// warps 4-7 softmax of block A, warps 8-11 softmax of block B (warp w reads
+// TMEM lanes 32*(w%4) .. +31); warps 2-3 idle.
+//
+// Softmax per score: one FFMA (scale and subtract the row max, in exp2
+// units) and one ex2.  The row max is refreshed lazily: O is rescaled only
+// when it grows by more than 2^8.  l sums the fp32 weights (for LSE); lb sums
+// the same weights rounded to bf16, as they enter the PV product, so O = z/lb
+// is a consistent weighted average of V.
+//
+// Masking ("... merge softmax globally" para 1-2, 5): a row's permitted keys
+// are one interval of logical positions; KV tiles never straddle a chunk of
+// the chunk map (chunk_len % 128 == 0), so the mask of a row in a tile is two
+// column bounds.  Tiles outside every row's interval are skipped by all
+// roles, so an all-masked chunk costs nothing and stays neutral.
 //
 // Every wait is bounded (2 s).  On expiry the CTA raises an abort flag, all
 // roles stop, in-flight TMA and MMA work is drained with bounded waits, TMEM
@@ -42,29 +59,28 @@ using namespace sm100;
 
 constexpr int BM = 128, BN = 128, HD = 128;
 constexpr int NS = 2;                          // K and V pipeline stages
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = BN * HD * 2;   // 32 KiB
 constexpr uint32_t kHalf = 16384;              // one 64-column swizzled box
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColO = 256;    // S double buffer at 0 / 128, O at 256
+constexpr uint32_t kColS = 0, kColO = 256;     // S_X at 128*X, O_X at 256 + 128*X
 constexpr float kRescaleThreshold = 8.f;       // log2 units
 
 struct TcParams {
   cpattn_attn_args a;
   int n_qtiles;
   int n_ktiles;
+  int head_pairs;   // 1: blocks are two heads of a GQA group; 0: two query tiles
+  int n_units;      // CTAs
 };
 
 struct Smem {
-  uint8_t q[kTileBytes];
+  uint8_t q[2][kTileBytes];
   uint8_t k[NS][kTileBytes];
   uint8_t v[NS][kTileBytes];
-  uint8_t p[kTileBytes];
   uint64_t q_full;
   uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
-  uint64_t s_full[2];
-  uint64_t p_full;
-  uint64_t o_ready;
+  uint64_t s_full[2], p_full[2], o_ready[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -94,6 +110,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&t);
 }
 
+// (head, first query row) of block X of unit u.
+struct Block {
+  int head, q0;
+};
+__device__ __forceinline__ Block block_of(const TcParams& p, int u, int X) {
+  const int Hq = p.a.Hq;
+  if (p.head_pairs) {
+    const int hp = Hq / 2;
+    const int qt = p.n_qtiles - 1 - u / hp;   // later query tiles (more keys) first
+    return Block{2 * (u % hp) + X, qt * BM};
+  }
+  const int n_pair = (p.n_qtiles + 1) / 2;
+  const int pi = n_pair - 1 - u / Hq;
+  return Block{u % Hq, (2 * pi + X) * BM};
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -102,11 +134,9 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                      ~uintptr_t(1023));
   const cpattn_attn_args& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA -> (query tile, head); later query tiles (more keys) are launched first.
-  const int qt = p.n_qtiles - 1 - (int)(blockIdx.x / a.Hq);
-  const int h = (int)(blockIdx.x % a.Hq);
-  const int g = h / (a.Hq / a.Hkv);
-  const int q0 = qt * BM;
+  const int u = blockIdx.x;
+  const Block blk[2] = {block_of(p, u, 0), block_of(p, u, 1)};
+  const int g = blk[0].head / (a.Hq / a.Hkv);
   volatile int* abort_flag = &s.abort;
 
   if (threadIdx.x == 0) {
@@ -117,10 +147,11 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_empty[i], 1);
     }
-    mbar_init(&s.s_full[0], 1);
-    mbar_init(&s.s_full[1], 1);
-    mbar_init(&s.p_full, 128);
-    mbar_init(&s.o_ready, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s.s_full[x], 1);
+      mbar_init(&s.p_full[x], 128);
+      mbar_init(&s.o_ready[x], 1);
+    }
     mbar_init(&s.drain, 1);
     s.abort = 0;
     s.min_lo = LLONG_MAX;
@@ -141,12 +172,13 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
-  // Each softmax thread owns one query row: its permitted key interval.
-  const bool softmax_role = warp >= 2;
+  // Softmax threads: block X = (warp - 4) / 4, row r = lane of TMEM.
+  const bool softmax_role = warp >= 4;
+  const int X = softmax_role ? (warp - 4) >> 2 : 0;
   const int r = (warp & 3) * 32 + lane;
   KeyInterval iv{1, 0};
   if (softmax_role) {
-    const int64_t tok = (int64_t)q0 + r;
+    const int64_t tok = (int64_t)blk[X].q0 + r;
     if (tok < a.Tq) iv = allowed_interval(a, query_pos(a, tok));
     if (iv.lo <= iv.hi) {
       atomicMin(&s.min_lo, (long long)iv.lo);
@@ -163,20 +195,27 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     kbase = logical_pos(a.kv_chunk_map, a.chunk_len, j0);
     return min_lo <= max_hi && kbase <= max_hi && kbase + kvalid - 1 >= min_lo;
   };
+  auto next_live = [&](int kt) -> int {   // first live tile index >= kt, or n_ktiles
+    for (; kt < p.n_ktiles; ++kt) {
+      int64_t kb;
+      int kv;
+      if (tile_info(kt, kb, kv)) break;
+    }
+    return kt;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
       bool q_issued = false;
-      for (int kt = 0; kt < p.n_ktiles; ++kt) {
-        int64_t kbase;
-        int kvalid;
-        if (!tile_info(kt, kbase, kvalid)) continue;
+      for (int kt = next_live(0); kt < p.n_ktiles; kt = next_live(kt + 1)) {
         if (!q_issued) {
-          mbar_arrive_expect_tx(&s.q_full, kTileBytes);
-          tma_load_3d(s.q, &tm_q, &s.q_full, 0, h, q0);
-          tma_load_3d(s.q + kHalf, &tm_q, &s.q_full, 64, h, q0);
+          mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
+          for (int x = 0; x < 2; ++x) {
+            tma_load_3d(s.q[x], &tm_q, &s.q_full, 0, blk[x].head, blk[x].q0);
+            tma_load_3d(s.q[x] + kHalf, &tm_q, &s.q_full, 64, blk[x].head, blk[x].q0);
+          }
           q_issued = true;
         }
         const int jt = k_issued, st = jt % NS;
@@ -205,110 +244,113 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);   // Q, K both K-major
-      const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);   // P K-major, V MN-major
-      const uint32_t q_addr = smem_u32(s.q), p_addr = smem_u32(s.p);
-      bool ok = true, q_ready = false;
-      int jt = 0;
-      auto issue_pv = [&](int j) -> bool {
-        const int st = j % NS;
-        const uint32_t ph = (j / NS) & 1;
-        if (!mbar_wait(&s.v_full[st], ph, abort_flag)) return false;
-        if (!mbar_wait(&s.p_full, j & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(s.v[st]);
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint64_t ad = smem_desc(p_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(v_addr + k * 2048, kHalf, 1024, kSwizzle128B);
-          umma_bf16_ss(tmem + kColO, ad, bd, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-        }
-        umma_commit(&s.v_empty[st]);
-        umma_commit(&s.o_ready);
-        return true;
-      };
-      for (int kt = 0; kt < p.n_ktiles && ok; ++kt) {
-        int64_t kbase;
-        int kvalid;
-        if (!tile_info(kt, kbase, kvalid)) continue;
-        if (!q_ready) {
-          if (!mbar_wait(&s.q_full, 0, abort_flag)) { ok = false; break; }
-          q_ready = true;
-        }
-        const int st = jt % NS;
-        const uint32_t ph = (jt / NS) & 1;
-        if (!mbar_wait(&s.k_full[st], ph, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(s.k[st]);
-        const uint32_t d = tmem + kColS0 + (uint32_t)(jt & 1) * BN;
+      const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);   // P (TMEM), V MN-major
+      int n = 0;
+      for (int kt = next_live(0); kt < p.n_ktiles; kt = next_live(kt + 1)) ++n;
+      bool ok = true;
+      auto issue_s = [&](int j, int x) {   // S_x(j) = Q_x K_j^T
+        const uint32_t q_addr = smem_u32(s.q[x]), k_addr = smem_u32(s.k[j % NS]);
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-          const uint64_t ad = smem_desc(q_addr + off, 16, 1024, kSwizzle128B);
-          const uint64_t bd = smem_desc(k_addr + off, 16, 1024, kSwizzle128B);
-          umma_bf16_ss(d, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+          umma_bf16_ss(tmem + kColS + x * BN, smem_desc(q_addr + off, 16, 1024, kSwizzle128B),
+                       smem_desc(k_addr + off, 16, 1024, kSwizzle128B), idesc_qk, k > 0 ? 1u : 0u);
         }
-        umma_commit(&s.s_full[jt & 1]);
-        umma_commit(&s.k_empty[st]);
-        if (jt >= 1 && !issue_pv(jt - 1)) { ok = false; break; }
-        ++jt;
+        umma_commit(&s.s_full[x]);
+      };
+      auto issue_pv = [&](int j, int x) {  // O_x += P_x(j) V_j
+        const uint32_t v_addr = smem_u32(s.v[j % NS]);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          umma_bf16_ts(tmem + kColO + x * HD, tmem + kColS + x * BN + k * 8,
+                       smem_desc(v_addr + k * 2048, kHalf, 1024, kSwizzle128B), idesc_pv,
+                       (j > 0 || k > 0) ? 1u : 0u);
+      };
+      if (n > 0) {
+        ok = mbar_wait(&s.q_full, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+          issue_s(0, 1);
+          umma_commit(&s.k_empty[0]);
+        }
       }
-      if (ok && jt >= 1) issue_pv(jt - 1);
+      for (int jt = 0; jt < n && ok; ++jt) {
+        const int st = jt % NS;
+        const bool more = jt + 1 < n;
+        const int st1 = (jt + 1) % NS;
+        // block A: PV_A(jt), then S_A(jt+1)
+        if (!mbar_wait(&s.v_full[st], (jt / NS) & 1, abort_flag) ||
+            !mbar_wait(&s.p_full[0], jt & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv(jt, 0);
+        if (!more) umma_commit(&s.o_ready[0]);
+        if (more) {
+          if (!mbar_wait(&s.k_full[st1], ((jt + 1) / NS) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(jt + 1, 0);
+        }
+        // block B: PV_B(jt), then S_B(jt+1)
+        if (!mbar_wait(&s.p_full[1], jt & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv(jt, 1);
+        umma_commit(&s.v_empty[st]);
+        if (!more) umma_commit(&s.o_ready[1]);
+        if (more) {
+          issue_s(jt + 1, 1);
+          umma_commit(&s.k_empty[st1]);
+        }
+      }
       // every MMA issued so far must finish before TMEM is released
       umma_commit(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }
-  } else {
+  } else if (softmax_role) {
     // ------------------------------------------------------------ softmax + epilogue
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_col = tmem + lane_base + kColS + X * BN;
+    const uint32_t o_col = tmem + lane_base + kColO + X * HD;
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in exp2 units
-    // l: fp32 sum of the weights (for LSE); lb: sum of the same weights as
-    // rounded to bf16 for the PV product, so O = z / lb is a consistent
-    // weighted average of V.
     float m2 = -CUDART_INF_F, l = 0.f, lb = 0.f;
     int jt = 0;
     bool ok = true;
-    for (int kt = 0; kt < p.n_ktiles; ++kt) {
+    for (int kt = next_live(0); kt < p.n_ktiles; kt = next_live(kt + 1)) {
       int64_t kbase;
       int kvalid;
-      if (!tile_info(kt, kbase, kvalid)) continue;
+      tile_info(kt, kbase, kvalid);
       int lo_c = 1, hi_c = 0;   // permitted columns of this row in this tile
       if (iv.lo <= iv.hi) {
         lo_c = (int)max((int64_t)0, min((int64_t)BN, iv.lo - kbase));
         hi_c = (int)max((int64_t)-1, min((int64_t)kvalid - 1, iv.hi - kbase));
       }
-      ok = __all_sync(kFullMask, mbar_wait(&s.s_full[jt & 1], (jt >> 1) & 1, abort_flag));
+      ok = __all_sync(kFullMask, mbar_wait(&s.s_full[X], jt & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
       float sv[BN];
 #pragma unroll
       for (int c4 = 0; c4 < BN / 32; ++c4) {
         uint32_t rr[32];
-        tmem_ld32_sync(tmem + lane_base + kColS0 + (uint32_t)(jt & 1) * BN + c4 * 32, rr);
+        tmem_ld32_sync(s_col + c4 * 32, rr);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[c4 * 32 + i] = __uint_as_float(rr[i]);
       }
-      float mx = -CUDART_INF_F;
-      if (lo_c == 0 && hi_c == BN - 1) {
+      if (!(lo_c == 0 && hi_c == BN - 1)) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          sv[c] *= sl2;
-          mx = fmaxf(mx, sv[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          sv[c] = (c >= lo_c && c <= hi_c) ? sv[c] * sl2 : -CUDART_INF_F;
-          mx = fmaxf(mx, sv[c]);
-        }
+        for (int c = 0; c < BN; ++c)
+          if (c < lo_c || c > hi_c) sv[c] = -CUDART_INF_F;
       }
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, sv[c]);
+      mx *= sl2;
       float alpha = 1.f;
       bool rescale = false;
       if (mx > m2) {
         if (m2 == -CUDART_INF_F) {
           m2 = mx;                      // nothing accumulated yet for this row
         } else if (mx > m2 + kRescaleThreshold) {
-          alpha = exp2f(m2 - mx);
+          alpha = ex2_approx(m2 - mx);
           m2 = mx;
           rescale = true;
         }
@@ -318,52 +360,48 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = exp2f(sv[2 * c] - mref);
-        const float p1 = exp2f(sv[2 * c + 1] - mref);
+        const float p0 = ex2_approx(fmaf(sv[2 * c], sl2, -mref));
+        const float p1 = ex2_approx(fmaf(sv[2 * c + 1], sl2, -mref));
         rs += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
         rsb += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
       }
       l = l * alpha + rs;
       lb = lb * alpha + rsb;
-      // O and the P buffer are free once the previous tile's PV has finished.
-      if (jt > 0) {
-        ok = __all_sync(kFullMask, mbar_wait(&s.o_ready, (jt - 1) & 1, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-      }
+      // PV_X(jt-1) has finished: S_X(jt) was issued after it and has landed.
       if (__any_sync(kFullMask, rescale)) {
 #pragma unroll
         for (int c4 = 0; c4 < HD / 32; ++c4) {
           uint32_t oo[32];
-          const uint32_t addr = tmem + lane_base + kColO + c4 * 32;
-          tmem_ld32_sync(addr, oo);
+          tmem_ld32_sync(o_col + c4 * 32, oo);
 #pragma unroll
           for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
-          tmem_st32(addr, oo);
+          tmem_st32(o_col + c4 * 32, oo);
         }
-        tmem_wait_st();
       }
-      // P row -> shared memory in the 128B-swizzled K-major layout
-      // [key block of 64][row][64 keys]: 16-byte chunk c of row r sits at
-      // chunk position c ^ (r % 8).
+      // P_X over the first 64 columns of S_X: column c holds keys 2c, 2c+1.
+      {
+        uint32_t lo[32], hi[32];
 #pragma unroll
-      for (int ci = 0; ci < BN / 8; ++ci) {
-        const int kb = ci >> 3, c16 = ci & 7;
-        uint4 val = make_uint4(pk[ci * 4], pk[ci * 4 + 1], pk[ci * 4 + 2], pk[ci * 4 + 3]);
-        *reinterpret_cast<uint4*>(s.p + kb * kHalf + r * 128 + ((c16 ^ (r & 7)) << 4)) = val;
+        for (int i = 0; i < 32; ++i) {
+          lo[i] = pk[i];
+          hi[i] = pk[32 + i];
+        }
+        tmem_st32(s_col, lo);
+        tmem_st32(s_col + 32, hi);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&s.p_full);
+      mbar_arrive(&s.p_full[X]);
       ++jt;
     }
     if (ok && jt > 0) {
-      ok = __all_sync(kFullMask, mbar_wait(&s.o_ready, (jt - 1) & 1, abort_flag));
+      ok = __all_sync(kFullMask, mbar_wait(&s.o_ready[X], 0, abort_flag));
       if (ok) tc_fence_after();
     }
-    // epilogue: O = z / l, LSE = m + ln l (natural log); no key -> (0, -inf)
-    const int64_t tok = (int64_t)q0 + r;
+    // epilogue: O = z / lb, LSE = m + ln l (natural log); no key -> (0, -inf)
+    const int64_t tok = (int64_t)blk[X].q0 + r;
+    const int h = blk[X].head;
     const bool live = ok && jt > 0 && l > 0.f;
     const float inv = (live && lb > 0.f) ? 1.f / lb : 0.f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + tok * a.o_stride_t + (int64_t)h * a.o_stride_h;
@@ -371,7 +409,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int c4 = 0; c4 < HD / 32; ++c4) {
       uint32_t oo[32];
       if (ok && jt > 0) {
-        tmem_ld32_sync(tmem + lane_base + kColO + c4 * 32, oo);
+        tmem_ld32_sync(o_col + c4 * 32, oo);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) oo[i] = 0u;
@@ -431,6 +469,7 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int64_t
 bool dense_tc_supported(const cpattn_attn_args& a) {
   if (a.dtype != CPATTN_BF16 || a.Dqk != HD || a.Dv != HD) return false;
   if (a.kv_chunk_len != 0 || a.Tq <= 0 || a.Tk <= 0) return false;
+  if (!(a.scale > 0.f)) return false;   // the row max is taken on unscaled scores
   if ((a.q_chunk_map || a.kv_chunk_map) && a.chunk_len % BN != 0) return false;
   // strides must be positive for the TMA descriptors
   if (a.q_stride_h <= 0 || a.k_stride_h <= 0 || a.v_stride_h <= 0) return false;
@@ -448,11 +487,12 @@ cudaError_t launch_dense_tc(const cpattn_attn_args& a, cudaStream_t stream, bool
   p.a = a;
   p.n_qtiles = (a.Tq + BM - 1) / BM;
   p.n_ktiles = (a.Tk + BN - 1) / BN;
+  p.head_pairs = ((a.Hq / a.Hkv) % 2 == 0) ? 1 : 0;
+  p.n_units = p.head_pairs ? p.n_qtiles * (a.Hq / 2) : ((p.n_qtiles + 1) / 2) * a.Hq;
   cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  const unsigned grid = (unsigned)p.n_qtiles * (unsigned)a.Hq;
-  dense_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  dense_tc_kernel<<<(unsigned)p.n_units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   *launched = true;
   return cudaGetLastError();
 }

@@ -58,13 +58,19 @@ namespace {
 using namespace sm100;
 
 constexpr int BM = 128, BN = 128, HD = 128;
-constexpr int NS = 2;                          // K and V pipeline stages
+constexpr int NS = 2;                          // K and V pipeline stages (j & 1 picks one)
 constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = BN * HD * 2;   // 32 KiB
 constexpr uint32_t kHalf = 16384;              // one 64-column swizzled box
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;     // S_X at 128*X, O_X at 256 + 128*X
 constexpr float kRescaleThreshold = 8.f;       // log2 units
+constexpr int kMaxKTiles = 4096;               // Tk <= 524288 on this path
+// Register split: launch budget 168 x 384.  Warpgroup 0 (producer, MMA, two
+// idle warps) drops to 64 registers per thread, the two softmax warpgroups
+// rise to 216: 128 * 64 + 256 * 216 = 63488 <= 168 * 384 = 64512.
+constexpr uint32_t kRegsControl = 64, kRegsSoftmax = 216;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 168 * kThreads, "register split");
 
 struct TcParams {
   cpattn_attn_args a;
@@ -84,7 +90,9 @@ struct Smem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int n_live;
   long long min_lo, max_hi;
+  uint16_t live_kt[kMaxKTiles];
 };
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
@@ -101,6 +109,16 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// 128 TMEM columns of this warp's 32 lanes in one load, complete on return.
+__device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
       : "r"(taddr)
       : "memory");
 }
@@ -180,36 +198,52 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (softmax_role) {
     const int64_t tok = (int64_t)blk[X].q0 + r;
     if (tok < a.Tq) iv = allowed_interval(a, query_pos(a, tok));
-    if (iv.lo <= iv.hi) {
-      atomicMin(&s.min_lo, (long long)iv.lo);
-      atomicMax(&s.max_hi, (long long)iv.hi);
+    long long lo = iv.lo <= iv.hi ? (long long)iv.lo : LLONG_MAX;
+    long long hi = iv.lo <= iv.hi ? (long long)iv.hi : LLONG_MIN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = min(lo, __shfl_xor_sync(kFullMask, lo, o));
+      hi = max(hi, __shfl_xor_sync(kFullMask, hi, o));
+    }
+    if (lane == 0 && lo <= hi) {
+      atomicMin(&s.min_lo, lo);
+      atomicMax(&s.max_hi, hi);
     }
   }
   __syncthreads();
   const int64_t min_lo = s.min_lo, max_hi = s.max_hi;
 
-  // A KV tile takes part iff its logical key range meets some row's interval.
-  auto tile_info = [&](int kt, int64_t& kbase, int& kvalid) -> bool {
-    const int64_t j0 = (int64_t)kt * BN;
-    kvalid = (int)min((int64_t)BN, (int64_t)a.Tk - j0);
-    kbase = logical_pos(a.kv_chunk_map, a.chunk_len, j0);
-    return min_lo <= max_hi && kbase <= max_hi && kbase + kvalid - 1 >= min_lo;
-  };
-  auto next_live = [&](int kt) -> int {   // first live tile index >= kt, or n_ktiles
-    for (; kt < p.n_ktiles; ++kt) {
-      int64_t kb;
-      int kv;
-      if (tile_info(kt, kb, kv)) break;
+  // Live KV tiles (those whose logical key range meets some row's interval),
+  // listed once by warp 3 for every role.
+  if (warp == 3) {
+    int base = 0;
+    for (int kt0 = 0; kt0 < p.n_ktiles; kt0 += 32) {
+      const int kt = kt0 + lane;
+      bool live = false;
+      if (kt < p.n_ktiles && min_lo <= max_hi) {
+        const int64_t j0 = (int64_t)kt * BN;
+        const int64_t kb = logical_pos(a.kv_chunk_map, a.chunk_len, j0);
+        const int64_t kv = min((int64_t)BN, (int64_t)a.Tk - j0);
+        live = kb <= max_hi && kb + kv - 1 >= min_lo;
+      }
+      const unsigned m = __ballot_sync(kFullMask, live);
+      if (live) s.live_kt[base + __popc(m & ((1u << lane) - 1))] = (uint16_t)kt;
+      base += __popc(m);
     }
-    return kt;
-  };
+    if (lane == 0) s.n_live = base;
+  }
+  __syncthreads();
+  const int n_live = s.n_live;
 
+  if (warp < 4) {
+  regs_dec<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
       bool q_issued = false;
-      for (int kt = next_live(0); kt < p.n_ktiles; kt = next_live(kt + 1)) {
+      for (int i = 0; i < n_live; ++i) {
+        const int kt = s.live_kt[i];
         if (!q_issued) {
           mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
           for (int x = 0; x < 2; ++x) {
@@ -242,51 +276,48 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread issues both blocks' MMAs in the ping-pong order
+    //   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+    // MMAs from one thread execute in issue order.
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);   // Q, K both K-major
       const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);   // P (TMEM), V MN-major
-      int n = 0;
-      for (int kt = next_live(0); kt < p.n_ktiles; kt = next_live(kt + 1)) ++n;
-      bool ok = true;
+      // Descriptor low words: K-major Q and K step 32 B along K inside a
+      // 64-column swizzled box and 16 KiB to the next box; V (MN-major,
+      // leading offset 16 KiB to the next 64 value channels) steps 2 KiB per
+      // 16 keys.
+      const uint32_t q_lo0 = desc_lo(smem_u32(s.q[0]), 16), q_lo1 = desc_lo(smem_u32(s.q[1]), 16);
+      const uint32_t k_lo0 = desc_lo(smem_u32(s.k[0]), 16), k_lo1 = desc_lo(smem_u32(s.k[1]), 16);
+      const uint32_t v_lo0 = desc_lo(smem_u32(s.v[0]), kHalf), v_lo1 = desc_lo(smem_u32(s.v[1]), kHalf);
+      const int n = n_live;
       auto issue_s = [&](int j, int x) {   // S_x(j) = Q_x K_j^T
-        const uint32_t q_addr = smem_u32(s.q[x]), k_addr = smem_u32(s.k[j % NS]);
-#pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
-          const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
-          umma_bf16_ss(tmem + kColS + x * BN, smem_desc(q_addr + off, 16, 1024, kSwizzle128B),
-                       smem_desc(k_addr + off, 16, 1024, kSwizzle128B), idesc_qk, k > 0 ? 1u : 0u);
-        }
+        umma8_ss_kmajor(tmem + kColS + x * BN, x ? q_lo1 : q_lo0, (j & 1) ? k_lo1 : k_lo0, idesc_qk);
         umma_commit(&s.s_full[x]);
       };
       auto issue_pv = [&](int j, int x) {  // O_x += P_x(j) V_j
-        const uint32_t v_addr = smem_u32(s.v[j % NS]);
-#pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          umma_bf16_ts(tmem + kColO + x * HD, tmem + kColS + x * BN + k * 8,
-                       smem_desc(v_addr + k * 2048, kHalf, 1024, kSwizzle128B), idesc_pv,
-                       (j > 0 || k > 0) ? 1u : 0u);
+        const uint32_t d = tmem + kColO + x * HD, pa = tmem + kColS + x * BN;
+        const uint32_t vb = (j & 1) ? v_lo1 : v_lo0;
+        if (j > 0) umma8_ts_mnmajor<1>(d, pa, vb, idesc_pv);
+        else umma8_ts_mnmajor<0>(d, pa, vb, idesc_pv);
       };
-      if (n > 0) {
-        ok = mbar_wait(&s.q_full, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0, 0);
-          issue_s(0, 1);
-          umma_commit(&s.k_empty[0]);
-        }
+      bool ok = n > 0 && mbar_wait(&s.q_full, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(0, 1);
+        umma_commit(&s.k_empty[0]);
       }
       for (int jt = 0; jt < n && ok; ++jt) {
-        const int st = jt % NS;
+        const int st = jt & 1, st1 = (jt + 1) & 1;
         const bool more = jt + 1 < n;
-        const int st1 = (jt + 1) % NS;
         // block A: PV_A(jt), then S_A(jt+1)
-        if (!mbar_wait(&s.v_full[st], (jt / NS) & 1, abort_flag) ||
+        if (!mbar_wait(&s.v_full[st], (jt >> 1) & 1, abort_flag) ||
             !mbar_wait(&s.p_full[0], jt & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         issue_pv(jt, 0);
         if (!more) umma_commit(&s.o_ready[0]);
         if (more) {
-          if (!mbar_wait(&s.k_full[st1], ((jt + 1) / NS) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.k_full[st1], ((jt + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
           issue_s(jt + 1, 0);
         }
@@ -306,7 +337,9 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }
-  } else if (softmax_role) {
+  }
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax + epilogue
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_base + kColS + X * BN;
@@ -315,10 +348,10 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float m2 = -CUDART_INF_F, l = 0.f, lb = 0.f;
     int jt = 0;
     bool ok = true;
-    for (int kt = next_live(0); kt < p.n_ktiles; kt = next_live(kt + 1)) {
-      int64_t kbase;
-      int kvalid;
-      tile_info(kt, kbase, kvalid);
+    for (int i = 0; i < n_live; ++i) {
+      const int kt = s.live_kt[i];
+      const int64_t kbase = logical_pos(a.kv_chunk_map, a.chunk_len, (int64_t)kt * BN);
+      const int kvalid = min(BN, a.Tk - kt * BN);
       int lo_c = 1, hi_c = 0;   // permitted columns of this row in this tile
       if (iv.lo <= iv.hi) {
         lo_c = (int)max((int64_t)0, min((int64_t)BN, iv.lo - kbase));
@@ -328,22 +361,27 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (!ok) break;
       tc_fence_after();
       float sv[BN];
+      {
+        uint32_t rr[BN];
+        tmem_ld128_sync(s_col, rr);
 #pragma unroll
-      for (int c4 = 0; c4 < BN / 32; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32_sync(s_col + c4 * 32, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[c4 * 32 + i] = __uint_as_float(rr[i]);
+        for (int c = 0; c < BN; ++c) sv[c] = __uint_as_float(rr[c]);
       }
       if (!(lo_c == 0 && hi_c == BN - 1)) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
           if (c < lo_c || c > hi_c) sv[c] = -CUDART_INF_F;
       }
-      float mx = sv[0];
+      // row max: four independent chains of 3-input max
+      float pm[4];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, sv[c]);
-      mx *= sl2;
+      for (int i = 0; i < 4; ++i) pm[i] = fmaxf(sv[2 * i], sv[2 * i + 1]);
+#pragma unroll
+      for (int c = 8; c < BN; c += 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pm[i] = fmax3(pm[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
+      }
+      float mx = fmax3(pm[0], pm[1], fmaxf(pm[2], pm[3])) * sl2;
       float alpha = 1.f;
       bool rescale = false;
       if (mx > m2) {
@@ -356,18 +394,32 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
       const float mref = (m2 == -CUDART_INF_F) ? 0.f : m2;
-      float rs = 0.f, rsb = 0.f;
-      uint32_t pk[BN / 2];
+      // p = 2^(s*scale*log2e - m): one packed FFMA per two scores, one ex2 each.
+      // P_X over the first 64 columns of S_X (column c holds keys 2c, 2c+1),
+      // written in two halves as soon as each is packed.
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mref, -mref);
+      uint64_t rs2[2] = {0ull, 0ull}, rsb2[2] = {0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(sv[2 * c], sl2, -mref));
-        const float p1 = ex2_approx(fmaf(sv[2 * c + 1], sl2, -mref));
-        rs += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
-        rsb += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int e = 64 * half + 2 * c;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(sv[e], sv[e + 1]), sl2x2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
+          pk[c] = pack_bf16(p0, p1);
+          rsb2[c & 1] = f2_add(rsb2[c & 1], f2_pack(__uint_as_float(pk[c] << 16),
+                                                     __uint_as_float(pk[c] & 0xffff0000u)));
+        }
+        tmem_st32(s_col + 32 * half, pk);
       }
-      l = l * alpha + rs;
-      lb = lb * alpha + rsb;
+      float a0, a1, b0, b1;
+      f2_unpack(f2_add(rs2[0], rs2[1]), a0, a1);
+      f2_unpack(f2_add(rsb2[0], rsb2[1]), b0, b1);
+      l = l * alpha + (a0 + a1);
+      lb = lb * alpha + (b0 + b1);
       // PV_X(jt-1) has finished: S_X(jt) was issued after it and has landed.
       if (__any_sync(kFullMask, rescale)) {
 #pragma unroll
@@ -378,17 +430,6 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
           tmem_st32(o_col + c4 * 32, oo);
         }
-      }
-      // P_X over the first 64 columns of S_X: column c holds keys 2c, 2c+1.
-      {
-        uint32_t lo[32], hi[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          lo[i] = pk[i];
-          hi[i] = pk[32 + i];
-        }
-        tmem_st32(s_col, lo);
-        tmem_st32(s_col + 32, hi);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -471,6 +512,7 @@ bool dense_tc_supported(const cpattn_attn_args& a) {
   if (a.kv_chunk_len != 0 || a.Tq <= 0 || a.Tk <= 0) return false;
   if (!(a.scale > 0.f)) return false;   // the row max is taken on unscaled scores
   if ((a.q_chunk_map || a.kv_chunk_map) && a.chunk_len % BN != 0) return false;
+  if ((a.Tk + BN - 1) / BN > kMaxKTiles) return false;
   // strides must be positive for the TMA descriptors
   if (a.q_stride_h <= 0 || a.k_stride_h <= 0 || a.v_stride_h <= 0) return false;
   return true;

@@ -182,6 +182,100 @@ __device__ __forceinline__ void umma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, u
       : "memory");
 }
 
+// Split form of a shared-memory descriptor for the issue loop: the high word
+// (stride byte offset 1024, version 1, 128-byte swizzle) is the same for
+// every operand here; the low word carries start address and leading byte
+// offset, so stepping along K is one 32-bit add.
+constexpr uint32_t kDescHiSw128 = (1024u >> 4) | (1u << 14) | (kSwizzle128B << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ void umma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 da, {%1, %5};\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHiSw128));
+}
+__device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHiSw128));
+}
+
+// Eight MMAs along K = 128 (16 per instruction) in one PTX block, both
+// operands K-major in 64-column 128-byte-swizzled boxes: step k reads the
+// descriptors lo + (k / 4) * 1024 + (k % 4) * 2 (16 KiB per box, 32 B per
+// step).  The first MMA overwrites D, the rest accumulate.
+__device__ __forceinline__ void umma8_ss_kmajor(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b32 a<8>, b<8>;\n\t.reg .b64 da<8>, db<8>;\n\t"
+      "add.u32 a0, %1, 0;    add.u32 b0, %2, 0;\n\t"
+      "add.u32 a1, %1, 2;    add.u32 b1, %2, 2;\n\t"
+      "add.u32 a2, %1, 4;    add.u32 b2, %2, 4;\n\t"
+      "add.u32 a3, %1, 6;    add.u32 b3, %2, 6;\n\t"
+      "add.u32 a4, %1, 1024; add.u32 b4, %2, 1024;\n\t"
+      "add.u32 a5, %1, 1026; add.u32 b5, %2, 1026;\n\t"
+      "add.u32 a6, %1, 1028; add.u32 b6, %2, 1028;\n\t"
+      "add.u32 a7, %1, 1030; add.u32 b7, %2, 1030;\n\t"
+      "mov.b64 da0, {a0, %4}; mov.b64 db0, {b0, %4};\n\t"
+      "mov.b64 da1, {a1, %4}; mov.b64 db1, {b1, %4};\n\t"
+      "mov.b64 da2, {a2, %4}; mov.b64 db2, {b2, %4};\n\t"
+      "mov.b64 da3, {a3, %4}; mov.b64 db3, {b3, %4};\n\t"
+      "mov.b64 da4, {a4, %4}; mov.b64 db4, {b4, %4};\n\t"
+      "mov.b64 da5, {a5, %4}; mov.b64 db5, {b5, %4};\n\t"
+      "mov.b64 da6, {a6, %4}; mov.b64 db6, {b6, %4};\n\t"
+      "mov.b64 da7, {a7, %4}; mov.b64 db7, {b7, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da0, db0, %3, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da1, db1, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da2, db2, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da3, db3, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da4, db4, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da5, db5, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da6, db6, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da7, db7, %3, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128));
+}
+
+// Eight MMAs along K = 128 with A (16-bit, M x K) in tensor memory at column
+// a_tmem + 8 k and B MN-major in shared memory, stepping b_lo by 128 (2 KiB,
+// 16 K-rows) per MMA.  acc0 = 0: the first MMA overwrites D.
+template <int ACC0>
+__device__ __forceinline__ void umma8_ts_mnmajor(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                                 uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b32 b<8>, t<8>;\n\t.reg .b64 db<8>;\n\t"
+      "add.u32 b0, %2, 0;   add.u32 t0, %1, 0;\n\t"
+      "add.u32 b1, %2, 128; add.u32 t1, %1, 8;\n\t"
+      "add.u32 b2, %2, 256; add.u32 t2, %1, 16;\n\t"
+      "add.u32 b3, %2, 384; add.u32 t3, %1, 24;\n\t"
+      "add.u32 b4, %2, 512; add.u32 t4, %1, 32;\n\t"
+      "add.u32 b5, %2, 640; add.u32 t5, %1, 40;\n\t"
+      "add.u32 b6, %2, 768; add.u32 t6, %1, 48;\n\t"
+      "add.u32 b7, %2, 896; add.u32 t7, %1, 56;\n\t"
+      "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"
+      "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"
+      "mov.b64 db4, {b4, %4}; mov.b64 db5, {b5, %4};\n\t"
+      "mov.b64 db6, {b6, %4}; mov.b64 db7, {b7, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t4], db4, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t5], db5, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t6], db6, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], db7, %3, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]; A (M x K, 16-bit, two elements per 32-bit
 // column, lane = row) is read from tensor memory.
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
@@ -202,6 +296,31 @@ __device__ __forceinline__ void regs_dec() {
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Packed fp32 pairs (Blackwell f32x2 arithmetic) and the 3-input max.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // Hardware base-2 exponential (PTX ex2.approx.ftz.f32; -inf -> +0).

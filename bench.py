@@ -189,12 +189,15 @@ class MobaRunner:
         nbytes = cpattn_workspace_size(_lib.OP_BLOCK_GATE, self.q, self.k, topk=w.topk,
                                        block_size=w.block_size)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+        nsp = cpattn_workspace_size(_lib.OP_TOPK_SPARSE_FWD, self.q, self.k, self.v, topk=w.topk + 1,
+                                    block_size=w.block_size)
+        self.ws_sparse = torch.empty(max(nsp, 16), dtype=torch.uint8, device=device)
         B = w.block_size
         qpos = w.causal_offset + np.arange(Tq)
         keys = 3 * B + (qpos % B) + 1
         self.flops = 4.0 * D * H * float(keys.sum())
         self.hbm_bytes = (2 * w.k.numel() + 2 * w.q.numel() * 2 + w.v.numel() * 2 + self.o.numel() * 2)
-        self.launches_per_step = 3
+        self.launches_per_step = 7   # gate: 2; attention: count, scan, scatter, attend, merge
         self.bound = "hbm"
         self.config = {"workload": "MoBA gate (top-3 + own of 512-key blocks) + block-sparse "
                                    "attention: 8192 q x 65536 kv, 32 heads, d=128",
@@ -207,7 +210,7 @@ class MobaRunner:
                           sel=self.sel, workspace=self.ws)
         cpattn_topk_sparse_fwd(self.q, self.k, self.v, self.sel, block_size=w.block_size,
                                scale=w.scale, causal_offset=w.causal_offset, out=self.o,
-                               lse=self.lse)
+                               lse=self.lse, workspace=self.ws_sparse)
 
 
 RUNNERS = {"dense_gqa": DenseRunner, "zigzag": ZigzagRunner, "dsa": DsaRunner, "moba": MobaRunner}

@@ -157,8 +157,6 @@ cpattn_status cpattn_lse_merge(int32_t n_parts, const float* part_o, const float
 cpattn_status cpattn_topk_sparse_fwd(const cpattn_attn_args* a, const int32_t* indices,
                                      int32_t topk, int32_t index_heads, int32_t block_size,
                                      void* workspace, size_t workspace_bytes, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   TRY(check_attn(a, true, true));
   CHECK(topk >= 0, CPATTN_ERR_INVALID_ARG, "topk=%d must be >= 0", topk);
   CHECK(index_heads == 1 || index_heads == a->Hq, CPATTN_ERR_INVALID_ARG,
@@ -166,9 +164,16 @@ cpattn_status cpattn_topk_sparse_fwd(const cpattn_attn_args* a, const int32_t* i
   CHECK(block_size >= 1, CPATTN_ERR_INVALID_ARG, "block_size=%d must be >= 1", block_size);
   CHECK(a->kv_chunk_len == 0, CPATTN_ERR_UNSUPPORTED, "partial summaries are not produced by the sparse path");
   if (topk > 0 && a->Tq > 0) CHECK(indices != nullptr, CPATTN_ERR_INVALID_ARG, "indices is NULL");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (block_size > 1 && topk > 0 && moba_tc_supported(*a, index_heads, block_size, topk)) {
+    const size_t need = moba_tc_workspace(*a, topk, block_size);
+    CHECK(workspace != nullptr && workspace_bytes >= need, CPATTN_ERR_WORKSPACE,
+          "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+    return cuda_status(launch_moba_tc(*a, indices, topk, index_heads, block_size, workspace, st),
+                       "cpattn_topk_sparse_fwd block-grouped launch");
+  }
   SparseArgs sp{indices, topk, index_heads, block_size};
-  return cuda_status(launch_rowwise(*a, block_size == 1 ? kTokens : kBlocks, sp,
-                                    reinterpret_cast<cudaStream_t>(stream)),
+  return cuda_status(launch_rowwise(*a, block_size == 1 ? kTokens : kBlocks, sp, st),
                      "cpattn_topk_sparse_fwd launch");
 }
 
@@ -195,9 +200,11 @@ cpattn_status cpattn_block_gate(const cpattn_attn_args* a, int32_t block_size, i
 }
 
 size_t cpattn_workspace_size(int32_t op, const cpattn_attn_args* a, int32_t topk, int32_t block_size) {
-  (void)topk;
   if (a == nullptr) return 0;
-  if (op == CPATTN_OP_BLOCK_GATE) return block_gate_workspace(*a, block_size);
+  if (op == CPATTN_OP_BLOCK_GATE) return block_size > 0 ? block_gate_workspace(*a, block_size) : 0;
+  if (op == CPATTN_OP_TOPK_SPARSE_FWD && block_size > 1 && topk > 0 &&
+      moba_tc_supported(*a, 1, block_size, topk))
+    return moba_tc_workspace(*a, topk, block_size);
   return 0;
 }
 

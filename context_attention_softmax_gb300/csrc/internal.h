@@ -35,6 +35,16 @@ cudaError_t launch_lse_merge(int32_t n_parts, const float* part_o, const float* 
 // described by TMA tensor maps (the caller then uses the general kernel).
 bool dense_tc_supported(const cpattn_attn_args& a);
 cudaError_t launch_dense_tc(const cpattn_attn_args& a, cudaStream_t stream, bool* launched);
+// Block-grouped MoBA attention on the tensor cores (bf16, d = 128, block
+// size a multiple of 128, keys in logical order).  `sel` is the block list
+// [Tq, index_heads, slots]; writes o and lse through partial summaries and
+// the LSE merge.
+bool moba_tc_supported(const cpattn_attn_args& a, int32_t index_heads, int32_t block_size,
+                       int32_t slots);
+size_t moba_tc_workspace(const cpattn_attn_args& a, int32_t slots, int32_t block_size);
+cudaError_t launch_moba_tc(const cpattn_attn_args& a, const int32_t* sel, int32_t slots,
+                           int32_t index_heads, int32_t block_size, void* workspace,
+                           cudaStream_t stream);
 size_t block_gate_workspace(const cpattn_attn_args& a, int32_t block_size);
 size_t block_gate_smem(int n_blocks, int D);
 cudaError_t launch_block_gate(const cpattn_attn_args& a, int32_t block_size, int32_t topk,

@@ -11,10 +11,11 @@
 //     widened to fp64 before the division by B, so the mean is accurate to
 //     far below fp32 rounding.  Both the fp64 mean and its fp32 rounding are
 //     kept in the workspace (the only scratch memory of this path).
-//  2. gate_select_kernel - fp32 gates from the fp32 means, each with a
-//     rigorous error bound e_b = 2 (D + 8) 2^-24 sum_d |q_d| |mu_d|, which
-//     covers the fp32 dot product, the rounding of the mean and the rounding
-//     of the bound itself.  With T = k-th largest lower bound g_b - e_b, the
+//  2. gate_select_kernel - fp32 gates from the fp32 means (a register-tiled
+//     product per head), each with a rigorous error bound
+//     e_b = 2 (D + 8) 2^-24 ||q||_2 ||mu_b||_2 >= 2 (D + 8) 2^-24 sum_d |q_d||mu_d|,
+//     which covers the fp32 dot product, the rounding of the mean and the
+//     rounding of the bound itself.  With T = k-th largest lower bound g_b - e_b, the
 //     set U = {b : g_b + e_b >= T} certainly contains the exact top-k and
 //     everything outside it is certainly out.  |U| == k decides the
 //     selection; otherwise the members of U are re-ranked by fp64 gates
@@ -25,8 +26,6 @@
 namespace cpattn {
 namespace {
 
-constexpr int kGateWarps = 4;
-constexpr int kQueriesPerWarp = 8;
 constexpr int kMaxTopk = 64;
 
 template <typename T>
@@ -59,70 +58,121 @@ __device__ __forceinline__ bool before64(double v1, int b1, double v2, int b2) {
   return v1 > v2 || (v1 == v2 && b1 < b2);
 }
 
+// Gates of 64 queries x all candidate blocks of one head, as a register-tiled
+// fp32 product: 256 threads, each a 4-query x 8-block tile per 128-block
+// chunk, both operands staged transposed in shared memory.  The error bound
+// uses norms: sum_d |q_d||mu_d| <= ||q||_2 ||mu||_2, so
+//   e_b = 2 (D + 8) 2^-24 ||q||_2 ||mu_b||_2
+// bounds |fp32 gate - exact gate| (dot product, rounding of the mean and of
+// the norms included).  Selection then as described at the top of the file.
+constexpr int kGQ = 64;          // queries per CTA
+constexpr int kGB = 128;         // blocks per chunk
+constexpr int kGThreads = 256;
+constexpr int kQPad = kGQ + 4;   // shared row strides (floats), 16-byte aligned
+constexpr int kBPad = kGB + 4;
+
+__host__ __device__ constexpr size_t gate_smem_floats(int n_blocks, int D) {
+  return (size_t)D * kQPad + (size_t)D * kBPad + (size_t)kGQ * (n_blocks + 1) + kGQ + n_blocks;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kGateWarps * 32)
+__global__ void __launch_bounds__(kGThreads, 1)
 gate_select_kernel(const cpattn_attn_args a, int B, int n_blocks, int topk,
                    const double* __restrict__ mu64, const float* __restrict__ mu32,
                    int32_t* __restrict__ sel) {
-  extern __shared__ __align__(16) unsigned char gate_smem[];
+  extern __shared__ __align__(16) float gsm[];
   const int D = a.Dqk;
-  const int ld = D + 1;                                         // padded row: no bank conflicts
-  double* g64_s = reinterpret_cast<double*>(gate_smem);         // [warps][n_blocks]
-  float* mu_s = reinterpret_cast<float*>(g64_s + kGateWarps * n_blocks);  // [n_blocks][D+1]
-  float* q_s = mu_s + (size_t)n_blocks * ld;                    // [warps][D]
-  float* g_s = q_s + kGateWarps * D;                            // [warps][n_blocks]
-  float* e_s = g_s + kGateWarps * n_blocks;                     // [warps][n_blocks]
-  __shared__ int chosen_s[kGateWarps][kMaxTopk + 1];
+  float* q_s = gsm;                              // [D][kQPad]   q^T of the 64 queries
+  float* m_s = q_s + (size_t)D * kQPad;          // [D][kBPad]   mu^T of one chunk
+  float* g_s = m_s + (size_t)D * kBPad;          // [kGQ][n_blocks + 1] gates
+  float* qn_s = g_s + (size_t)kGQ * (n_blocks + 1);  // [kGQ]  ||q||
+  float* mn_s = qn_s + kGQ;                      // [n_blocks] ||mu||
+  __shared__ int chosen_s[kGThreads / 32][kMaxTopk + 1];
+  const int gld = n_blocks + 1;
 
   const int h = blockIdx.y;
   const int gkv = h / (a.Hq / a.Hkv);
-  for (int idx = threadIdx.x; idx < n_blocks * D; idx += blockDim.x) {
-    const int b = idx / D, d = idx - b * D;
-    mu_s[b * ld + d] = mu32[((int64_t)b * a.Hkv + gkv) * D + d];
+  const int q0 = blockIdx.x * kGQ;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // q^T (fp32, exact from bf16) and ||q||
+  for (int idx = tid; idx < kGQ * D; idx += kGThreads) {
+    const int i = idx / D, d = idx - i * D;
+    float v = 0.f;
+    if (q0 + i < a.Tq)
+      v = to_f32(reinterpret_cast<const T*>(a.q)[(int64_t)(q0 + i) * a.q_stride_t +
+                                                   (int64_t)h * a.q_stride_h + d]);
+    q_s[d * kQPad + i] = v;
+  }
+  __syncthreads();
+  if (tid < kGQ) {
+    float ss = 0.f;
+    for (int d = 0; d < D; ++d) ss = fmaf(q_s[d * kQPad + tid], q_s[d * kQPad + tid], ss);
+    qn_s[tid] = sqrtf(ss);
+  }
+
+  const int tq = tid >> 4, tb = tid & 15;   // 4 queries x 8 blocks per thread
+  for (int c0 = 0; c0 < n_blocks; c0 += kGB) {
+    const int nb = min(kGB, n_blocks - c0);
+    __syncthreads();
+    for (int idx = tid; idx < kGB * D; idx += kGThreads) {
+      const int b = idx / D, d = idx - b * D;
+      m_s[d * kBPad + b] = b < nb ? mu32[((int64_t)(c0 + b) * a.Hkv + gkv) * D + d] : 0.f;
+    }
+    __syncthreads();
+    if (tid < nb) {
+      float ss = 0.f;
+      for (int d = 0; d < D; ++d) ss = fmaf(m_s[d * kBPad + tid], m_s[d * kBPad + tid], ss);
+      mn_s[c0 + tid] = sqrtf(ss);
+    }
+    float acc[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int d = 0; d < D; ++d) {
+      const float4 qv = *reinterpret_cast<const float4*>(q_s + d * kQPad + 4 * tq);
+      const float4 m0 = *reinterpret_cast<const float4*>(m_s + d * kBPad + 8 * tb);
+      const float4 m1 = *reinterpret_cast<const float4*>(m_s + d * kBPad + 8 * tb + 4);
+      const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
+      const float ma[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(qa[i], ma[j], acc[i][j]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (8 * tb + j < nb) g_s[(4 * tq + i) * gld + c0 + 8 * tb + j] = acc[i][j];
   }
   __syncthreads();
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float* q = q_s + warp * D;
-  float* gw = g_s + warp * n_blocks;
-  float* ew = e_s + warp * n_blocks;
-  double* g64 = g64_s + warp * n_blocks;
+  // selection: warp w takes queries w, w + 8, ...
   int* chosen = chosen_s[warp];
-  const float gamma = 2.f * (float)(D + 8) * 5.9604645e-8f;  // 2 (D + 8) 2^-24
-
-  for (int qi = 0; qi < kQueriesPerWarp; ++qi) {
-    const int i = (blockIdx.x * kGateWarps + warp) * kQueriesPerWarp + qi;
-    if (i >= a.Tq) break;
-    const T* qrow = reinterpret_cast<const T*>(a.q) + (int64_t)i * a.q_stride_t + (int64_t)h * a.q_stride_h;
-    for (int d = lane; d < D; d += 32) q[d] = to_f32(qrow[d]);
-    __syncwarp();
-    const int64_t own = query_pos(a, i) / B;
+  const float gamma = 2.f * (float)(D + 8) * 5.9604645e-8f * 1.01f;   // 2 (D + 8) 2^-24, padded
+  for (int i = warp; i < kGQ; i += kGThreads / 32) {
+    const int qi = q0 + i;
+    if (qi >= a.Tq) break;
+    const float* gw = g_s + i * gld;
+    const float qn = qn_s[i];
+    const int64_t own = query_pos(a, qi) / B;
     const int n_cand = (int)min((int64_t)n_blocks, own);
     int n_chosen = 0;
-
+    auto err = [&](int b) { return gamma * qn * mn_s[b] + 1e-30f; };
     if (n_cand <= topk) {
       for (int b = lane; b < n_cand; b += 32) chosen[b] = b;
       n_chosen = max(n_cand, 0);
     } else {
-      for (int b = lane; b < n_cand; b += 32) {
-        const float* mu = mu_s + b * ld;
-        float acc = 0.f, mag = 0.f;
-        for (int d = 0; d < D; ++d) {
-          acc = fmaf(q[d], mu[d], acc);
-          mag = fmaf(fabsf(q[d]), fabsf(mu[d]), mag);
-        }
-        gw[b] = acc;
-        ew[b] = gamma * mag + 1e-30f;
-      }
-      __syncwarp();
-      // T: the topk-th largest lower bound.
+      // T: the topk-th largest lower bound
       float pv = CUDART_INF_F;
       int pb = -1;
       for (int r = 0; r < topk; ++r) {
         float bv = -CUDART_INF_F;
         int bb = 0x7fffffff;
         for (int b = lane; b < n_cand; b += 32) {
-          const float lo = gw[b] - ew[b];
+          const float lo = gw[b] - err(b);
           if (before(pv, pb, lo, b) && before(lo, b, bv, bb)) { bv = lo; bb = b; }
         }
         for (int o = 16; o > 0; o >>= 1) {
@@ -135,47 +185,36 @@ gate_select_kernel(const cpattn_attn_args a, int B, int n_blocks, int topk,
       }
       const float T_lo = pv;
       int n_u = 0;
-      for (int b = lane; b < n_cand; b += 32) n_u += (gw[b] + ew[b] >= T_lo) ? 1 : 0;
+      for (int b = lane; b < n_cand; b += 32) n_u += (gw[b] + err(b) >= T_lo) ? 1 : 0;
       for (int o = 16; o > 0; o >>= 1) n_u += __shfl_xor_sync(kFullMask, n_u, o);
-
       if (n_u == topk) {
-        // U is exactly the selection; compact it in block order.
         int base = 0;
         for (int b0 = 0; b0 < n_cand; b0 += 32) {
           const int b = b0 + lane;
-          const bool in = b < n_cand && gw[b] + ew[b] >= T_lo;
+          const bool in = b < n_cand && gw[b] + err(b) >= T_lo;
           const unsigned m = __ballot_sync(kFullMask, in);
           if (in) chosen[base + __popc(m & ((1u << lane) - 1))] = b;
           base += __popc(m);
         }
         n_chosen = topk;
       } else {
-        // Re-rank the uncertain set by fp64 gates (members only).
-        for (int b = 0; b < n_cand; ++b) {
-          if (!(gw[b] + ew[b] >= T_lo)) continue;
-          const double* mu = mu64 + ((int64_t)b * a.Hkv + gkv) * D;
-          double acc = 0.0;
-          for (int d = lane; d < D; d += 32) acc = fma((double)q[d], mu[d], acc);
-          acc = warp_sum_f64(acc);
-          if (lane == 0) g64[b] = acc;
-        }
-        __syncwarp();
+        // re-rank the uncertain set by fp64 gates (q exact from its input type)
+        const T* qrow = reinterpret_cast<const T*>(a.q) + (int64_t)qi * a.q_stride_t +
+                        (int64_t)h * a.q_stride_h;
         double pv64 = CUDART_INF;
         pb = -1;
         for (int r = 0; r < topk; ++r) {
           double bv = -CUDART_INF;
           int bb = 0x7fffffff;
-          for (int b = lane; b < n_cand; b += 32) {
-            if (!(gw[b] + ew[b] >= T_lo)) continue;
-            const double gv = g64[b];
-            if (before64(pv64, pb, gv, b) && before64(gv, b, bv, bb)) { bv = gv; bb = b; }
+          for (int b = 0; b < n_cand; ++b) {
+            if (!(gw[b] + err(b) >= T_lo)) continue;
+            const double* mu = mu64 + ((int64_t)b * a.Hkv + gkv) * D;
+            double acc = 0.0;
+            for (int d = lane; d < D; d += 32) acc = fma((double)to_f32(qrow[d]), mu[d], acc);
+            acc = warp_sum_f64(acc);
+            if (before64(pv64, pb, acc, b) && before64(acc, b, bv, bb)) { bv = acc; bb = b; }
           }
-          for (int o = 16; o > 0; o >>= 1) {
-            const double ov = __shfl_xor_sync(kFullMask, bv, o);
-            const int ob = __shfl_xor_sync(kFullMask, bb, o);
-            if (before64(ov, ob, bv, bb)) { bv = ov; bb = ob; }
-          }
-          if (bb == 0x7fffffff) break;  // fewer members than topk (only with NaN gates)
+          if (bb == 0x7fffffff) break;   // fewer members than topk (only with NaN gates)
           if (lane == 0) chosen[r] = bb;
           n_chosen = r + 1;
           pv64 = bv;
@@ -185,14 +224,13 @@ gate_select_kernel(const cpattn_attn_args a, int B, int n_blocks, int topk,
     }
     __syncwarp();
     if (lane == 0) {
-      // ascending order; every chosen block is below the own block
       for (int x = 1; x < n_chosen; ++x) {
         const int v = chosen[x];
         int y = x - 1;
         while (y >= 0 && chosen[y] > v) { chosen[y + 1] = chosen[y]; --y; }
         chosen[y + 1] = v;
       }
-      int32_t* out = sel + ((int64_t)i * a.Hq + h) * (topk + 1);
+      int32_t* out = sel + ((int64_t)qi * a.Hq + h) * (topk + 1);
       for (int x = 0; x < n_chosen; ++x) out[x] = chosen[x];
       out[n_chosen] = (int32_t)own;
       for (int x = n_chosen + 1; x <= topk; ++x) out[x] = -1;
@@ -219,18 +257,14 @@ cudaError_t launch_gate_t(const cpattn_attn_args& a, int B, int topk, int32_t* s
   auto kern = gate_select_kernel<T>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int q_per_cta = kGateWarps * kQueriesPerWarp;
-  dim3 grid((a.Tq + q_per_cta - 1) / q_per_cta, a.Hq);
-  kern<<<grid, kGateWarps * 32, smem, stream>>>(a, B, n_blocks, topk, mu64, mu32, sel);
+  dim3 grid((a.Tq + kGQ - 1) / kGQ, a.Hq);
+  kern<<<grid, kGThreads, smem, stream>>>(a, B, n_blocks, topk, mu64, mu32, sel);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t block_gate_smem(int n_blocks, int D) {
-  return (size_t)kGateWarps * n_blocks * sizeof(double) + (size_t)n_blocks * (D + 1) * 4 +
-         (size_t)kGateWarps * D * 4 + (size_t)kGateWarps * n_blocks * 8;
-}
+size_t block_gate_smem(int n_blocks, int D) { return gate_smem_floats(n_blocks, D) * sizeof(float); }
 
 size_t block_gate_workspace(const cpattn_attn_args& a, int32_t block_size) {
   const size_t n_blocks = block_size > 0 ? (size_t)(a.Tk / block_size) : 0;

@@ -200,8 +200,9 @@ cpattn_status cpattn_topk_sparse_fwd(const cpattn_attn_args* args, const int32_t
  * Uses args->dtype, q, k (strides, Tq, Hq, Dqk, Tk, Hkv), causal_offset and
  * q_chunk_map/chunk_len for qpos.  cu_seqlens and kv_chunk_map must be NULL.
  * Workspace: cpattn_workspace_size(CPATTN_OP_BLOCK_GATE, ...) bytes (block
- * means).  Limits: topk <= 64; the fp32 block means of one head must fit in
- * shared memory (Tk / B * (Dqk + 1) * 4 bytes <= 160 KiB).
+ * means).  Limits: topk <= 64; the number of complete blocks Tk / B is
+ * limited by the kernel's shared-memory staging (about 370 at Dqk = 128;
+ * CPATTN_ERR_UNSUPPORTED beyond).
  */
 cpattn_status cpattn_block_gate(const cpattn_attn_args* args, int32_t block_size, int32_t topk,
                                 int32_t* sel, void* workspace, size_t workspace_bytes,

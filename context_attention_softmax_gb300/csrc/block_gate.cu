@@ -59,14 +59,15 @@ __device__ __forceinline__ bool before64(double v1, int b1, double v2, int b2) {
 }
 
 // Gates of 64 queries x all candidate blocks of one head, as a register-tiled
-// fp32 product: 256 threads, each a 4-query x 8-block tile per 128-block
-// chunk, both operands staged transposed in shared memory.  The error bound
+// fp32 product: 256 threads, each a 4-query x 4-block tile per 64-block
+// chunk, both operands staged transposed in shared memory (about 100 KiB, so
+// two CTAs share an SM).  The error bound
 // uses norms: sum_d |q_d||mu_d| <= ||q||_2 ||mu||_2, so
 //   e_b = 2 (D + 8) 2^-24 ||q||_2 ||mu_b||_2
 // bounds |fp32 gate - exact gate| (dot product, rounding of the mean and of
 // the norms included).  Selection then as described at the top of the file.
 constexpr int kGQ = 64;          // queries per CTA
-constexpr int kGB = 128;         // blocks per chunk
+constexpr int kGB = 64;          // blocks per chunk
 constexpr int kGThreads = 256;
 constexpr int kQPad = kGQ + 4;   // shared row strides (floats), 16-byte aligned
 constexpr int kBPad = kGB + 4;
@@ -76,7 +77,7 @@ __host__ __device__ constexpr size_t gate_smem_floats(int n_blocks, int D) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __launch_bounds__(kGThreads, 2)
 gate_select_kernel(const cpattn_attn_args a, int B, int n_blocks, int topk,
                    const double* __restrict__ mu64, const float* __restrict__ mu32,
                    int32_t* __restrict__ sel) {
@@ -111,7 +112,7 @@ gate_select_kernel(const cpattn_attn_args a, int B, int n_blocks, int topk,
     qn_s[tid] = sqrtf(ss);
   }
 
-  const int tq = tid >> 4, tb = tid & 15;   // 4 queries x 8 blocks per thread
+  const int tq = tid >> 4, tb = tid & 15;   // 4 queries x 4 blocks per thread
   for (int c0 = 0; c0 < n_blocks; c0 += kGB) {
     const int nb = min(kGB, n_blocks - c0);
     __syncthreads();
@@ -125,27 +126,27 @@ gate_select_kernel(const cpattn_attn_args a, int B, int n_blocks, int topk,
       for (int d = 0; d < D; ++d) ss = fmaf(m_s[d * kBPad + tid], m_s[d * kBPad + tid], ss);
       mn_s[c0 + tid] = sqrtf(ss);
     }
-    float acc[4][8];
+    float acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
     for (int d = 0; d < D; ++d) {
       const float4 qv = *reinterpret_cast<const float4*>(q_s + d * kQPad + 4 * tq);
-      const float4 m0 = *reinterpret_cast<const float4*>(m_s + d * kBPad + 8 * tb);
-      const float4 m1 = *reinterpret_cast<const float4*>(m_s + d * kBPad + 8 * tb + 4);
+      const float4 mv = *reinterpret_cast<const float4*>(m_s + d * kBPad + 4 * tb);
       const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
-      const float ma[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+      const float ma[4] = {mv.x, mv.y, mv.z, mv.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(qa[i], ma[j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(qa[i], ma[j], acc[i][j]);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (8 * tb + j < nb) g_s[(4 * tq + i) * gld + c0 + 8 * tb + j] = acc[i][j];
+      for (int j = 0; j < 4; ++j)
+        if (4 * tb + j < nb) g_s[(4 * tq + i) * gld + c0 + 4 * tb + j] = acc[i][j];
   }
   __syncthreads();
 

@@ -172,6 +172,11 @@ cpattn_status cpattn_topk_sparse_fwd(const cpattn_attn_args* a, const int32_t* i
     return cuda_status(launch_moba_tc(*a, indices, topk, index_heads, block_size, workspace, st),
                        "cpattn_topk_sparse_fwd block-grouped launch");
   }
+  if (block_size == 1 && topk > 0 && dsa_tc_supported(*a, index_heads, block_size)) {
+    bool launched = false;
+    cudaError_t e = launch_dsa_tc(*a, indices, topk, st, &launched);
+    if (e != cudaSuccess || launched) return cuda_status(e, "cpattn_topk_sparse_fwd tensor-core launch");
+  }
   SparseArgs sp{indices, topk, index_heads, block_size};
   return cuda_status(launch_rowwise(*a, block_size == 1 ? kTokens : kBlocks, sp, st),
                      "cpattn_topk_sparse_fwd launch");

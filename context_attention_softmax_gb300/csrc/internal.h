@@ -45,6 +45,12 @@ size_t moba_tc_workspace(const cpattn_attn_args& a, int32_t slots, int32_t block
 cudaError_t launch_moba_tc(const cpattn_attn_args& a, const int32_t* sel, int32_t slots,
                            int32_t index_heads, int32_t block_size, void* workspace,
                            cudaStream_t stream);
+// DSA token-index attention on the tensor cores for absorbed-MLA shapes:
+// bf16, 128 query heads over one KV head, key rows of 576 channels whose
+// first 512 are the values (v aliases k), indices shared by all heads.
+bool dsa_tc_supported(const cpattn_attn_args& a, int32_t index_heads, int32_t block_size);
+cudaError_t launch_dsa_tc(const cpattn_attn_args& a, const int32_t* indices, int32_t topk,
+                          cudaStream_t stream, bool* launched);
 size_t block_gate_workspace(const cpattn_attn_args& a, int32_t block_size);
 size_t block_gate_smem(int n_blocks, int D);
 cudaError_t launch_block_gate(const cpattn_attn_args& a, int32_t block_size, int32_t topk,

@@ -289,6 +289,66 @@ __device__ __forceinline__ void umma8_ts_mnmajor(uint32_t d_tmem, uint32_t a_tme
       "r"(a_tmem), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
 }
 
+// Four MMAs (K = 64) with both operands K-major in one 128-byte-swizzled
+// 64-column box: steps advance both descriptors by 32 B (2 in >> 4 units).
+template <int ACC0>
+__device__ __forceinline__ void umma4_ss_k(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b32 a<4>, b<4>;\n\t.reg .b64 da<4>, db<4>;\n\t"
+      "add.u32 a0, %1, 0; add.u32 b0, %2, 0;\n\t"
+      "add.u32 a1, %1, 2; add.u32 b1, %2, 2;\n\t"
+      "add.u32 a2, %1, 4; add.u32 b2, %2, 4;\n\t"
+      "add.u32 a3, %1, 6; add.u32 b3, %2, 6;\n\t"
+      "mov.b64 da0, {a0, %4}; mov.b64 db0, {b0, %4};\n\t"
+      "mov.b64 da1, {a1, %4}; mov.b64 db1, {b1, %4};\n\t"
+      "mov.b64 da2, {a2, %4}; mov.b64 db2, {b2, %4};\n\t"
+      "mov.b64 da3, {a3, %4}; mov.b64 db3, {b3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da0, db0, %3, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da1, db1, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da2, db2, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da3, db3, %3, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+}
+// Four MMAs (K = 64) with A in tensor memory (columns a_tmem + 8 k) and B
+// K-major in one swizzled box (b_lo + 2 k).
+template <int ACC0>
+__device__ __forceinline__ void umma4_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b32 b<4>, t<4>;\n\t.reg .b64 db<4>;\n\t"
+      "add.u32 b0, %2, 0; add.u32 t0, %1, 0;\n\t"
+      "add.u32 b1, %2, 2; add.u32 t1, %1, 8;\n\t"
+      "add.u32 b2, %2, 4; add.u32 t2, %1, 16;\n\t"
+      "add.u32 b3, %2, 6; add.u32 t3, %1, 24;\n\t"
+      "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"
+      "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+}
+// Four MMAs (K = 64) with A in tensor memory and B MN-major (16 K-rows =
+// 2 KiB per step, b_lo + 128 k; leading offset carried in b_lo).
+template <int ACC0>
+__device__ __forceinline__ void umma4_ts_mn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                            uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .b32 b<4>, t<4>;\n\t.reg .b64 db<4>;\n\t"
+      "add.u32 b0, %2, 0;   add.u32 t0, %1, 0;\n\t"
+      "add.u32 b1, %2, 128; add.u32 t1, %1, 8;\n\t"
+      "add.u32 b2, %2, 256; add.u32 t2, %1, 16;\n\t"
+      "add.u32 b3, %2, 384; add.u32 t3, %1, 24;\n\t"
+      "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"
+      "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]; A (M x K, 16-bit, two elements per 32-bit
 // column, lane = row) is read from tensor memory.
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,

@@ -194,6 +194,25 @@ def test_dsa_small_with_padding_and_bad_indices():
     assert_matches(o, lse, O, L, "bf16", "dsa small")
 
 
+def test_dsa_tensor_core_small():
+    # 128 heads over one KV head, v = first 512 channels of k: the tensor-core
+    # path; top-k 200 leaves a ragged last tile of 64 keys
+    w = inputs.dsa_absorbed(seed=10, Tq=24, Tk=3000, offset=1500, Hq=128, topk=200)
+    idx = w.indices.clone()
+    idx[2, 0, 150:] = -1                 # fewer than topk selected
+    idx[4, 0, :] = -1                    # nothing selected -> (0, -inf)
+    idx[6, 0, 7] = 4000                  # out of range: skipped, flagged
+    idx[8, 0, 11] = idx[8, 0, 12]        # duplicate counts twice
+    idx[9, 0, 20] = 2999                 # in range but after the query: masked again
+    w.indices = idx
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = _dsa_run(w, status)
+    q, k, v = f64(w)
+    O, L, bad = orc.sparse_attention(q, k, v, w.scale, layout_of(w), idx.numpy())
+    assert bad == 1 and int(status.item()) == 6
+    assert_matches(o, lse, O, L, "bf16", "dsa tensor-core small")
+
+
 def test_dsa_full_size_sampled():
     w = inputs.dsa_absorbed(device="cuda")
     o, lse = _dsa_run(w)

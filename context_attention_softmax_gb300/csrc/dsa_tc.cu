@@ -19,8 +19,8 @@
 //     with 16-byte cp.async straight into the 128-byte-swizzled layout; the
 //     value rows are the first 512 channels of the same rows;
 //   * the permitted relation (causal + packed bounds) is re-applied to every
-//     index and kept as a 64-bit column mask per tile; -1 and out-of-range
-//     indices are masked (out-of-range also sets dev_status).
+//     index and kept as one flag per key slot of the tile; -1 and
+//     out-of-range indices are masked (out-of-range also sets dev_status).
 // TMEM: Q^T part [0,128), S double buffer [128,192) / [192,256), O half
 // [256,512).  Work items (query, half) are taken in a fixed stride by
 // persistent CTAs; all roles walk the same sequence.
@@ -40,7 +40,8 @@ constexpr int HQ = 128;                  // heads = MMA rows
 constexpr int DQK = 576, DVH = 256;      // key width, value channels per CTA
 constexpr int BNK = 64;                  // keys per tile
 constexpr int NS = 2;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kGatherThreads = 192;     // warps 2-3 and 8-11
 constexpr int kChunks = DQK / 64;        // 9 channel chunks of a key row
 constexpr int kQT = 4;                   // Q channel chunks in TMEM (0..255)
 constexpr int kQS = kChunks - kQT;       // 5 chunks in shared memory
@@ -62,7 +63,7 @@ struct DsaParams {
 struct DSmem {
   uint8_t qs[kQS][kQChunkBytes];
   uint8_t kv[NS][kStageBytes];
-  uint32_t kmask[NS][2];
+  uint8_t take[NS][BNK];   // permitted flag of each key slot of the stage
   uint64_t qs_full, qs_empty, qt_full;
   uint64_t kv_full[NS], kv_empty[NS];
   uint64_t s_full[2], p_full[2];
@@ -93,9 +94,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&t);
 }
 
-// Roles (256 threads): warp 0 Q loader (TMA, channels 256..575), warp 1 MMA
-// issuer + TMEM owner, warps 2-3 key-row gather (one key of the tile per
-// thread), warps 4-7 softmax, Q^T TMEM fill and epilogue (row = head).
+// Roles (384 threads): warp 0 Q loader (TMA, channels 256..575), warp 1 MMA
+// issuer + TMEM owner, warps 2-3 and 8-11 key-row gather (a warp per key
+// row at a time), warps 4-7 softmax, Q^T TMEM fill and epilogue (row =
+// head).  The gather is bounded by how many 16-byte copies are in flight, so
+// it gets the most threads.
 __global__ void __launch_bounds__(kThreads, 1)
 dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -110,7 +113,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
     mbar_init(&s.qs_empty, 1);
     mbar_init(&s.qt_full, 128);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&s.kv_full[i], 64);
+      mbar_init(&s.kv_full[i], kGatherThreads);
       mbar_init(&s.kv_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -152,9 +155,13 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         mbar_wait(&s.qs_full, ui & 1, &no_abort, 200000000ull);
       }
     }
-  } else if (warp == 2 || warp == 3) {
+  } else if (warp == 2 || warp == 3 || warp >= 8) {
     // ------------------------------------------------------------ key-row gather
-    const int t = threadIdx.x - 64;   // key slot of the tile
+    // Six warps; warp w takes key slots w, w + 6, ... of the tile and its 32
+    // lanes copy consecutive 16-byte chunks of that row (72 chunks), so every
+    // copy uses whole 32-byte sectors.  Gather warp 0 publishes the tile's
+    // permitted flags in take[] for the softmax mask.
+    const int gw = (warp <= 3) ? warp - 2 : warp - 6;   // 0..5
     int gj = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
@@ -164,21 +171,33 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         const int st = gj % NS;
         ok = __all_sync(kFullMask, mbar_wait(&s.kv_empty[st], ((gj / NS) & 1) ^ 1, abort_flag));
         if (!ok) break;
-        const int slot = BNK * j + t;
-        const int64_t e = slot < p.topk ? (int64_t)__ldg(p.idx + (int64_t)i * p.topk + slot) : -1;
-        if (e < -1 || e >= a.Tk) report_status(a.dev_status, CPATTN_ERR_BAD_INDEX);
-        const bool take = e >= 0 && e < a.Tk && e >= iv.lo && e <= iv.hi;
-        const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(a.k) +
-                                   (take ? e : 0) * a.k_stride_t;
-        const uint32_t dst0 = smem_u32(s.kv[st]) + t * 128;
-#pragma unroll 8
-        for (int cc = 0; cc < kChunks * 8; ++cc) {
-          const uint32_t dst = dst0 + (cc >> 3) * kKChunkBytes + (((cc & 7) ^ (t & 7)) << 4);
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + 8 * cc)
-                       : "memory");
+        // The tile's 64 indices, two per lane, each checked once.
+        int64_t e2[2];
+        bool tk2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int slot = BNK * j + 32 * h + lane;
+          const int64_t e = slot < p.topk ? (int64_t)__ldg(p.idx + (int64_t)i * p.topk + slot) : -1;
+          if (gw == 0 && (e < -1 || e >= a.Tk)) report_status(a.dev_status, CPATTN_ERR_BAD_INDEX);
+          tk2[h] = e >= 0 && e < a.Tk && e >= iv.lo && e <= iv.hi;
+          e2[h] = tk2[h] ? e : 0;
+          if (gw == 0) s.take[st][32 * h + lane] = tk2[h] ? 1 : 0;
         }
-        const unsigned m = __ballot_sync(kFullMask, take);
-        if (lane == 0) s.kmask[st][warp - 2] = m;
+        const uint32_t stage = smem_u32(s.kv[st]);
+        for (int t = gw; t < BNK; t += 6) {
+          const int64_t e = __shfl_sync(kFullMask, t < 32 ? e2[0] : e2[1], t & 31);
+          const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(a.k) + e * a.k_stride_t;
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            const int cc = lane + 32 * k;
+            if (cc < kChunks * 8) {
+              const uint32_t dst = stage + (cc >> 3) * kKChunkBytes + t * 128 +
+                                   (((cc & 7) ^ (t & 7)) << 4);
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + 8 * cc)
+                           : "memory");
+            }
+          }
+        }
         asm volatile("cp.async.wait_all;" ::: "memory");
         fence_proxy_async_smem();
         mbar_arrive(&s.kv_full[st]);
@@ -249,7 +268,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax + epilogue
     const int r = (warp & 3) * 32 + lane;   // head
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -286,7 +305,15 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         if (!ok) break;
         tc_fence_after();
         const uint32_t s_col = tmem + lane_base + kColS + (gj & 1) * BNK;
-        const uint32_t m0 = s.kmask[st][0], m1 = s.kmask[st][1];
+        uint32_t m0 = 0, m1 = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t w0 = reinterpret_cast<const uint32_t*>(s.take[st])[q];
+          const uint32_t w1 = reinterpret_cast<const uint32_t*>(s.take[st])[8 + q];
+          // bytes -> bits: byte b of the word is key 4q + b
+          m0 |= ((w0 & 1u) | ((w0 >> 7) & 2u) | ((w0 >> 14) & 4u) | ((w0 >> 21) & 8u)) << (4 * q);
+          m1 |= ((w1 & 1u) | ((w1 >> 7) & 2u) | ((w1 >> 14) & 4u) | ((w1 >> 21) & 8u)) << (4 * q);
+        }
         float sv[BNK];
         {
           uint32_t r0[32], r1[32];

@@ -63,9 +63,9 @@ struct DsaParams {
 struct DSmem {
   uint8_t qs[kQS][kQChunkBytes];
   uint8_t kv[NS][kStageBytes];
-  uint8_t take[NS][BNK];   // permitted flag of each key slot of the stage
   uint64_t qs_full, qs_empty, qt_full;
-  uint64_t kv_full[NS], kv_empty[NS];
+  uint64_t ka_full[NS], ka_empty[NS];   // key chunks this half's PV does not read
+  uint64_t kb_full[NS], kb_empty[NS];   // the four value chunks of this half
   uint64_t s_full[2], p_full[2];
   uint64_t pv_done, o_full, o_free, drain;
   uint32_t tmem_base;
@@ -113,8 +113,10 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
     mbar_init(&s.qs_empty, 1);
     mbar_init(&s.qt_full, 128);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&s.kv_full[i], kGatherThreads);
-      mbar_init(&s.kv_empty[i], 1);
+      mbar_init(&s.ka_full[i], kGatherThreads);
+      mbar_init(&s.ka_empty[i], 1);
+      mbar_init(&s.kb_full[i], kGatherThreads);
+      mbar_init(&s.kb_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.s_full[i], 1);
@@ -158,51 +160,71 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
   } else if (warp == 2 || warp == 3 || warp >= 8) {
     // ------------------------------------------------------------ key-row gather
     // Six warps; warp w takes key slots w, w + 6, ... of the tile and its 32
-    // lanes copy consecutive 16-byte chunks of that row (72 chunks), so every
-    // copy uses whole 32-byte sectors.  Gather warp 0 publishes the tile's
-    // permitted flags in take[] for the softmax mask.
+    // lanes copy consecutive 16-byte pieces of that row, so every copy uses
+    // whole 32-byte sectors.  A stage is filled in two parts with their own
+    // barriers: part A (the five 64-channel chunks that this half's PV does
+    // not read) is free again as soon as S is done, part B (the four value
+    // chunks 4c..4c+3) only after PV.  Each part's barrier is arrived on by
+    // the copies themselves when they land, so the warps never block on
+    // their own copies and several parts stay in flight.
     const int gw = (warp <= 3) ? warp - 2 : warp - 6;   // 0..5
+    const __nv_bfloat16* kbase = reinterpret_cast<const __nv_bfloat16*>(a.k);
     int gj = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const int i = it >> 1;
+      const int i = it >> 1, hc = it & 1;
       const KeyInterval iv = allowed_interval(a, query_pos(a, i));
       for (int j = 0; j < T; ++j, ++gj) {
         const int st = gj % NS;
-        ok = __all_sync(kFullMask, mbar_wait(&s.kv_empty[st], ((gj / NS) & 1) ^ 1, abort_flag));
+        const uint32_t ph = ((gj / NS) & 1) ^ 1;
+        const uint32_t stage = smem_u32(s.kv[st]);
+        ok = __all_sync(kFullMask, mbar_wait(&s.ka_empty[st], ph, abort_flag));
         if (!ok) break;
         // The tile's 64 indices, two per lane, each checked once.
         int64_t e2[2];
-        bool tk2[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int slot = BNK * j + 32 * h + lane;
           const int64_t e = slot < p.topk ? (int64_t)__ldg(p.idx + (int64_t)i * p.topk + slot) : -1;
           if (gw == 0 && (e < -1 || e >= a.Tk)) report_status(a.dev_status, CPATTN_ERR_BAD_INDEX);
-          tk2[h] = e >= 0 && e < a.Tk && e >= iv.lo && e <= iv.hi;
-          e2[h] = tk2[h] ? e : 0;
-          if (gw == 0) s.take[st][32 * h + lane] = tk2[h] ? 1 : 0;
+          e2[h] = (e >= 0 && e < a.Tk && e >= iv.lo && e <= iv.hi) ? e : 0;
         }
-        const uint32_t stage = smem_u32(s.kv[st]);
+        // part A: 40 pieces per row
         for (int t = gw; t < BNK; t += 6) {
-          const int64_t e = __shfl_sync(kFullMask, t < 32 ? e2[0] : e2[1], t & 31);
-          const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(a.k) + e * a.k_stride_t;
+          const __nv_bfloat16* src =
+              kbase + __shfl_sync(kFullMask, t < 32 ? e2[0] : e2[1], t & 31) * a.k_stride_t;
 #pragma unroll
-          for (int k = 0; k < 3; ++k) {
-            const int cc = lane + 32 * k;
-            if (cc < kChunks * 8) {
-              const uint32_t dst = stage + (cc >> 3) * kKChunkBytes + t * 128 +
-                                   (((cc & 7) ^ (t & 7)) << 4);
-              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + 8 * cc)
+          for (int k = 0; k < 2; ++k) {
+            const int pc = lane + 32 * k;
+            if (pc < 40) {
+              const int q = pc >> 3;
+              const int ch = hc == 0 ? 4 + q : (q < 4 ? q : 8);
+              const uint32_t dst = stage + ch * kKChunkBytes + t * 128 + (((pc & 7) ^ (t & 7)) << 4);
+              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                           "l"(src + 64 * ch + 8 * (pc & 7))
                            : "memory");
             }
           }
         }
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        fence_proxy_async_smem();
-        mbar_arrive(&s.kv_full[st]);
+        cp_async_mbar_arrive_noinc(&s.ka_full[st]);
+        // part B: 32 pieces per row, one per lane
+        ok = __all_sync(kFullMask, mbar_wait(&s.kb_empty[st], ph, abort_flag));
+        if (!ok) break;
+        {
+          const int ch = 4 * hc + (lane >> 3);
+          for (int t = gw; t < BNK; t += 6) {
+            const __nv_bfloat16* src =
+                kbase + __shfl_sync(kFullMask, t < 32 ? e2[0] : e2[1], t & 31) * a.k_stride_t;
+            const uint32_t dst = stage + ch * kKChunkBytes + t * 128 + (((lane & 7) ^ (t & 7)) << 4);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                         "l"(src + 64 * ch + 8 * (lane & 7))
+                         : "memory");
+          }
+        }
+        cp_async_mbar_arrive_noinc(&s.kb_full[st]);
       }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -223,12 +245,13 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         const uint32_t pa = tmem + kColS + (g & 1) * BNK;
         if (prev_first) umma4_ts_mn<0>(tmem + kColO, pa, vb, idesc_pv);
         else umma4_ts_mn<1>(tmem + kColO, pa, vb, idesc_pv);
-        umma_commit(&s.kv_empty[g % NS]);
+        umma_commit(&s.kb_empty[g % NS]);
         umma_commit(&s.pv_done);
         if (prev_last) umma_commit(&s.o_full);
         return true;
       };
       for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++ui) {
+        const int hc = it & 1;
         // The previous item's last PV goes first: its epilogue frees the Q^T
         // columns that this item's S needs (qt_full follows o_full).
         if (prev >= 0) {
@@ -239,20 +262,40 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
             !mbar_wait(&s.qs_full, ui & 1, abort_flag)) { ok = false; break; }
         for (int j = 0; j < T; ++j, ++gj) {
           const int st = gj % NS;
-          if (!mbar_wait(&s.kv_full[st], (gj / NS) & 1, abort_flag)) { ok = false; break; }
+          const uint32_t ph = (gj / NS) & 1;
+          if (!mbar_wait(&s.ka_full[st], ph, abort_flag)) { ok = false; break; }
+          fence_proxy_async_smem();   // the gathered rows were written by cp.async
           tc_fence_after();
           const uint32_t d = tmem + kColS + (gj & 1) * BNK;
           const uint32_t kb = desc_lo(smem_u32(s.kv[st]), 16);
-          // channels 0..255: A = Q^T from TMEM (32 columns per 64 channels)
-          umma4_ts_k<0>(d, tmem + kColQ + 0, kb + 0 * (kKChunkBytes >> 4), idesc_s);
-          umma4_ts_k<1>(d, tmem + kColQ + 32, kb + 1 * (kKChunkBytes >> 4), idesc_s);
-          umma4_ts_k<1>(d, tmem + kColQ + 64, kb + 2 * (kKChunkBytes >> 4), idesc_s);
-          umma4_ts_k<1>(d, tmem + kColQ + 96, kb + 3 * (kKChunkBytes >> 4), idesc_s);
-          // channels 256..575: A = Q from shared memory
+          constexpr uint32_t kC = kKChunkBytes >> 4, kQC = kQChunkBytes >> 4;
+          // Channels 0..255 take A = Q^T from TMEM (32 columns per 64
+          // channels), channels 256..575 A = Q from shared memory.  Part A
+          // chunks first, then the value chunks of this half.
+          if (hc == 0) {
+            umma4_ss_k<0>(d, qs_lo, kb + 4 * kC, idesc_s);
 #pragma unroll
-          for (int c = 0; c < kQS; ++c)
-            umma4_ss_k<1>(d, qs_lo + c * (kQChunkBytes >> 4), kb + (kQT + c) * (kKChunkBytes >> 4),
-                          idesc_s);
+            for (int c = 1; c < kQS; ++c) umma4_ss_k<1>(d, qs_lo + c * kQC, kb + (kQT + c) * kC, idesc_s);
+          } else {
+            umma4_ts_k<0>(d, tmem + kColQ + 0, kb + 0 * kC, idesc_s);
+            umma4_ts_k<1>(d, tmem + kColQ + 32, kb + 1 * kC, idesc_s);
+            umma4_ts_k<1>(d, tmem + kColQ + 64, kb + 2 * kC, idesc_s);
+            umma4_ts_k<1>(d, tmem + kColQ + 96, kb + 3 * kC, idesc_s);
+            umma4_ss_k<1>(d, qs_lo + 4 * kQC, kb + 8 * kC, idesc_s);
+          }
+          umma_commit(&s.ka_empty[st]);
+          if (!mbar_wait(&s.kb_full[st], ph, abort_flag)) { ok = false; break; }
+          fence_proxy_async_smem();
+          tc_fence_after();
+          if (hc == 0) {
+            umma4_ts_k<1>(d, tmem + kColQ + 0, kb + 0 * kC, idesc_s);
+            umma4_ts_k<1>(d, tmem + kColQ + 32, kb + 1 * kC, idesc_s);
+            umma4_ts_k<1>(d, tmem + kColQ + 64, kb + 2 * kC, idesc_s);
+            umma4_ts_k<1>(d, tmem + kColQ + 96, kb + 3 * kC, idesc_s);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) umma4_ss_k<1>(d, qs_lo + c * kQC, kb + (kQT + c) * kC, idesc_s);
+          }
           umma_commit(&s.s_full[gj & 1]);
           if (j == T - 1) umma_commit(&s.qs_empty);
           if (prev >= 0 && !issue_pv()) { ok = false; break; }
@@ -277,6 +320,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++ui) {
       const int i = it >> 1, c = it & 1;
+      const KeyInterval iv = allowed_interval(a, query_pos(a, i));
       // Q channels 0..255 of (query i, head r) into TMEM as bf16 pairs.  The
       // previous item's MMAs finished with them (its epilogue waited o_full).
       {
@@ -300,20 +344,21 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
       float m2 = -CUDART_INF_F, l = 0.f, lb = 0.f;
       for (int j = 0; j < T; ++j, ++gj) {
         const int st = gj % NS;
-        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[gj & 1], (gj >> 1) & 1, abort_flag) &&
-                                       mbar_wait(&s.kv_full[st], (gj / NS) & 1, abort_flag));
+        // column mask of the tile: the index is present, in range and
+        // permitted for this query (lane holds keys lane and lane + 32)
+        uint32_t m0, m1;
+        {
+          const int slot = BNK * j + lane;
+          const int64_t e0 = slot < p.topk ? (int64_t)__ldg(p.idx + (int64_t)i * p.topk + slot) : -1;
+          const int64_t e1 =
+              slot + 32 < p.topk ? (int64_t)__ldg(p.idx + (int64_t)i * p.topk + slot + 32) : -1;
+          m0 = __ballot_sync(kFullMask, e0 >= 0 && e0 < a.Tk && e0 >= iv.lo && e0 <= iv.hi);
+          m1 = __ballot_sync(kFullMask, e1 >= 0 && e1 < a.Tk && e1 >= iv.lo && e1 <= iv.hi);
+        }
+        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[gj & 1], (gj >> 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const uint32_t s_col = tmem + lane_base + kColS + (gj & 1) * BNK;
-        uint32_t m0 = 0, m1 = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t w0 = reinterpret_cast<const uint32_t*>(s.take[st])[q];
-          const uint32_t w1 = reinterpret_cast<const uint32_t*>(s.take[st])[8 + q];
-          // bytes -> bits: byte b of the word is key 4q + b
-          m0 |= ((w0 & 1u) | ((w0 >> 7) & 2u) | ((w0 >> 14) & 4u) | ((w0 >> 21) & 8u)) << (4 * q);
-          m1 |= ((w1 & 1u) | ((w1 >> 7) & 2u) | ((w1 >> 14) & 4u) | ((w1 >> 21) & 8u)) << (4 * q);
-        }
         float sv[BNK];
         {
           uint32_t r0[32], r1[32];

@@ -41,7 +41,7 @@ constexpr int DQK = 576, DVH = 256;      // key width, value channels per CTA
 constexpr int BNK = 64;                  // keys per tile
 constexpr int NS = 2;
 constexpr int kThreads = 384;
-constexpr int kGatherThreads = 192;     // warps 2-3 and 8-11
+constexpr int kPartThreads = 96;        // gather threads per stage part
 constexpr int kChunks = DQK / 64;        // 9 channel chunks of a key row
 constexpr int kQT = 4;                   // Q channel chunks in TMEM (0..255)
 constexpr int kQS = kChunks - kQT;       // 5 chunks in shared memory
@@ -95,10 +95,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Roles (384 threads): warp 0 Q loader (TMA, channels 256..575), warp 1 MMA
-// issuer + TMEM owner, warps 2-3 and 8-11 key-row gather (a warp per key
-// row at a time), warps 4-7 softmax, Q^T TMEM fill and epilogue (row =
-// head).  The gather is bounded by how many 16-byte copies are in flight, so
-// it gets the most threads.
+// issuer + TMEM owner, warps 2-3 and 8-11 key-row gather, warps 4-7
+// softmax, Q^T TMEM fill and epilogue (row = head).
 __global__ void __launch_bounds__(kThreads, 1)
 dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -113,9 +111,9 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
     mbar_init(&s.qs_empty, 1);
     mbar_init(&s.qt_full, 128);
     for (int i = 0; i < NS; ++i) {
-      mbar_init(&s.ka_full[i], kGatherThreads);
+      mbar_init(&s.ka_full[i], kPartThreads);
       mbar_init(&s.ka_empty[i], 1);
-      mbar_init(&s.kb_full[i], kGatherThreads);
+      mbar_init(&s.kb_full[i], kPartThreads);
       mbar_init(&s.kb_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -159,16 +157,19 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
     }
   } else if (warp == 2 || warp == 3 || warp >= 8) {
     // ------------------------------------------------------------ key-row gather
-    // Six warps; warp w takes key slots w, w + 6, ... of the tile and its 32
-    // lanes copy consecutive 16-byte pieces of that row, so every copy uses
-    // whole 32-byte sectors.  A stage is filled in two parts with their own
-    // barriers: part A (the five 64-channel chunks that this half's PV does
-    // not read) is free again as soon as S is done, part B (the four value
-    // chunks 4c..4c+3) only after PV.  Each part's barrier is arrived on by
-    // the copies themselves when they land, so the warps never block on
-    // their own copies and several parts stay in flight.
-    const int gw = (warp <= 3) ? warp - 2 : warp - 6;   // 0..5
+    // A stage is filled in two parts with their own barriers: part A (the
+    // five 64-channel chunks that this half's PV does not read) is free again
+    // as soon as S is done, part B (the four value chunks 4c..4c+3) only
+    // after PV.  Warps 2, 3, 8 fetch part A and warps 9-11 part B, so part A
+    // of the next tiles never queues behind a part B that waits for PV.  A
+    // warp takes key slots w, w + 3, ... and its lanes copy consecutive
+    // 16-byte pieces of the row (whole 32-byte sectors).  The barriers are
+    // arrived on by the copies themselves when they land.
+    const bool part_a = warp <= 3 || warp == 8;
+    const int gw = warp <= 3 ? warp - 2 : (warp == 8 ? 2 : warp - 9);   // 0..2
     const __nv_bfloat16* kbase = reinterpret_cast<const __nv_bfloat16*>(a.k);
+    uint64_t* empty = part_a ? s.ka_empty : s.kb_empty;
+    uint64_t* full = part_a ? s.ka_full : s.kb_full;
     int gj = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
@@ -178,41 +179,40 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         const int st = gj % NS;
         const uint32_t ph = ((gj / NS) & 1) ^ 1;
         const uint32_t stage = smem_u32(s.kv[st]);
-        ok = __all_sync(kFullMask, mbar_wait(&s.ka_empty[st], ph, abort_flag));
+        ok = __all_sync(kFullMask, mbar_wait(&empty[st], ph, abort_flag));
         if (!ok) break;
-        // The tile's 64 indices, two per lane, each checked once.
+        // The tile's 64 indices, two per lane; masked slots fetch row 0.
         int64_t e2[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int slot = BNK * j + 32 * h + lane;
           const int64_t e = slot < p.topk ? (int64_t)__ldg(p.idx + (int64_t)i * p.topk + slot) : -1;
-          if (gw == 0 && (e < -1 || e >= a.Tk)) report_status(a.dev_status, CPATTN_ERR_BAD_INDEX);
+          if (part_a && gw == 0 && (e < -1 || e >= a.Tk))
+            report_status(a.dev_status, CPATTN_ERR_BAD_INDEX);
           e2[h] = (e >= 0 && e < a.Tk && e >= iv.lo && e <= iv.hi) ? e : 0;
         }
-        // part A: 40 pieces per row
-        for (int t = gw; t < BNK; t += 6) {
-          const __nv_bfloat16* src =
-              kbase + __shfl_sync(kFullMask, t < 32 ? e2[0] : e2[1], t & 31) * a.k_stride_t;
+        if (part_a) {
+          // 40 pieces per row
+          for (int t = gw; t < BNK; t += 3) {
+            const __nv_bfloat16* src =
+                kbase + __shfl_sync(kFullMask, t < 32 ? e2[0] : e2[1], t & 31) * a.k_stride_t;
 #pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int pc = lane + 32 * k;
-            if (pc < 40) {
-              const int q = pc >> 3;
-              const int ch = hc == 0 ? 4 + q : (q < 4 ? q : 8);
-              const uint32_t dst = stage + ch * kKChunkBytes + t * 128 + (((pc & 7) ^ (t & 7)) << 4);
-              asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
-                           "l"(src + 64 * ch + 8 * (pc & 7))
-                           : "memory");
+            for (int k = 0; k < 2; ++k) {
+              const int pc = lane + 32 * k;
+              if (pc < 40) {
+                const int q = pc >> 3;
+                const int ch = hc == 0 ? 4 + q : (q < 4 ? q : 8);
+                const uint32_t dst = stage + ch * kKChunkBytes + t * 128 + (((pc & 7) ^ (t & 7)) << 4);
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                             "l"(src + 64 * ch + 8 * (pc & 7))
+                             : "memory");
+              }
             }
           }
-        }
-        cp_async_mbar_arrive_noinc(&s.ka_full[st]);
-        // part B: 32 pieces per row, one per lane
-        ok = __all_sync(kFullMask, mbar_wait(&s.kb_empty[st], ph, abort_flag));
-        if (!ok) break;
-        {
+        } else {
+          // 32 pieces per row, one per lane
           const int ch = 4 * hc + (lane >> 3);
-          for (int t = gw; t < BNK; t += 6) {
+          for (int t = gw; t < BNK; t += 3) {
             const __nv_bfloat16* src =
                 kbase + __shfl_sync(kFullMask, t < 32 ? e2[0] : e2[1], t & 31) * a.k_stride_t;
             const uint32_t dst = stage + ch * kKChunkBytes + t * 128 + (((lane & 7) ^ (t & 7)) << 4);
@@ -221,7 +221,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
                          : "memory");
           }
         }
-        cp_async_mbar_arrive_noinc(&s.kb_full[st]);
+        cp_async_mbar_arrive_noinc(&full[st]);
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -284,6 +284,10 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
             umma4_ss_k<1>(d, qs_lo + 4 * kQC, kb + 8 * kC, idesc_s);
           }
           umma_commit(&s.ka_empty[st]);
+          // PV of the previous tile goes between the two parts of S, so that
+          // its value chunks are released as early as possible.
+          if (prev >= 0 && !issue_pv()) { ok = false; break; }
+          prev = -1;
           if (!mbar_wait(&s.kb_full[st], ph, abort_flag)) { ok = false; break; }
           fence_proxy_async_smem();
           tc_fence_after();
@@ -298,7 +302,6 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
           }
           umma_commit(&s.s_full[gj & 1]);
           if (j == T - 1) umma_commit(&s.qs_empty);
-          if (prev >= 0 && !issue_pv()) { ok = false; break; }
           prev = gj;
           prev_first = (j == 0);
           prev_last = (j == T - 1);

@@ -76,13 +76,15 @@ class DenseRunner:
             self.q, self.k, self.v = (t.to(device) for t in (w.q, w.k, w.v))
             self.o = torch.empty((Tq, Hq, w.v.shape[2]), dtype=torch.bfloat16, device=device)
             self.lse = torch.empty((Tq, Hq), dtype=torch.float32, device=device)
+            self.ws = torch.empty(64 << 20, dtype=torch.uint8, device=device)   # per-piece summaries
 
     def step(self, q=None, k=None, v=None):
         from context_attention_softmax_gb300 import cpattn_chunk_fwd
         w = self.w
         cpattn_chunk_fwd(q if q is not None else self.q, k if k is not None else self.k,
                          v if v is not None else self.v, scale=w.scale, causal=True,
-                         causal_offset=w.causal_offset, out=self.o, lse=self.lse)
+                         causal_offset=w.causal_offset, out=self.o, lse=self.lse,
+                         workspace=self.ws)
 
     # host buffers for the end-to-end measurement
     def host_inputs(self):

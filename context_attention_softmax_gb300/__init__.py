@@ -92,9 +92,10 @@ def _args(q, k, v, scale, causal, causal_offset, cu_seqlens, q_chunk_map, kv_chu
 def cpattn_chunk_fwd(q, k, v, scale=None, causal=True, causal_offset=0, cu_seqlens=None,
                      q_chunk_map=None, kv_chunk_map=None, chunk_len=0, kv_chunk_len=0,
                      out=None, lse=None, partial_o=None, partial_lse=None, dev_status=None,
-                     stream=None):
+                     workspace=None, stream=None):
     """Dense CP-chunk attention; returns (out, lse) or, with kv_chunk_len > 0,
-    (out, lse, partial_o, partial_lse)."""
+    (out, lse, partial_o, partial_lse).  `workspace` (uint8, device) enables
+    the SM-balanced schedule; one is allocated when it is missing or short."""
     dev = q.device
     cu, qm, km = (_device_i32(x, dev) for x in (cu_seqlens, q_chunk_map, kv_chunk_map))
     Tq, Hq = q.shape[0], q.shape[1]
@@ -110,7 +111,12 @@ def cpattn_chunk_fwd(q, k, v, scale=None, causal=True, causal_offset=0, cu_seqle
             partial_lse = torch.empty((n, Tq, Hq), dtype=torch.float32, device=dev)
     a = _args(q, k, v, scale, causal, causal_offset, cu, qm, km, chunk_len, out, lse,
               kv_chunk_len, partial_o, partial_lse, dev_status)
-    _lib.check(_lib.load().cpattn_chunk_fwd(ctypes.byref(a), None, 0, _stream(stream)))
+    lib = _lib.load()
+    ws_bytes = lib.cpattn_workspace_size(_lib.OP_CHUNK_FWD, ctypes.byref(a), 0, 1)
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _lib.check(lib.cpattn_chunk_fwd(ctypes.byref(a), _ptr(workspace) if ws_bytes else None,
+                                    ws_bytes, _stream(stream)))
     if kv_chunk_len > 0:
         return out, lse, partial_o, partial_lse
     return out, lse

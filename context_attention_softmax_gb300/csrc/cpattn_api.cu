@@ -117,8 +117,6 @@ extern "C" {
 
 cpattn_status cpattn_chunk_fwd(const cpattn_attn_args* a, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   TRY(check_attn(a, true, true));
   CHECK(a->kv_chunk_len >= 0, CPATTN_ERR_INVALID_ARG, "kv_chunk_len=%d must be >= 0", a->kv_chunk_len);
   if (a->kv_chunk_len > 0 && a->Tk > 0 && (int64_t)a->Tq * a->Hq > 0)
@@ -127,7 +125,9 @@ cpattn_status cpattn_chunk_fwd(const cpattn_attn_args* a, void* workspace, size_
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (dense_tc_supported(*a)) {
     bool launched = false;
-    cudaError_t e = launch_dense_tc(*a, st, &launched);
+    cudaError_t e = launch_dense_tc_bal(*a, workspace, workspace_bytes, st, &launched);
+    if (e != cudaSuccess || launched) return cuda_status(e, "cpattn_chunk_fwd tensor-core launch");
+    e = launch_dense_tc(*a, st, &launched);
     if (e != cudaSuccess || launched) return cuda_status(e, "cpattn_chunk_fwd tensor-core launch");
   }
   SparseArgs none{nullptr, 0, 1, 1};
@@ -207,6 +207,7 @@ cpattn_status cpattn_block_gate(const cpattn_attn_args* a, int32_t block_size, i
 size_t cpattn_workspace_size(int32_t op, const cpattn_attn_args* a, int32_t topk, int32_t block_size) {
   if (a == nullptr) return 0;
   if (op == CPATTN_OP_BLOCK_GATE) return block_size > 0 ? block_gate_workspace(*a, block_size) : 0;
+  if (op == CPATTN_OP_CHUNK_FWD) return a->kv_chunk_len == 0 ? dense_tc_bal_workspace(*a) : 0;
   if (op == CPATTN_OP_TOPK_SPARSE_FWD && block_size > 1 && topk > 0 &&
       moba_tc_supported(*a, 1, block_size, topk))
     return moba_tc_workspace(*a, topk, block_size);

@@ -35,6 +35,12 @@ cudaError_t launch_lse_merge(int32_t n_parts, const float* part_o, const float* 
 // described by TMA tensor maps (the caller then uses the general kernel).
 bool dense_tc_supported(const cpattn_attn_args& a);
 cudaError_t launch_dense_tc(const cpattn_attn_args& a, cudaStream_t stream, bool* launched);
+// Balanced schedule of the dense tensor-core kernel (no KV chunk map): the
+// workspace it needs (0 when it does not apply) and its launch; `launched`
+// stays false when the workspace is missing or too small.
+size_t dense_tc_bal_workspace(const cpattn_attn_args& a);
+cudaError_t launch_dense_tc_bal(const cpattn_attn_args& a, void* ws, size_t ws_bytes,
+                                cudaStream_t stream, bool* launched);
 // Block-grouped MoBA attention on the tensor cores (bf16, d = 128, block
 // size a multiple of 128, keys in logical order).  `sel` is the block list
 // [Tq, index_heads, slots]; writes o and lse through partial summaries and

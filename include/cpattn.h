@@ -134,7 +134,13 @@ typedef struct cpattn_attn_args {
  * globally" para 1-5; "[Feature-request] Context Parallel support for
  * DSAttention", allgather CP mode (causal_offset).
  * Computes o [Tq, Hq, Dv] and lse [Tq, Hq] (and the partial summaries when
- * kv_chunk_len > 0).  Needs no workspace (workspace may be NULL, size 0).
+ * kv_chunk_len > 0).  Workspace is optional: with at least
+ * cpattn_workspace_size(CPATTN_OP_CHUNK_FWD, ...) bytes (device memory, no
+ * initialisation needed, not touched by the host) the KV work of all query
+ * blocks is spread evenly over the SMs and blocks cut between CTAs are
+ * merged in the kernel; with NULL or fewer bytes every CTA takes whole
+ * blocks.  Both give the same results up to fp32 summation order.  Calls
+ * sharing one workspace must be ordered on a stream.
  * Limits: Dqk, Dv multiples of 8, Dqk <= 1024, Dv <= 512; chunk maps need
  * chunk_len > 0.
  */
@@ -233,8 +239,9 @@ cpattn_status cpattn_block_gate(const cpattn_attn_args* args, int32_t block_size
 cpattn_status cpattn_block_gate_static(const cpattn_attn_args* args, int32_t block_size,
                                        int32_t topk, int32_t* sel, void* stream);
 
-/* Bytes of device workspace the call needs (0 if none).  `args` supplies the
- * shapes; topk and block_size as passed to the call. */
+/* Bytes of device workspace the call needs (0 if none; for
+ * CPATTN_OP_CHUNK_FWD the bytes that enable the SM-balanced schedule).
+ * `args` supplies the shapes; topk and block_size as passed to the call. */
 size_t cpattn_workspace_size(int32_t op, const cpattn_attn_args* args, int32_t topk,
                              int32_t block_size);
 

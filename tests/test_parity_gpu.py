@@ -11,6 +11,7 @@ import pytest
 import torch
 
 import oracle as orc
+import context_attention_softmax_gb300 as pkg
 from context_attention_softmax_gb300 import (cpattn_block_gate, cpattn_chunk_fwd,
                                              cpattn_lse_merge, cpattn_topk_sparse_fwd, inputs)
 
@@ -58,6 +59,8 @@ def test_tiny_fp32_two_summaries_then_merge():
     (300, 1000, 700, 4, 2, 0),       # single pass (tensor-core path), ragged tails
     (257, 1300, 700, 4, 1, 0),
     (1, 129, 128, 1, 1, 0),          # one query, one key past a tile edge
+    (128, 8192, 8064, 2, 2, 0),      # two long units over far more CTAs than tiles each
+    (600, 3000, 2500, 8, 2, 0),      # head pairs, units cut across several CTAs
 ])
 def test_dense_gqa_small(Tq, Tk, off, Hq, Hkv, kvc):
     rng_w = inputs.dense_gqa(seed=1, global_seq=Tq, cp_size=1, rank=0, Hq=Hq, Hkv=Hkv, Tk=Tk,
@@ -296,3 +299,23 @@ def test_lse_merge_neutral_parts():
                               out_dtype=torch.float32)
     assert_matches(o, lse, O, L, "fp32", "lse_merge")
     assert (o[20] == 0).all() and torch.isneginf(lse[20]).all()
+
+
+def test_dense_per_unit_schedule_without_workspace():
+    """Without a workspace the one-unit-per-CTA kernel runs; same answer."""
+    import ctypes
+    from context_attention_softmax_gb300 import _lib
+    w = inputs.dense_gqa(seed=3, global_seq=640, cp_size=1, rank=0, Hq=4, Hkv=2, Tk=1500,
+                         kv_chunks=0)
+    w.causal_offset = 900
+    q, k, v = f64(w)
+    O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w))
+    dev = torch.device("cuda")
+    qd, kd, vd = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    o = torch.empty((qd.shape[0], qd.shape[1], vd.shape[2]), dtype=qd.dtype, device=dev)
+    lse = torch.empty((qd.shape[0], qd.shape[1]), dtype=torch.float32, device=dev)
+    a = pkg._args(qd, kd, vd, w.scale, True, w.causal_offset, None, None, None, 0, o, lse)
+    lib = _lib.load()
+    _lib.check(lib.cpattn_chunk_fwd(ctypes.byref(a), None, 0, torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert_matches(o, lse, O, L, "bf16", "per-unit schedule")

@@ -242,7 +242,7 @@ gate_select_kernel(const cpattn_attn_args a, int B, int n_blocks, int topk,
 
 template <typename T>
 cudaError_t launch_gate_t(const cpattn_attn_args& a, int B, int topk, int32_t* sel, void* ws,
-                          cudaStream_t stream) {
+                          size_t ws_bytes, cudaStream_t stream) {
   const int n_blocks = a.Tk / B;
   const int D = a.Dqk;
   const size_t n_mu = (size_t)n_blocks * a.Hkv * D;
@@ -253,6 +253,11 @@ cudaError_t launch_gate_t(const cpattn_attn_args& a, int B, int topk, int32_t* s
         reinterpret_cast<const T*>(a.k), a.k_stride_t, a.k_stride_h, a.Hkv, D, B, mu64, mu32);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+  }
+  if (n_blocks > 0 && gate_tc_supported(a, B, topk) && ws_bytes >= block_gate_workspace(a, B)) {
+    bool launched = false;
+    cudaError_t e = launch_gate_tc(a, B, topk, sel, mu64, mu32, mu32 + n_mu, stream, &launched);
+    if (e != cudaSuccess || launched) return e;
   }
   const size_t smem = block_gate_smem(n_blocks, D);
   auto kern = gate_select_kernel<T>;
@@ -267,17 +272,24 @@ cudaError_t launch_gate_t(const cpattn_attn_args& a, int B, int topk, int32_t* s
 
 size_t block_gate_smem(int n_blocks, int D) { return gate_smem_floats(n_blocks, D) * sizeof(float); }
 
-size_t block_gate_workspace(const cpattn_attn_args& a, int32_t block_size) {
+size_t block_gate_workspace_min(const cpattn_attn_args& a, int32_t block_size) {
   const size_t n_blocks = block_size > 0 ? (size_t)(a.Tk / block_size) : 0;
   return n_blocks * a.Hkv * a.Dqk * (sizeof(double) + sizeof(float));
 }
 
+size_t block_gate_workspace(const cpattn_attn_args& a, int32_t block_size) {
+  size_t n = block_gate_workspace_min(a, block_size);
+  if (block_size > 0 && gate_tc_supported(a, block_size, 0)) n += gate_tc_parts_bytes(a, block_size);
+  return n;
+}
+
 cudaError_t launch_block_gate(const cpattn_attn_args& a, int32_t block_size, int32_t topk,
-                              int32_t* sel, void* workspace, cudaStream_t stream) {
+                              int32_t* sel, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
   if ((int64_t)a.Tq * a.Hq == 0) return cudaSuccess;
   if (a.dtype == CPATTN_BF16)
-    return launch_gate_t<__nv_bfloat16>(a, block_size, topk, sel, workspace, stream);
-  return launch_gate_t<float>(a, block_size, topk, sel, workspace, stream);
+    return launch_gate_t<__nv_bfloat16>(a, block_size, topk, sel, workspace, workspace_bytes, stream);
+  return launch_gate_t<float>(a, block_size, topk, sel, workspace, workspace_bytes, stream);
 }
 
 }  // namespace cpattn

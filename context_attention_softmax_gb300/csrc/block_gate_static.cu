@@ -62,7 +62,7 @@ extern "C" cpattn_status cpattn_block_gate_static(const cpattn_attn_args* args,
   if (args == nullptr || block_size < 1 || args->Tk < 0 || args->Hkv < 1 || args->Dqk < 1)
     // malformed arguments: the regular entry point rejects them with its message
     return cpattn_block_gate(args, block_size, topk, sel, nullptr, 0, stream);
-  const size_t need = cpattn_workspace_size(CPATTN_OP_BLOCK_GATE, args, topk, block_size);
+  const size_t need = block_gate_workspace_min(*args, block_size);
   if (need > kStaticScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),

@@ -195,11 +195,11 @@ cpattn_status cpattn_block_gate(const cpattn_attn_args* a, int32_t block_size, i
   const int n_blocks = a->Tk / block_size;
   CHECK(block_gate_smem(n_blocks, a->Dqk) <= 200 * 1024, CPATTN_ERR_UNSUPPORTED,
         "%d blocks of head dim %d do not fit the gate's shared-memory staging", n_blocks, a->Dqk);
-  const size_t need = block_gate_workspace(*a, block_size);
+  const size_t need = block_gate_workspace_min(*a, block_size);
   CHECK(workspace_bytes >= need && (need == 0 || workspace != nullptr), CPATTN_ERR_WORKSPACE,
         "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
   if (need > 0) CHECK(aligned16(workspace), CPATTN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
-  return cuda_status(launch_block_gate(*a, block_size, topk, sel, workspace,
+  return cuda_status(launch_block_gate(*a, block_size, topk, sel, workspace, workspace_bytes,
                                        reinterpret_cast<cudaStream_t>(stream)),
                      "cpattn_block_gate launch");
 }

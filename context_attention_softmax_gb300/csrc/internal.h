@@ -57,9 +57,19 @@ cudaError_t launch_moba_tc(const cpattn_attn_args& a, const int32_t* sel, int32_
 bool dsa_tc_supported(const cpattn_attn_args& a, int32_t index_heads, int32_t block_size);
 cudaError_t launch_dsa_tc(const cpattn_attn_args& a, const int32_t* indices, int32_t topk,
                           cudaStream_t stream, bool* launched);
+// Workspace of the block gate: the preferred size (with it, bf16 queries of
+// head dim 128 over at most 128 blocks use the tensor-core gate) and the
+// minimum (block means only).
 size_t block_gate_workspace(const cpattn_attn_args& a, int32_t block_size);
+size_t block_gate_workspace_min(const cpattn_attn_args& a, int32_t block_size);
+bool gate_tc_supported(const cpattn_attn_args& a, int32_t block_size, int32_t topk);
+size_t gate_tc_parts_bytes(const cpattn_attn_args& a, int32_t block_size);
+cudaError_t launch_gate_tc(const cpattn_attn_args& a, int32_t block_size, int32_t topk, int32_t* sel,
+                           const double* mu64, const float* mu32, void* parts, cudaStream_t stream,
+                           bool* launched);
 size_t block_gate_smem(int n_blocks, int D);
 cudaError_t launch_block_gate(const cpattn_attn_args& a, int32_t block_size, int32_t topk,
-                              int32_t* sel, void* workspace, cudaStream_t stream);
+                              int32_t* sel, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
 
 }  // namespace cpattn

@@ -117,8 +117,9 @@ def test_sparse_and_gate_validation(lib):
     assert lib.cpattn_topk_sparse_fwd(ctypes.byref(a), 0x7000, 8, 1, 1, None, 0, None) == 2
     g = _valid_args()
     need = lib.cpattn_workspace_size(2, ctypes.byref(g), 3, 64)
-    # fp64 + fp32 block means, plus the three bf16 mean terms of the tensor-core gate
-    assert need == (256 // 64) * 4 * 128 * (12 + 6)
+    # fp64 + fp32 block means, plus the three bf16 mean terms and the fp32
+    # mean norms of the tensor-core gate
+    assert need == (256 // 64) * 4 * (128 * (12 + 6) + 4)
     assert lib.cpattn_block_gate(ctypes.byref(g), 64, 3, 0x8000, None, 0, None) == 4
     assert lib.cpattn_block_gate(ctypes.byref(g), 64, 65, 0x8000, 0x9000, need, None) == 2
     g.cu_seqlens, g.num_seqs = 0x6000, 2

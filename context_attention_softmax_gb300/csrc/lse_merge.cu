@@ -19,6 +19,7 @@ namespace cpattn {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kMaxUnrolled = 8;   // parts merged with all loads in flight
 
 template <typename TO>
 __device__ __forceinline__ void store4(TO* p, float4 v);
@@ -46,6 +47,46 @@ lse_merge_kernel(int n_parts, const float* __restrict__ part_o, const float* __r
   if (row >= rows) return;
   const int64_t t = row / H;
   const int h = (int)(row - t * H);
+
+  if (n_parts <= kMaxUnrolled && Dv == 128) {
+    // every part's LSE, then every part's 4 channels of this lane, in flight together
+    float lc[kMaxUnrolled];
+#pragma unroll
+    for (int c = 0; c < kMaxUnrolled; ++c)
+      lc[c] = c < n_parts ? __ldg(part_lse + (int64_t)c * rows + row) : -CUDART_INF_F;
+    float L = lc[0];
+#pragma unroll
+    for (int c = 1; c < kMaxUnrolled; ++c) L = fmaxf(L, lc[c]);
+    TO* orow = o + t * ost + h * osh + lane * 4;
+    if (L == -CUDART_INF_F) {
+      store4<TO>(orow, make_float4(0.f, 0.f, 0.f, 0.f));
+      if (lane == 0 && lse != nullptr) lse[row] = -CUDART_INF_F;
+      return;
+    }
+    float4 x[kMaxUnrolled];
+    float w[kMaxUnrolled];
+#pragma unroll
+    for (int c = 0; c < kMaxUnrolled; ++c) {
+      w[c] = (lc[c] == -CUDART_INF_F) ? 0.f : expf(lc[c] - L);
+      x[c] = w[c] != 0.f
+                 ? __ldg(reinterpret_cast<const float4*>(part_o + ((int64_t)c * rows + row) * Dv) + lane)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxUnrolled; ++c) {
+      wsum += w[c];
+      acc.x = fmaf(w[c], x[c].x, acc.x);
+      acc.y = fmaf(w[c], x[c].y, acc.y);
+      acc.z = fmaf(w[c], x[c].z, acc.z);
+      acc.w = fmaf(w[c], x[c].w, acc.w);
+    }
+    const float inv = 1.f / wsum;
+    store4<TO>(orow, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    if (lane == 0 && lse != nullptr) lse[row] = L + logf(wsum);
+    return;
+  }
 
   float L = -CUDART_INF_F;
   for (int c = lane; c < n_parts; c += 32) L = fmaxf(L, __ldg(part_lse + (int64_t)c * rows + row));

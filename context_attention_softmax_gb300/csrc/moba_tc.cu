@@ -39,11 +39,15 @@ using namespace sm100;
 
 constexpr int BM = 128, BN = 128, HD = 128;
 constexpr int NS = 2;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+// Register split at a launch budget of 168 x 384: control warps 64, softmax
+// warps 216, epilogue warps 80.
+constexpr uint32_t kRegsControl = 64, kRegsSoftmax = 216, kRegsEpilogue = 80;
+static_assert(128 * (kRegsControl + kRegsSoftmax + kRegsEpilogue) <= 168 * kThreads, "register split");
 constexpr uint32_t kTileBytes = BN * HD * 2;   // 32 KiB
 constexpr uint32_t kHalf = 16384;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;     // S double buffer at 0 / 128, O at 256
+constexpr uint32_t kColS = 0, kColO = 256;     // S double buffer at 0 / 128, O double buffer at 256 / 384
 constexpr float kRescaleThreshold = 8.f;
 
 struct MobaWs {
@@ -208,7 +212,8 @@ struct MSmem {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
   uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, o_full, o_free, drain;
+  uint64_t pv_done, o_full[2], o_free[2], st_full[2], drain;
+  float4 stats[2][BM];             // (m, l, lb) of each row at the end of a unit
   uint32_t tmem_base;
   int abort;
 };
@@ -273,8 +278,11 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       mbar_init(&s.v_empty[i], 1);
     }
     mbar_init(&s.pv_done, 1);
-    mbar_init(&s.o_full, 1);
-    mbar_init(&s.o_free, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.o_full[i], 1);
+      mbar_init(&s.o_free[i], 128);
+      mbar_init(&s.st_full[i], 128);
+    }
     mbar_init(&s.drain, 1);
     s.abort = 0;
     fence_mbar_init();
@@ -292,6 +300,8 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
+  if (warp < 4) {
+  regs_dec<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------------ K/V producer
     if (lane == 0) {
@@ -372,16 +382,20 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const int j = prev;
         if (!mbar_wait(&s.p_full[j & 1], (j >> 1) & 1, abort_flag) ||
             !mbar_wait(&s.v_full[j % NS], (j / NS) & 1, abort_flag)) return false;
-        if (prev_first && prev_ui > 0 &&
-            !mbar_wait(&s.o_free, (prev_ui - 1) & 1, abort_flag)) return false;
+        // O of unit u lives in buffer u & 1; its first PV waits until the
+        // epilogue has read unit u - 2 out of that buffer
+        const int ob = prev_ui & 1;
+        if (prev_first && prev_ui >= 2 &&
+            !mbar_wait(&s.o_free[ob], ((prev_ui - 2) >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t vb = (j % NS) ? v_lo1 : v_lo0;
         const uint32_t pa = tmem + kColS + (j & 1) * BN;
-        if (prev_first) umma8_ts_mnmajor<0>(tmem + kColO, pa, vb, idesc_pv);
-        else umma8_ts_mnmajor<1>(tmem + kColO, pa, vb, idesc_pv);
+        const uint32_t od = tmem + kColO + ob * HD;
+        if (prev_first) umma8_ts_mnmajor<0>(od, pa, vb, idesc_pv);
+        else umma8_ts_mnmajor<1>(od, pa, vb, idesc_pv);
         umma_commit(&s.v_empty[j % NS]);
         umma_commit(&s.pv_done);
-        if (prev_last) umma_commit(&s.o_full);
+        if (prev_last) umma_commit(&s.o_full[ob]);
         return true;
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
@@ -409,8 +423,10 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
+  }
+  } else if (warp < 8) {
+    regs_inc<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale * 1.4426950408889634f;
@@ -507,7 +523,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
 #pragma unroll
           for (int c4 = 0; c4 < HD / 32; ++c4) {
             uint32_t oo[32];
-            const uint32_t addr = tmem + lane_base + kColO + c4 * 32;
+            const uint32_t addr = tmem + lane_base + kColO + (ui & 1) * HD + c4 * 32;
             tmem_ld32_sync(addr, oo);
 #pragma unroll
             for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
@@ -519,18 +535,44 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         mbar_arrive(&s.p_full[jt & 1]);
       }
       if (!ok) break;
-      ok = __all_sync(kFullMask, mbar_wait(&s.o_full, ui & 1, abort_flag));
+      // the row's running summary to the epilogue warps
+      s.stats[ui & 1][r] = make_float4(m2, l, lb, 0.f);
+      mbar_arrive(&s.st_full[ui & 1]);
+    }
+  } else {
+    regs_dec<kRegsEpilogue>();
+    // ------------------------------------------------------------ epilogue
+    // Finalised summary (O_c, LSE_c) of each (query, head, slot) of a unit,
+    // from O in TMEM buffer ui & 1 and the row's (m, l, lb); the softmax
+    // warps meanwhile run the next unit.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    int ui = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
+      const int4 un = p.units[u];
+      const int ob = ui & 1;
+      ok = __all_sync(kFullMask, mbar_wait(&s.o_full[ob], (ui >> 1) & 1, abort_flag) &&
+                                     mbar_wait(&s.st_full[ob], (ui >> 1) & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      // epilogue: finalised summary of (query, head, slot)
-      const bool live = row_live && l > 0.f;
-      const float inv = (live && lb > 0.f) ? 1.f / lb : 0.f;
+      const float4 st = s.stats[ob][r];
+      const bool row_live = r < un.w;
+      int64_t q = 0;
+      int slot = 0;
+      if (row_live) {
+        const int32_t e = __ldg(p.lists + un.z + r);
+        q = e / p.S;
+        slot = e - (int)q * p.S;
+      }
+      const bool live = row_live && st.y > 0.f;
+      const float inv = (live && st.z > 0.f) ? 1.f / st.z : 0.f;
       const int64_t prow = ((int64_t)slot * a.Tq + q) * a.Hq + un.x;
       float* orow = p.part_o + prow * HD;
 #pragma unroll
       for (int c4 = 0; c4 < HD / 32; ++c4) {
         uint32_t oo[32];
-        tmem_ld32_sync(tmem + lane_base + kColO + c4 * 32, oo);
+        tmem_ld32_sync(tmem + lane_base + kColO + ob * HD + c4 * 32, oo);
         if (row_live) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
@@ -539,9 +581,9 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                             __uint_as_float(oo[i + 2]) * inv, __uint_as_float(oo[i + 3]) * inv);
         }
       }
-      if (row_live) p.part_lse[prow] = live ? (m2 + log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+      if (row_live) p.part_lse[prow] = live ? (st.x + log2f(st.y)) * 0.6931471805599453f : -CUDART_INF_F;
       tc_fence_before();
-      mbar_arrive(&s.o_free);
+      mbar_arrive(&s.o_free[ob]);
     }
   }
 

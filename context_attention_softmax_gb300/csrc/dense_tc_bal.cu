@@ -12,13 +12,13 @@
 // para 3) to the workspace, and the CTA that finishes the unit's last piece
 // merges the pieces by rescaling to the larger max and writes O and LSE.
 //
-// The stream needs every unit's live-tile count in every CTA.  Without a KV
-// chunk map the live tiles of a unit are one contiguous range, found from
-// the permitted intervals of its first and last valid rows (intervals are
-// monotone in the query position: packed-sequence bounds and the causal cut
-// both grow with it), so each CTA derives all counts itself in a few
-// hundred cycles and no grid-wide step is needed.  With a KV chunk map the
-// launcher keeps the one-unit-per-CTA kernel.
+// The stream needs every unit's live-tile count in every CTA.  A unit's
+// permitted keys are one interval of logical positions, found from the
+// intervals of its first and last valid rows (they are monotone in the
+// query position: packed-sequence bounds and the causal cut both grow with
+// it).  Without a KV chunk map its live tiles are one range of tiles; with
+// one, a range inside every chunk whose logical keys meet the interval.  So
+// each CTA derives all counts itself and no grid-wide step is needed.
 //
 // Pieces of a unit are counted on a per-unit word in the workspace whose high
 // half carries a per-launch tag, so stale words from earlier launches read as
@@ -61,7 +61,6 @@ struct BalSmem {
   int abort;
   int merge;                       // this CTA finishes the current unit
   int scan[kThreads / 32];
-  int kt_lo[kMaxUnits];            // first live KV tile of each unit
   int pref[kMaxUnits + 1];         // exclusive prefix of live-tile counts; pref[n] = W
 };
 
@@ -87,6 +86,91 @@ __device__ bool block_bounds(const cpattn_attn_args& a, int q0, int64_t& lo, int
   hi = ib.hi;
   return lo <= hi;
 }
+
+// Permitted key interval of work unit u (both blocks).
+__device__ bool unit_bounds(const BalParams& p, int u, int64_t& lo, int64_t& hi) {
+  lo = INT64_MAX;
+  hi = INT64_MIN;
+  for (int x = 0; x < 2; ++x) {
+    const Block b = block_of(p.a.Hq, p.head_pairs, p.n_qtiles, u, x);
+    int64_t l, h;
+    if (block_bounds(p.a, b.q0, l, h)) {
+      lo = min(lo, l);
+      hi = max(hi, h);
+    }
+  }
+  return lo <= hi;
+}
+
+// The live KV tiles of a unit with permitted keys [lo, hi], in physical
+// order: per KV chunk (the whole key range when there is no chunk map) the
+// tiles whose logical keys meet [lo, hi], one range since a chunk's keys are
+// consecutive logical positions and tiles never straddle chunks.
+struct LiveTiles {
+  const cpattn_attn_args* a;
+  int64_t lo, hi;
+  int n_chunks, clen;   // chunks and keys per chunk (1 and Tk without a map)
+  int c, j, j1;         // cursor: chunk c, its tile j (last live one j1)
+  __device__ void init(const cpattn_attn_args& args, int64_t l, int64_t h) {
+    a = &args;
+    lo = l;
+    hi = h;
+    if (args.kv_chunk_map != nullptr) {
+      n_chunks = (args.Tk + args.chunk_len - 1) / args.chunk_len;
+      clen = args.chunk_len;
+    } else {
+      n_chunks = 1;
+      clen = args.Tk;
+    }
+    c = -1;
+    j = j1 = 0;
+  }
+  // live tiles [t0, t1] of chunk cc within the chunk; false if none
+  __device__ bool range(int cc, int& t0, int& t1) const {
+    const int64_t start = (int64_t)cc * clen;
+    const int64_t len = min((int64_t)clen, (int64_t)a->Tk - start);
+    const int64_t L = a->kv_chunk_map != nullptr ? (int64_t)__ldg(a->kv_chunk_map + cc) * clen : 0;
+    const int64_t l = max(lo, L), h = min(hi, L + len - 1);
+    if (l > h) return false;
+    t0 = (int)((l - L) / BN);
+    t1 = (int)((h - L) / BN);
+    return true;
+  }
+  __device__ int count() const {
+    if (lo > hi) return 0;
+    int n = 0, t0, t1;
+    for (int cc = 0; cc < n_chunks; ++cc)
+      if (range(cc, t0, t1)) n += t1 - t0 + 1;
+    return n;
+  }
+  // place the cursor on the t-th live tile
+  __device__ void seek(int t) {
+    int t0, t1;
+    for (c = 0; c < n_chunks; ++c) {
+      if (!range(c, t0, t1)) continue;
+      if (t <= t1 - t0) {
+        j = t0 + t;
+        j1 = t1;
+        return;
+      }
+      t -= t1 - t0 + 1;
+    }
+  }
+  // current tile (physical index, logical position of its first key); advance
+  __device__ void next(int& kt, int64_t& kb) {
+    kt = (int)((int64_t)c * clen / BN) + j;
+    kb = (a->kv_chunk_map != nullptr ? (int64_t)__ldg(a->kv_chunk_map + c) * clen : 0) + (int64_t)j * BN;
+    if (++j > j1) {
+      int t0, t1;
+      for (++c; c < n_chunks; ++c)
+        if (range(c, t0, t1)) {
+          j = t0;
+          j1 = t1;
+          break;
+        }
+    }
+  }
+};
 
 // Largest u with pref[u] <= pos (pos < W, so pref[u + 1] > pos).
 __device__ __forceinline__ int unit_at(const int* pref, int n, int pos) {
@@ -382,25 +466,15 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tmem_relinquish();
   }
 
-  // Live KV tiles of every unit: one contiguous range [kt_lo, kt_lo + count).
+  // Live KV tiles of every unit.
   for (int u = threadIdx.x; u < nu; u += kThreads) {
-    int64_t lo = INT64_MAX, hi = INT64_MIN;
-    for (int x = 0; x < 2; ++x) {
-      const Block b = block_of(a.Hq, p.head_pairs, p.n_qtiles, u, x);
-      int64_t l, h;
-      if (block_bounds(a, b.q0, l, h)) {
-        lo = min(lo, l);
-        hi = max(hi, h);
-      }
+    int64_t lo, hi;
+    int count = 0;
+    if (unit_bounds(p, u, lo, hi)) {
+      LiveTiles lt;
+      lt.init(a, lo, hi);
+      count = lt.count();
     }
-    int first = 0, count = 0;
-    lo = max(lo, (int64_t)0);
-    hi = min(hi, (int64_t)a.Tk - 1);
-    if (lo <= hi) {
-      first = (int)(lo / BN);
-      count = (int)(hi / BN) - first + 1;
-    }
-    s.kt_lo[u] = first;
     s.pref[u] = count;
   }
   __syncthreads();
@@ -461,8 +535,14 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         tma_load_3d(s.q[1], &tm_q, &s.q_full, 0, b1.head, b1.q0);
         tma_load_3d(s.q[1] + kHalf, &tm_q, &s.q_full, 64, b1.head, b1.q0);
         ++pc;
+        int64_t ulo, uhi, kb;
+        unit_bounds(p, pw.u, ulo, uhi);
+        LiveTiles lt;
+        lt.init(a, ulo, uhi);
+        lt.seek(pw.t0);
         for (int t = pw.t0; t < pw.t1; ++t) {
-          const int kt = s.kt_lo[pw.u] + t;
+          int kt;
+          lt.next(kt, kb);
           const int st = gj % NS;
           const uint32_t ph = (gj / NS) & 1;
           if (!mbar_wait(&s.k_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
@@ -597,12 +677,15 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       KeyInterval iv{1, 0};
       if (tok < a.Tq) iv = allowed_interval(a, query_pos(a, tok));
       float m2 = -CUDART_INF_F, l = 0.f, lb = 0.f;
-      // the piece counter of the CTA's last (partial) piece, read while the
-      // piece runs
-
+      int64_t ulo, uhi;
+      unit_bounds(p, u, ulo, uhi);
+      LiveTiles lt;
+      lt.init(a, ulo, uhi);
+      lt.seek(pw.t0);
       for (int t = pw.t0; t < pw.t1 && ok; ++t) {
-        const int kt = s.kt_lo[u] + t;
-        const int64_t kbase = (int64_t)kt * BN;
+        int kt;
+        int64_t kbase;
+        lt.next(kt, kbase);
         const int kvalid = min(BN, a.Tk - kt * BN);
         int lo_c = 1, hi_c = 0;   // permitted columns of this row in this tile
         if (iv.lo <= iv.hi) {
@@ -813,10 +896,18 @@ int dense_units(const cpattn_attn_args& a, int* head_pairs) {
 }  // namespace
 
 size_t dense_tc_bal_workspace(const cpattn_attn_args& a) {
-  if (!dense_tc_supported(a) || a.kv_chunk_map != nullptr) return 0;
+  if (!dense_tc_supported(a)) return 0;
   int hp = 0;
   const int nu = dense_units(a, &hp);
   if (nu > kMaxUnits) return 0;
+  // Cutting units into pieces costs a Q reload, a partial summary and a merge
+  // per piece.  Measured on one GB300: with units filling more than 3/4 of
+  // the SMs (128 units on 152) one unit per CTA was 2 % faster, and on many
+  // short varlen units (256) 34 % faster; balancing pays when most SMs would
+  // otherwise idle.
+  if (4 * nu > 3 * dense_tc_grid()) return 0;
+  // every CTA counts every unit's tiles chunk by chunk
+  if (a.kv_chunk_map != nullptr && (int64_t)nu * a.n_kv_chunks > 131072) return 0;
   return dense_tc_bal_part_bytes(dense_tc_grid()) + (size_t)nu * sizeof(unsigned long long);
 }
 

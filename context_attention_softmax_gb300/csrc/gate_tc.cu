@@ -49,7 +49,6 @@ constexpr int kGateMaxTopk = 8;
 constexpr int kGateThreads = 320;
 constexpr uint32_t kQBox = GM * 128;          // one 64-channel box of a query tile: 16 KiB
 constexpr uint32_t kMuBoxMax = kGateMaxBlocks * 128;   // one 64-channel box of a mean term
-constexpr int kMaxU = kGateMaxBlocks;         // uncertain blocks (local memory, rarely more than k)
 
 struct GateTcParams {
   cpattn_attn_args a;

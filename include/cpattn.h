@@ -139,7 +139,8 @@ typedef struct cpattn_attn_args {
  * initialisation needed, not touched by the host) the KV work of all query
  * blocks is spread evenly over the SMs and blocks cut between CTAs are
  * merged in the kernel; with NULL or fewer bytes every CTA takes whole
- * blocks.  Both give the same results up to fp32 summation order.  Calls
+ * blocks.  The size is 0 (no workspace used) when the problem's 2-block
+ * work units already fill more than 3/4 of the device's SMs.  Both give the same results up to fp32 summation order.  Calls
  * sharing one workspace must be ordered on a stream.
  * Limits: Dqk, Dv multiples of 8, Dqk <= 1024, Dv <= 512; chunk maps need
  * chunk_len > 0.

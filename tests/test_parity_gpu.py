@@ -164,6 +164,34 @@ def test_zigzag_varlen_small():
     _zigzag_check(z)
 
 
+def _chunk_without_workspace(w):
+    """cpattn_chunk_fwd through the C ABI with no workspace: one unit per CTA."""
+    import ctypes
+    from context_attention_softmax_gb300 import _lib
+    q, k, v = to_gpu(w)
+    dev = q.device
+    cu, qm, km = (pkg._device_i32(x, dev) for x in (w.cu_seqlens, w.q_chunk_map, w.kv_chunk_map))
+    o = torch.empty((q.shape[0], q.shape[1], v.shape[2]), dtype=q.dtype, device=dev)
+    lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=dev)
+    a = pkg._args(q, k, v, w.scale, w.causal, w.causal_offset, cu, qm, km, w.chunk_len, o, lse)
+    _lib.check(_lib.load().cpattn_chunk_fwd(ctypes.byref(a), None, 0,
+                                            torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def test_zigzag_schedules_agree():
+    """Chunk maps: the SM-balanced schedule and one unit per CTA both match."""
+    z = inputs.zigzag_varlen(seed=5, total=4096, n_seqs=3, len_lo=256, len_hi=2048, cp_size=4, H=6)
+    w = z.rank_workload(1)
+    q, k, v = f64(w)
+    O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w))
+    o1, l1 = _chunk(w)
+    o2, l2 = _chunk_without_workspace(w)
+    assert_matches(o1, l1, O, L, "bf16", "balanced")
+    assert_matches(o2, l2, O, L, "bf16", "per unit")
+
+
 def test_zigzag_varlen_full_size_sampled():
     z = inputs.zigzag_varlen()
     _zigzag_check(z, rows_per_rank=12)

@@ -492,7 +492,9 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 2000 for our arm, so the clock sampler sees the "
+                         "timed region; 20 for the reference arm)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(RUNNERS), default="dense_gqa")
@@ -500,6 +502,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps is None:
+        args.steps = 20 if args.impl == "reference" else 2000
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":

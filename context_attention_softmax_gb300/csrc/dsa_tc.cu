@@ -344,9 +344,8 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         tc_fence_before();
         mbar_arrive(&s.qt_full);
       }
-      float m2 = -CUDART_INF_F, l = 0.f, lb = 0.f;
+      float m2 = -CUDART_INF_F, l = 0.f;
       for (int j = 0; j < T; ++j, ++gj) {
-        const int st = gj % NS;
         // column mask of the tile: the index is present, in range and
         // permitted for this query (lane holds keys lane and lane + 32)
         uint32_t m0, m1;
@@ -395,7 +394,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         }
         const float mref = (m2 == -CUDART_INF_F) ? 0.f : m2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mref, -mref);
-        uint64_t rs2[2] = {0ull, 0ull}, rsb2[2] = {0ull, 0ull};
+        uint64_t rs2[2] = {0ull, 0ull};
         uint32_t pk[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
@@ -404,15 +403,11 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           rs2[q & 1] = f2_add(rs2[q & 1], f2_pack(p0, p1));
           pk[q] = pack_bf16(p0, p1);
-          rsb2[q & 1] = f2_add(rsb2[q & 1], f2_pack(__uint_as_float(pk[q] << 16),
-                                                     __uint_as_float(pk[q] & 0xffff0000u)));
         }
         tmem_st32(s_col, pk);
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2_unpack(f2_add(rs2[0], rs2[1]), a0, a1);
-        f2_unpack(f2_add(rsb2[0], rsb2[1]), b0, b1);
         l = l * alpha + (a0 + a1);
-        lb = lb * alpha + (b0 + b1);
         if (__any_sync(kFullMask, rescale)) {
           ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (gj - 1) & 1, abort_flag));
           if (!ok) break;
@@ -435,9 +430,9 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
       ok = __all_sync(kFullMask, mbar_wait(&s.o_full, ui & 1, abort_flag));
       if (!ok) break;
       tc_fence_after();
-      // epilogue: O[i, r, 256c ...] = z / lb; LSE = m + ln l (half 0 writes it)
+      // epilogue: O[i, r, 256c ...] = z / l; LSE = m + ln l (half 0 writes it)
       const bool live = l > 0.f;
-      const float inv = (live && lb > 0.f) ? 1.f / lb : 0.f;
+      const float inv = live ? 1.f / l : 0.f;
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)i * a.o_stride_t +
                             (int64_t)r * a.o_stride_h + DVH * c;
 #pragma unroll 1

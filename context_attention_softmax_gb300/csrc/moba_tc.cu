@@ -213,7 +213,7 @@ struct MSmem {
   uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
   uint64_t s_full[2], p_full[2];
   uint64_t pv_done, o_full[2], o_free[2], st_full[2], drain;
-  float4 stats[2][BM];             // (m, l, lb) of each row at the end of a unit
+  float4 stats[2][BM];             // (m, l, -, -) of each row at the end of a unit
   uint32_t tmem_base;
   int abort;
 };
@@ -437,15 +437,13 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       const int T = unit_tiles(p, un.y);
       const bool row_live = r < un.w;
       int64_t q = 0;
-      int slot = 0;
       KeyInterval iv{1, 0};
       if (row_live) {
         const int32_t e = __ldg(p.lists + un.z + r);
         q = e / p.S;
-        slot = e - (int)q * p.S;
         iv = allowed_interval(a, query_pos(a, q));
       }
-      float m2 = -CUDART_INF_F, l = 0.f, lb = 0.f;
+      float m2 = -CUDART_INF_F, l = 0.f;
       for (int t = 0; t < T; ++t, ++jt) {
         const int64_t kbase = (int64_t)un.y * p.B + t * BN;
         const int kvalid = min(BN, a.Tk - (int)kbase);
@@ -493,7 +491,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
         const float mref = (m2 == -CUDART_INF_F) ? 0.f : m2;
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mref, -mref);
-        uint64_t rs2[2] = {0ull, 0ull}, rsb2[2] = {0ull, 0ull};
+        uint64_t rs2[2] = {0ull, 0ull};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
@@ -505,16 +503,12 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
             pk[c] = pack_bf16(p0, p1);
-            rsb2[c & 1] = f2_add(rsb2[c & 1], f2_pack(__uint_as_float(pk[c] << 16),
-                                                       __uint_as_float(pk[c] & 0xffff0000u)));
           }
           tmem_st32(s_col + 32 * half, pk);
         }
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2_unpack(f2_add(rs2[0], rs2[1]), a0, a1);
-        f2_unpack(f2_add(rsb2[0], rsb2[1]), b0, b1);
         l = l * alpha + (a0 + a1);
-        lb = lb * alpha + (b0 + b1);
         if (__any_sync(kFullMask, rescale)) {
           // O holds PV of this unit's earlier tiles: wait for the last one
           ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (jt - 1) & 1, abort_flag));
@@ -536,14 +530,14 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       }
       if (!ok) break;
       // the row's running summary to the epilogue warps
-      s.stats[ui & 1][r] = make_float4(m2, l, lb, 0.f);
+      s.stats[ui & 1][r] = make_float4(m2, l, 0.f, 0.f);
       mbar_arrive(&s.st_full[ui & 1]);
     }
   } else {
     regs_dec<kRegsEpilogue>();
     // ------------------------------------------------------------ epilogue
     // Finalised summary (O_c, LSE_c) of each (query, head, slot) of a unit,
-    // from O in TMEM buffer ui & 1 and the row's (m, l, lb); the softmax
+    // from O in TMEM buffer ui & 1 and the row's (m, l); the softmax
     // warps meanwhile run the next unit.
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -566,7 +560,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         slot = e - (int)q * p.S;
       }
       const bool live = row_live && st.y > 0.f;
-      const float inv = (live && st.z > 0.f) ? 1.f / st.z : 0.f;
+      const float inv = live ? 1.f / st.y : 0.f;
       const int64_t prow = ((int64_t)slot * a.Tq + q) * a.Hq + un.x;
       float* orow = p.part_o + prow * HD;
 #pragma unroll

@@ -7,7 +7,7 @@
 // unit per CTA leaves SMs idle.  Here the live KV tiles of all units form
 // one stream (unit by unit, tile by tile) and persistent CTA g takes stream
 // positions [g*W/G, (g+1)*W/G).  A unit cut by a segment boundary is
-// computed in pieces; each piece writes its running summary (m, l, lb, z)
+// computed in pieces; each piece writes its running summary (m, l, z)
 // ("Context parallel attention: exchange keys and merge softmax globally"
 // para 3) to the workspace, and the CTA that finishes the unit's last piece
 // merges the pieces by rescaling to the larger max and writes O and LSE.
@@ -31,7 +31,7 @@ namespace cpattn {
 namespace {
 
 constexpr int kMaxUnits = 2048;
-constexpr int kPartChunks = HD / 4 + 1;   // per row: 32 float4 of z, then (m in log2 units, l, lb, 0)
+constexpr int kPartChunks = HD / 4 + 1;   // per row: 32 float4 of z, then (m in log2 units, l, 0, 0)
 constexpr float kLn2 = 0.6931471805599453f;
 // The producer and MMA loops here also walk the piece list: 72 registers for
 // warpgroup 0 (128 * 72 + 256 * 216 = 64512 = 168 * 384).
@@ -59,7 +59,7 @@ struct BalSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int merge;                       // this CTA finishes the current unit
+  int merge[2];                    // this CTA finishes block X of the current unit
   int scan[kThreads / 32];
   int pref[kMaxUnits + 1];         // exclusive prefix of live-tile counts; pref[n] = W
 };
@@ -202,14 +202,16 @@ __device__ __forceinline__ int pieces_of(int ca, int cb, int64_t W, int G) {
   return n;
 }
 
-// Counts one finished piece of unit u on its tagged word; true for the piece
-// that completes the count (that CTA merges the unit).
-__device__ bool count_piece(const BalParams& p, int u, int n_pieces) {
-  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(p.pieces + u);
+// Counts one finished piece of block X of unit u on its tagged word (one
+// word per block, so the two blocks of a unit finish independently); true
+// for the piece that completes the count (that CTA merges the block).
+__device__ bool count_piece(const BalParams& p, int u, int X, int n_pieces) {
+  unsigned long long* word = p.pieces + 2 * u + X;
+  unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(word);
   for (int it = 0; it < (1 << 20); ++it) {
     const unsigned long long nxt =
         ((unsigned)(cur >> 32) == p.tag) ? cur + 1 : (((unsigned long long)p.tag << 32) | 1ull);
-    const unsigned long long seen = atomicCAS(p.pieces + u, cur, nxt);
+    const unsigned long long seen = atomicCAS(word, cur, nxt);
     if (seen == cur) return (int)(nxt & 0xffffffffull) == n_pieces;
     cur = seen;
   }
@@ -242,7 +244,7 @@ __device__ __noinline__ void merge_unit(const BalParams& p, int X, int r, int pr
   constexpr int kMaxP = 8;
   if (cb - ca + 1 > kMaxP) {
     // many pieces (a unit much longer than a segment): one piece at a time
-    float M = -CUDART_INF_F, L = 0.f, LB = 0.f;
+    float M = -CUDART_INF_F, L = 0.f;
     for (int c = ca; c <= cb; ++c) {
       const int64_t s0 = seg_start(c, W, G);
       if (seg_start(c + 1, W, G) == s0) continue;
@@ -251,11 +253,10 @@ __device__ __noinline__ void merge_unit(const BalParams& p, int X, int r, int pr
       const float Mn = fmaxf(M, st.x);
       const float a0 = ex2_approx(M - Mn), a1 = ex2_approx(st.x - Mn);
       L = L * a0 + st.y * a1;
-      LB = LB * a0 + st.z * a1;
       M = Mn;
     }
     const bool live = L > 0.f;
-    const float inv = (live && LB > 0.f) ? 1.f / LB : 0.f;
+    const float inv = live ? 1.f / L : 0.f;
 #pragma unroll 1
     for (int c8 = 0; c8 < HD / 8; ++c8) {
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -296,15 +297,14 @@ __device__ __noinline__ void merge_unit(const BalParams& p, int X, int r, int pr
 #pragma unroll
   for (int i = 0; i < kMaxP; ++i)
     if (st[i].y > 0.f) M = fmaxf(M, st[i].x);
-  float wt[kMaxP], L = 0.f, LB = 0.f;
+  float wt[kMaxP], L = 0.f;
 #pragma unroll
   for (int i = 0; i < kMaxP; ++i) {
     wt[i] = st[i].y > 0.f ? ex2_approx(st[i].x - M) : 0.f;
     L += st[i].y * wt[i];
-    LB += st[i].z * wt[i];
   }
   const bool live = L > 0.f;
-  const float inv = (live && LB > 0.f) ? 1.f / LB : 0.f;
+  const float inv = live ? 1.f / L : 0.f;
   // 64 columns at a time, two pieces per round: 32 loads in flight per thread
 #pragma unroll 1
   for (int c64 = 0; c64 < HD / 64; ++c64) {
@@ -352,7 +352,7 @@ __device__ __noinline__ void merge_unit(const BalParams& p, int X, int r, int pr
 // `write` says whether row r is a query row.
 __device__ __noinline__ void merge_unit_direct(const BalParams& p, int X, int r, int pref_u, int ca,
                                                int cb, int64_t W, int G, int self, bool ok,
-                                               float m_own, float l_own, float lb_own, uint32_t o_col,
+                                               float m_own, float l_own, uint32_t o_col,
                                                bool write, __nv_bfloat16* orow, float* lse_out) {
   constexpr int kMaxP = 8;
   const float4* rows[kMaxP];
@@ -372,53 +372,62 @@ __device__ __noinline__ void merge_unit_direct(const BalParams& p, int X, int r,
   for (int i = 0; i < kMaxP; ++i)
     if (st[i].y > 0.f) M = fmaxf(M, st[i].x);
   const float w_own = l_own > 0.f ? ex2_approx(m_own - M) : 0.f;
-  float wt[kMaxP], L = l_own * w_own, LB = lb_own * w_own;
+  float wt[kMaxP], L = l_own * w_own;
 #pragma unroll
   for (int i = 0; i < kMaxP; ++i) {
     wt[i] = st[i].y > 0.f ? ex2_approx(st[i].x - M) : 0.f;
     L += st[i].y * wt[i];
-    LB += st[i].z * wt[i];
   }
   const bool live = L > 0.f;
-  const float inv = (live && LB > 0.f) ? 1.f / LB : 0.f;
+  const float inv = live ? 1.f / L : 0.f;
+  // 64 columns per round: this piece's z from TMEM and the first other
+  // piece's z from the workspace are in flight together
 #pragma unroll 1
-  for (int c32 = 0; c32 < HD / 32; ++c32) {
-    float acc[32];
-    {
-      uint32_t oo[32];
-      tmem_ld32_sync(o_col + 32 * c32, oo);
+  for (int c64 = 0; c64 < HD / 64; ++c64) {
+    float4 z[16];
+    uint32_t oa[32], ob[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = w_own > 0.f ? __uint_as_float(oo[j]) * w_own : 0.f;
+    for (int j = 0; j < 16; ++j)
+      z[j] = np > 0 ? __ldcg(rows[0] + (16 * c64 + j) * BM) : make_float4(0.f, 0.f, 0.f, 0.f);
+    tmem_ld32(o_col + 64 * c64, oa);
+    tmem_ld32(o_col + 64 * c64 + 32, ob);
+    tmem_wait_ld();
+    float acc[64];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      acc[j] = w_own > 0.f ? __uint_as_float(oa[j]) * w_own : 0.f;
+      acc[32 + j] = w_own > 0.f ? __uint_as_float(ob[j]) * w_own : 0.f;
+    }
+    const float w0 = np > 0 ? wt[0] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      acc[4 * j] += z[j].x * w0;
+      acc[4 * j + 1] += z[j].y * w0;
+      acc[4 * j + 2] += z[j].z * w0;
+      acc[4 * j + 3] += z[j].w * w0;
     }
 #pragma unroll 1
-    for (int i = 0; i < np; i += 2) {
-      float4 z[2][8];
+    for (int i = 1; i < np; ++i) {   // more than two pieces: one more at a time
+      float4 zi[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int j = 0; j < 16; ++j) zi[j] = __ldcg(rows[i] + (16 * c64 + j) * BM);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          z[h][j] = (i + h < np) ? __ldcg(rows[i + h] + (8 * c32 + j) * BM) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float w = (i + h < np) ? wt[i + h] : 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          acc[4 * j] += z[h][j].x * w;
-          acc[4 * j + 1] += z[h][j].y * w;
-          acc[4 * j + 2] += z[h][j].z * w;
-          acc[4 * j + 3] += z[h][j].w * w;
-        }
+      for (int j = 0; j < 16; ++j) {
+        acc[4 * j] += zi[j].x * wt[i];
+        acc[4 * j + 1] += zi[j].y * wt[i];
+        acc[4 * j + 2] += zi[j].z * wt[i];
+        acc[4 * j + 3] += zi[j].w * wt[i];
       }
     }
     if (write) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
+      for (int j = 0; j < 64; j += 8) {
         uint4 val;
         val.x = pack_bf16(acc[j] * inv, acc[j + 1] * inv);
         val.y = pack_bf16(acc[j + 2] * inv, acc[j + 3] * inv);
         val.z = pack_bf16(acc[j + 4] * inv, acc[j + 5] * inv);
         val.w = pack_bf16(acc[j + 6] * inv, acc[j + 7] * inv);
-        *reinterpret_cast<uint4*>(orow + 32 * c32 + j) = val;
+        *reinterpret_cast<uint4*>(orow + 64 * c64 + j) = val;
       }
     }
   }
@@ -676,7 +685,7 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const int64_t tok = (int64_t)b.q0 + r;
       KeyInterval iv{1, 0};
       if (tok < a.Tq) iv = allowed_interval(a, query_pos(a, tok));
-      float m2 = -CUDART_INF_F, l = 0.f, lb = 0.f;
+      float m2 = -CUDART_INF_F, l = 0.f;
       int64_t ulo, uhi;
       unit_bounds(p, u, ulo, uhi);
       LiveTiles lt;
@@ -733,7 +742,7 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // P_X over the first 64 columns of S_X (column c holds keys 2c, 2c+1),
         // written in two halves as soon as each is packed.
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-mref, -mref);
-        uint64_t rs2[2] = {0ull, 0ull}, rsb2[2] = {0ull, 0ull};
+        uint64_t rs2[2] = {0ull, 0ull};
   #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
@@ -745,16 +754,12 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
             pk[c] = pack_bf16(p0, p1);
-            rsb2[c & 1] = f2_add(rsb2[c & 1], f2_pack(__uint_as_float(pk[c] << 16),
-                                                       __uint_as_float(pk[c] & 0xffff0000u)));
           }
           tmem_st32(s_col + 32 * half, pk);
         }
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2_unpack(f2_add(rs2[0], rs2[1]), a0, a1);
-        f2_unpack(f2_add(rsb2[0], rsb2[1]), b0, b1);
         l = l * alpha + (a0 + a1);
-        lb = lb * alpha + (b0 + b1);
         // PV_X(jt-1) has finished: S_X(jt) was issued after it and has landed.
         if (__any_sync(kFullMask, rescale)) {
   #pragma unroll
@@ -778,9 +783,9 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + tok * a.o_stride_t +
                             (int64_t)b.head * a.o_stride_h;
       if (whole) {
-        // O = z / lb, LSE = m + ln l (natural log); no key -> (0, -inf)
+        // O = z / l, LSE = m + ln l (natural log); no key -> (0, -inf)
         const bool live = ok && l > 0.f;
-        const float inv = (live && lb > 0.f) ? 1.f / lb : 0.f;
+        const float inv = live ? 1.f / l : 0.f;
 #pragma unroll
         for (int c4 = 0; c4 < HD / 32; ++c4) {
           uint32_t oo[32];
@@ -814,19 +819,21 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // The last piece of a segment usually ends after the unit's other
         // pieces (they open later segments).  If they are all written, merge
         // straight from this CTA's accumulator.
+        // Each block's warpgroup decides for itself (barrier 2 + X).
+        const bool lead = (threadIdx.x & 127) == 0;
         bool direct = false;
         if (last && cb - ca + 1 <= 8) {
-          if (threadIdx.x == 128) {
-            const unsigned long long cur = atomicAdd(p.pieces + u, 0ull);
-            s.merge = ((unsigned)(cur >> 32) == p.tag &&
-                       (int)(cur & 0xffffffffull) == pieces_of(ca, cb, W, G) - 1) ? 2 : 0;
+          if (lead) {
+            const unsigned long long cur = atomicAdd(p.pieces + 2 * u + X, 0ull);
+            s.merge[X] = ((unsigned)(cur >> 32) == p.tag &&
+                          (int)(cur & 0xffffffffull) == pieces_of(ca, cb, W, G) - 1) ? 2 : 0;
             __threadfence();
           }
-          named_bar_sync(1, 256);
-          direct = s.merge == 2;
+          named_bar_sync(2 + X, 128);
+          direct = s.merge[X] == 2;
         }
         if (direct) {
-          merge_unit_direct(p, X, r, s.pref[u], ca, cb, W, G, g, ok, m2, l, lb, o_col, tok < a.Tq, orow,
+          merge_unit_direct(p, X, r, s.pref[u], ca, cb, W, G, g, ok, m2, l, o_col, tok < a.Tq, orow,
                             a.lse != nullptr ? a.lse + tok * a.Hq + b.head : nullptr);
           tc_fence_before();
           mbar_arrive(&s.o_free[X]);
@@ -848,18 +855,21 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
               prow[(c4 * 8 + i / 4) * BM] = make_float4(__uint_as_float(oo[i]), __uint_as_float(oo[i + 1]),
                                                         __uint_as_float(oo[i + 2]), __uint_as_float(oo[i + 3]));
           }
-          prow[(HD / 4) * BM] = make_float4(ok ? m2 : -CUDART_INF_F, ok ? l : 0.f, ok ? lb : 0.f, 0.f);
+          prow[(HD / 4) * BM] = make_float4(ok ? m2 : -CUDART_INF_F, ok ? l : 0.f, 0.f, 0.f);
           tc_fence_before();
           mbar_arrive(&s.o_free[X]);
           {
-            __threadfence();
-            named_bar_sync(1, 256);
-            if (threadIdx.x == 128) {
-              s.merge = count_piece(p, u, pieces_of(ca, cb, W, G));
+            // The barrier orders the warpgroup's stores before the lead
+            // thread's fence and count (the fence is cumulative), as in a
+            // grid-wide barrier; the CTA that completes the count merges.
+            named_bar_sync(2 + X, 128);
+            if (lead) {
+              __threadfence();
+              s.merge[X] = count_piece(p, u, X, pieces_of(ca, cb, W, G));
               __threadfence();
             }
-            named_bar_sync(1, 256);
-            if (s.merge && tok < a.Tq)
+            named_bar_sync(2 + X, 128);
+            if (s.merge[X] && tok < a.Tq)
               merge_unit(p, X, r, s.pref[u], ca, cb, W, G, orow,
                          a.lse != nullptr ? a.lse + tok * a.Hq + b.head : nullptr);
           }
@@ -908,7 +918,7 @@ size_t dense_tc_bal_workspace(const cpattn_attn_args& a) {
   if (4 * nu > 3 * dense_tc_grid()) return 0;
   // every CTA counts every unit's tiles chunk by chunk
   if (a.kv_chunk_map != nullptr && (int64_t)nu * a.n_kv_chunks > 131072) return 0;
-  return dense_tc_bal_part_bytes(dense_tc_grid()) + (size_t)nu * sizeof(unsigned long long);
+  return dense_tc_bal_part_bytes(dense_tc_grid()) + (size_t)2 * nu * sizeof(unsigned long long);
 }
 
 cudaError_t launch_dense_tc_bal(const cpattn_attn_args& a, void* ws, size_t ws_bytes,

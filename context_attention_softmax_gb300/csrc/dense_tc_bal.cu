@@ -20,7 +20,7 @@
 // one, a range inside every chunk whose logical keys meet the interval.  So
 // each CTA derives all counts itself and no grid-wide step is needed.
 //
-// Pieces of a unit are counted on a per-unit word in the workspace whose high
+// Pieces of a unit are counted on a per-(unit, block) word in the workspace whose high
 // half carries a per-launch tag, so stale words from earlier launches read as
 // zero and the workspace needs no clearing.
 #include <atomic>

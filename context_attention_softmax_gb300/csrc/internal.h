@@ -1,6 +1,7 @@
 // Host-side declarations shared by the API layer and the kernel launchers.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,6 +31,11 @@ cudaError_t launch_lse_merge(int32_t n_parts, const float* part_o, const float* 
                              int32_t Tq, int32_t H, int32_t Dv, void* o, int32_t o_dtype,
                              int64_t o_stride_t, int64_t o_stride_h, float* lse,
                              cudaStream_t stream);
+// The same merge over bf16 parts (the MoBA slot summaries).
+cudaError_t launch_lse_merge_bf16parts(int32_t n_parts, const __nv_bfloat16* part_o,
+                                       const float* part_lse, int32_t Tq, int32_t H, int32_t Dv,
+                                       void* o, int32_t o_dtype, int64_t o_stride_t,
+                                       int64_t o_stride_h, float* lse, cudaStream_t stream);
 // tcgen05 dense kernel (bf16, d = 128): supported() says whether the
 // arguments fit it; launch sets *launched = false when the layout cannot be
 // described by TMA tensor maps (the caller then uses the general kernel).

@@ -57,7 +57,7 @@ struct MobaWs {
   int32_t* lists;
   int4* units;
   int32_t* n_units;
-  float* part_o;
+  __nv_bfloat16* part_o;   // finalised O of each (slot, query, head), bf16
   float* part_lse;
   int64_t max_units;
 };
@@ -88,7 +88,7 @@ MobaWs carve(void* ws, const Dims& d) {
   w.lists = reinterpret_cast<int32_t*>(p);   p += align256((size_t)d.entries * 4);
   w.units = reinterpret_cast<int4*>(p);      p += align256((size_t)d.max_units * 16);
   w.n_units = reinterpret_cast<int32_t*>(p); p += 256;
-  w.part_o = reinterpret_cast<float*>(p);    p += align256((size_t)d.entries * HD * 4);
+  w.part_o = reinterpret_cast<__nv_bfloat16*>(p); p += align256((size_t)d.entries * HD * 2);
   w.part_lse = reinterpret_cast<float*>(p);  p += align256((size_t)d.entries * 4);
   w.max_units = d.max_units;
   return w;
@@ -97,7 +97,7 @@ MobaWs carve(void* ws, const Dims& d) {
 size_t ws_bytes(const Dims& d) {
   const size_t nhb = (size_t)(d.H * d.NB + 1);
   return 3 * align256(nhb * 4) + align256((size_t)d.entries * 4) +
-         align256((size_t)d.max_units * 16) + 256 + align256((size_t)d.entries * HD * 4) +
+         align256((size_t)d.max_units * 16) + 256 + align256((size_t)d.entries * HD * 2) +
          align256((size_t)d.entries * 4);
 }
 
@@ -201,7 +201,7 @@ struct MobaParams {
   const int32_t* lists;
   const int4* units;
   const int32_t* n_units;
-  float* part_o;
+  __nv_bfloat16* part_o;
   float* part_lse;
 };
 
@@ -562,17 +562,21 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       const bool live = row_live && st.y > 0.f;
       const float inv = live ? 1.f / st.y : 0.f;
       const int64_t prow = ((int64_t)slot * a.Tq + q) * a.Hq + un.x;
-      float* orow = p.part_o + prow * HD;
+      __nv_bfloat16* orow = p.part_o + prow * HD;
 #pragma unroll
       for (int c4 = 0; c4 < HD / 32; ++c4) {
         uint32_t oo[32];
         tmem_ld32_sync(tmem + lane_base + kColO + ob * HD + c4 * 32, oo);
         if (row_live) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(orow + c4 * 32 + i) =
-                make_float4(__uint_as_float(oo[i]) * inv, __uint_as_float(oo[i + 1]) * inv,
-                            __uint_as_float(oo[i + 2]) * inv, __uint_as_float(oo[i + 3]) * inv);
+          for (int i = 0; i < 32; i += 8) {
+            uint4 val;
+            val.x = pack_bf16(__uint_as_float(oo[i + 0]) * inv, __uint_as_float(oo[i + 1]) * inv);
+            val.y = pack_bf16(__uint_as_float(oo[i + 2]) * inv, __uint_as_float(oo[i + 3]) * inv);
+            val.z = pack_bf16(__uint_as_float(oo[i + 4]) * inv, __uint_as_float(oo[i + 5]) * inv);
+            val.w = pack_bf16(__uint_as_float(oo[i + 6]) * inv, __uint_as_float(oo[i + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c4 * 32 + i) = val;
+          }
         }
       }
       if (row_live) p.part_lse[prow] = live ? (st.x + log2f(st.y)) * 0.6931471805599453f : -CUDART_INF_F;
@@ -678,8 +682,8 @@ cudaError_t launch_moba_tc(const cpattn_attn_args& a, const int32_t* sel, int32_
   moba_attn_kernel<<<grid, kThreads, kMSmemBytes, stream>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return launch_lse_merge(slots, w.part_o, w.part_lse, a.Tq, a.Hq, HD, a.o, CPATTN_BF16,
-                          a.o_stride_t, a.o_stride_h, a.lse, stream);
+  return launch_lse_merge_bf16parts(slots, w.part_o, w.part_lse, a.Tq, a.Hq, HD, a.o, CPATTN_BF16,
+                                    a.o_stride_t, a.o_stride_h, a.lse, stream);
 }
 
 }  // namespace cpattn

@@ -109,11 +109,40 @@ __global__ void gate_split_kernel(const float* __restrict__ mu32, int n_blocks, 
 }
 
 // Strict ranking order: larger value first, then lower block (branch-free).
-__device__ __forceinline__ bool ahead(float v1, int b1, float v2, int b2) {
-  return (v1 > v2) | ((v1 == v2) & (b1 < b2));
-}
 __device__ __forceinline__ bool ahead64(double v1, int b1, double v2, int b2) {
   return (v1 > v2) | ((v1 == v2) & (b1 < b2));
+}
+
+// The k-th largest of the lower bounds of blocks 0 .. n_cand-1 held in TMEM
+// (row = lane, 128 columns from acc): each value passes down a chain of
+// KMAX slots kept in descending order by max / min exchanges, so the slots
+// end holding the KMAX largest values with multiplicity.  NaN never enters
+// (fmaxf / fminf drop it), as NaN gates are never selected.
+template <int KMAX>
+__device__ __forceinline__ float kth_lower(uint32_t acc, int k, int n_cand) {
+  float tv[KMAX];
+#pragma unroll
+  for (int t = 0; t < KMAX; ++t) tv[t] = -CUDART_INF_F;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t rr[32];
+    tmem_ld32(acc + 32 * c, rr);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float v = (32 * c + j < n_cand) ? __uint_as_float(rr[j]) : -CUDART_INF_F;
+#pragma unroll
+      for (int t = 0; t < KMAX; ++t) {
+        const float hi = fmaxf(tv[t], v);
+        v = fminf(tv[t], v);
+        tv[t] = hi;
+      }
+    }
+  }
+  float T = tv[0];
+#pragma unroll
+  for (int t = 1; t < KMAX; ++t) T = (t == k - 1) ? tv[t] : T;
+  return T;
 }
 
 __global__ void __launch_bounds__(kGateThreads, 1)
@@ -251,7 +280,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                   (valid ? qi : 0) * a.q_stride_t + (int64_t)h * a.q_stride_h;
       float qss = 0.f;
       if (valid) {
-#pragma unroll 4
+#pragma unroll 8
         for (int d8 = 0; d8 < GD / 8; ++d8) {
           const uint4 w = *reinterpret_cast<const uint4*>(qrow + 8 * d8);
           const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -288,34 +317,9 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           tmem_st32(acc + 32 * c, rr);
         }
         tmem_wait_st();
-        float pv = CUDART_INF_F;   // T: the k-th largest lower bound
-        int pb = -1;
-        for (int rr_ = 0; rr_ < k; ++rr_) {
-          float bv[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-          int bb[4] = {0x7fffffff, 0x7fffffff, 0x7fffffff, 0x7fffffff};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(acc + 32 * c, rr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {   // four interleaved chains, merged below
-              const int b = 32 * c + j, x = j & 3;
-              const float lo = __uint_as_float(rr[j]);
-              const bool take = (b < n_cand) & ahead(pv, pb, lo, b) & ahead(lo, b, bv[x], bb[x]);
-              bv[x] = take ? lo : bv[x];
-              bb[x] = take ? b : bb[x];
-            }
-          }
-#pragma unroll
-          for (int x = 1; x < 4; ++x) {
-            const bool take = ahead(bv[x], bb[x], bv[0], bb[0]);
-            bv[0] = take ? bv[x] : bv[0];
-            bb[0] = take ? bb[x] : bb[0];
-          }
-          pv = bv[0];
-          pb = bb[0];
-        }
+        // T: the k-th largest lower bound (with multiplicity), from one pass
+        // keeping the k largest in a max/min exchange chain
+        const float pv = k <= 4 ? kth_lower<4>(acc, k, n_cand) : kth_lower<kGateMaxTopk>(acc, k, n_cand);
         int n_u = 0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {

@@ -23,7 +23,7 @@
 //      keys and merge softmax globally", para 3-4).
 //
 // Workspace (256-byte aligned regions): counts, cursors, offsets [H*NB(+1)],
-// lists [Tq*H*S], units [max_units], n_units, partial O fp32 [S][Tq][H][128],
+// lists [Tq*H*S], units [max_units], n_units, partial O bf16 [S][Tq][H][128],
 // partial LSE fp32 [S][Tq][H], with NB = ceil(Tk / B) and S = slots per row.
 #include <cuda.h>
 #include <cudaTypedefs.h>

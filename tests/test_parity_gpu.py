@@ -329,6 +329,26 @@ def test_lse_merge_neutral_parts():
     assert (o[20] == 0).all() and torch.isneginf(lse[20]).all()
 
 
+@pytest.mark.parametrize("n_parts", [1, 2, 4, 6])
+@pytest.mark.parametrize("out", ["fp32", "bf16"])
+def test_lse_merge_128_channels_neutral_parts_hold_garbage(n_parts, out):
+    """Dv = 128 (the half-warp path up to four parts, the unrolled one beyond):
+    a neutral part's channels are never used, whatever they hold."""
+    d = torch.device("cuda")
+    rng = np.random.default_rng(11 + n_parts)
+    po = rng.standard_normal((n_parts, 53, 3, 128))
+    pl = rng.standard_normal((n_parts, 53, 3)) * 4
+    pl[0, :7] = -np.inf
+    pl[:, 30] = -np.inf                           # every part neutral for row 30
+    O, L = orc.lse_merge(np.where(np.isneginf(pl)[..., None], 0.0, po), pl)
+    po_dev = torch.tensor(po, dtype=torch.float32, device=d)
+    po_dev[torch.isneginf(torch.tensor(pl, device=d))] = float("nan")
+    o, lse = cpattn_lse_merge(po_dev, torch.tensor(pl, dtype=torch.float32, device=d),
+                              out_dtype=torch.float32 if out == "fp32" else torch.bfloat16)
+    assert_matches(o, lse, O, L, out, f"lse_merge {n_parts} parts")
+    assert (o[30].float() == 0).all() and torch.isneginf(lse[30]).all()
+
+
 def test_dense_per_unit_schedule_without_workspace():
     """Without a workspace the one-unit-per-CTA kernel runs; same answer."""
     import ctypes

@@ -297,6 +297,25 @@ def test_moba_gate_ties_and_few_candidates():
     assert sel2[0, 0].tolist() == [0, 1, -1, -1]
 
 
+@pytest.mark.parametrize("dtype,D", [("fp32", 64), ("bf16", 72), ("fp32", 136)])
+def test_moba_gate_other_shapes_and_fp32(dtype, D):
+    """The SIMT gate over the vectorised block means: fp32 inputs, head dims
+    other than 128 (D = 136 leaves 7 row groups of 34 column quads):
+    selections equal the float64 oracle's."""
+    rng = np.random.default_rng(21 + D)
+    Tq, Tk, H, B, topk = 48, 1536, 3, 128, 3
+    qf = rng.standard_normal((Tq, H, D)) * 0.5
+    kf = rng.standard_normal((Tk, H, D)) * 0.5
+    tdt = torch.float32 if dtype == "fp32" else torch.bfloat16
+    q = torch.tensor(qf, dtype=torch.float32).to(tdt)
+    k = torch.tensor(kf, dtype=torch.float32).to(tdt)
+    offset = Tk - Tq
+    sel = cpattn_block_gate(q.cuda(), k.cuda(), B, topk, causal_offset=offset)
+    qpos = offset + np.arange(Tq)
+    ref = orc.moba_block_gate(q.double().numpy(), k.double().numpy(), qpos, B, topk)
+    np.testing.assert_array_equal(sel.cpu().numpy(), ref)
+
+
 def test_moba_full_size():
     w = inputs.moba()
     sel, o, lse = _moba_gpu(w)

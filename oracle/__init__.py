@@ -12,6 +12,7 @@ from .attention import (  # noqa: F401
     block_means,
     chunk_summary,
     dense_attention,
+    dsa_indexer_topk,
     finalise,
     logical_positions,
     lse_merge,

@@ -444,3 +444,45 @@ def moba_attention(q, k, v, scale, layout, sel, block_size, rows=None):
     """Attention over the selected blocks, causal within the own block."""
     O, LSE, _ = sparse_attention(q, k, v, scale, layout, sel, block_size, rows)
     return O, LSE
+
+
+# ---------------------------------------------------------------------------
+# DSA indexer: which keys a query attends to  ([DSA-THD] sequence diagram)
+# ---------------------------------------------------------------------------
+
+def dsa_indexer_topk(qI, kI, w, layout, topk, rows=None):
+    """Key selection of the DSA indexer, per query row.
+
+    [DSA-THD] sequence diagram: the index mask and the varlen bounds first,
+    then the indexer's QK scores, then the top-k keys that the sparse
+    attention gathers ([DSA-CP]: indices in global coordinates).  The score
+    of key j for query i over the indexer heads h is
+
+        score(i, j) = sum_h w_h * max(0, <qI[i, h], kI[j]>),
+
+    taken over the keys the layout permits (same sequence, kpos_j <= qpos_i
+    when causal), in float64 from the exact inputs.  The ``topk`` keys with
+    the largest score are chosen, equal scores going to the lower j; a row
+    with fewer permitted keys takes all of them.  Each row is returned in
+    ascending j and padded with -1.
+
+    qI: [Tq, H, D], kI: [Tk, D], w: [H].  Returns int32 [R, 1, topk].
+    """
+    qI = np.asarray(qI, np.float64)
+    kI = np.asarray(kI, np.float64)
+    w = np.asarray(w, np.float64)
+    Tq, H, _ = qI.shape
+    Tk = kI.shape[0]
+    rows = np.arange(Tq) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.full((len(rows), 1, topk), -1, dtype=np.int32)
+    j = np.arange(Tk)
+    for r, i in enumerate(rows):
+        A = layout.allowed(np.array([i]))[0]
+        dots = qI[i] @ kI.T                               # [H, Tk]
+        score = (w[:, None] * np.maximum(dots, 0.0)).sum(axis=0)
+        cand = j[A]
+        # descending score, ties to the lower j: sort by (-score, j)
+        order = np.lexsort((cand, -score[cand]))
+        chosen = np.sort(cand[order[:topk]])
+        out[r, 0, :len(chosen)] = chosen
+    return out

@@ -1,0 +1,121 @@
+"""Pins of the float64 DSA indexer oracle (oracle.dsa_indexer_topk).
+
+Each test fixes the oracle against something other than its own formula:
+special cases that reduce to a library sort, an algebraic identity of the
+ReLU, constructed ties, the permitted relation, and the row convention for
+rows with fewer permitted keys than k.
+"""
+
+import numpy as np
+import pytest
+
+import oracle as orc
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def _sel(qI, kI, w, layout, topk):
+    return orc.dsa_indexer_topk(qI, kI, w, layout, topk)[:, 0, :]
+
+
+def test_one_head_positive_dots_is_a_plain_top_k_of_the_dot_product():
+    """H = 1, w = 1 and positive entries: the score is the dot product, so the
+    selection is numpy's stable argsort of -q.k (ties to the lower j) cut at k
+    and sorted ascending."""
+    rng = np.random.default_rng(1)
+    qI = rng.random((9, 1, 16))
+    kI = rng.random((70, 16))
+    lay = orc.make_layout(9, 70, causal=False)
+    got = _sel(qI, kI, np.ones(1), lay, 12)
+    dots = qI[:, 0, :] @ kI.T
+    for i in range(9):
+        ref = np.sort(np.argsort(-dots[i], kind="stable")[:12])
+        np.testing.assert_array_equal(got[i], ref)
+
+
+def test_relu_pair_of_opposite_heads_scores_the_absolute_dot():
+    """Heads +q and -q with equal weights: relu(x) + relu(-x) = |x|, so the
+    selection is the top-k of |q.k|."""
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal((7, 32))
+    qI = np.stack([q, -q], axis=1)
+    kI = rng.standard_normal((90, 32))
+    lay = orc.make_layout(7, 90, causal=False)
+    got = _sel(qI, kI, np.array([0.7, 0.7]), lay, 10)
+    absdot = np.abs(q @ kI.T)
+    for i in range(7):
+        ref = np.sort(np.argsort(-absdot[i], kind="stable")[:10])
+        np.testing.assert_array_equal(got[i], ref)
+
+
+def test_negative_dots_contribute_nothing():
+    """A head whose dots are all negative adds zero: the selection equals the
+    one computed with that head removed."""
+    rng = np.random.default_rng(3)
+    kI = rng.random((60, 8))                      # positive keys
+    q_pos = rng.random((5, 8))
+    q_neg = -rng.random((5, 8))                   # every dot with kI negative
+    qI = np.stack([q_pos, q_neg], axis=1)
+    lay = orc.make_layout(5, 60, causal=False)
+    both = _sel(qI, kI, np.array([0.3, 0.9]), lay, 9)
+    alone = _sel(q_pos[:, None, :], kI, np.array([0.3]), lay, 9)
+    np.testing.assert_array_equal(both, alone)
+
+
+def test_equal_scores_go_to_the_lower_key():
+    """Keys 4, 17 and 33 are the same vector and score highest; with k = 2 the
+    two lowest of them are chosen."""
+    rng = np.random.default_rng(4)
+    kI = rng.standard_normal((40, 16)) * 0.1
+    star = rng.standard_normal(16)
+    for j in (4, 17, 33):
+        kI[j] = star
+    qI = np.stack([star * 3.0, star * 2.0], axis=0)[None, :, :].repeat(3, axis=0)
+    lay = orc.make_layout(3, 40, causal=False)
+    got = _sel(qI, kI, np.array([0.5, 0.25]), lay, 2)
+    np.testing.assert_array_equal(got, [[4, 17]] * 3)
+
+
+def test_only_permitted_keys_and_fewer_than_k_rows():
+    """Causal at offset 3: query i sees keys 0..3+i only; rows with fewer
+    permitted keys than k take all of them, ascending, padded with -1."""
+    rng = np.random.default_rng(5)
+    qI = rng.standard_normal((6, 2, 8))
+    kI = rng.standard_normal((30, 8))
+    lay = orc.make_layout(6, 30, causal=True, causal_offset=3)
+    got = _sel(qI, kI, np.array([1.0, 0.5]), lay, 6)
+    for i in range(6):
+        n = 4 + i
+        if n <= 6:
+            np.testing.assert_array_equal(got[i, :n], np.arange(n))
+            assert (got[i, n:] == -1).all()
+        else:
+            assert (got[i] >= 0).all() and (got[i] <= 3 + i).all()
+            assert (np.diff(got[i]) > 0).all()
+
+
+def test_packed_sequences_never_cross():
+    """Two packed sequences (cut at 20): a query of the second sequence never
+    selects a key of the first, however well it scores."""
+    rng = np.random.default_rng(6)
+    kI = rng.standard_normal((40, 8))
+    kI[:20] *= 10.0                               # first sequence scores far higher
+    qI = np.abs(rng.standard_normal((40, 1, 8)))
+    kI = np.abs(kI)
+    lay = orc.make_layout(40, 40, causal=True, cu_seqlens=np.array([0, 20, 40]))
+    got = _sel(qI, kI, np.ones(1), lay, 5)
+    for i in range(20, 40):
+        row = got[i][got[i] >= 0]
+        assert (row >= 20).all() and (row <= i).all()
+
+
+def test_weight_scale_and_head_order_do_not_change_the_selection():
+    rng = np.random.default_rng(7)
+    qI = rng.standard_normal((8, 4, 16))
+    kI = rng.standard_normal((50, 16))
+    w = rng.random(4)
+    lay = orc.make_layout(8, 50, causal=True, causal_offset=30)
+    base = _sel(qI, kI, w, lay, 7)
+    np.testing.assert_array_equal(_sel(qI, kI, w * 4.0, lay, 7), base)   # power-of-two scale is exact
+    perm = np.array([2, 0, 3, 1])
+    np.testing.assert_array_equal(_sel(qI[:, perm], kI, w[perm], lay, 7), base)

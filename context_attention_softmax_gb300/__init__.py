@@ -18,7 +18,7 @@ from ._lib import CPATTN_BF16, CPATTN_FP32, CpattnError  # noqa: F401
 
 __all__ = [
     "cpattn_chunk_fwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd", "cpattn_block_gate",
-    "cpattn_workspace_size", "cpattn_version", "CpattnError",
+    "cpattn_dsa_indexer", "cpattn_workspace_size", "cpattn_version", "CpattnError",
 ]
 
 
@@ -177,6 +177,29 @@ def cpattn_block_gate(q, k, block_size, topk, causal_offset=0, q_chunk_map=None,
     _lib.check(lib.cpattn_block_gate(ctypes.byref(a), int(block_size), int(topk), sel.data_ptr(),
                                      _ptr(workspace), ws_bytes, _stream(stream)))
     return sel
+
+
+def cpattn_dsa_indexer(qI, kI, w, topk, causal=True, causal_offset=0, cu_seqlens=None,
+                       q_chunk_map=None, chunk_len=0, out=None, workspace=None, stream=None):
+    """DSA indexer top-k: int32 [Tq, topk] key indices, ascending, -1 padded.
+
+    qI: fp32 [Tq, H, D], kI: fp32 [Tk, 1, D] (or [Tk, D]), w: fp32 [H].
+    """
+    dev = qI.device
+    if kI.dim() == 2:
+        kI = kI.unsqueeze(1)
+    cu = _device_i32(cu_seqlens, dev)
+    qm = _device_i32(q_chunk_map, dev)
+    if out is None:
+        out = torch.empty((qI.shape[0], topk), dtype=torch.int32, device=dev)
+    a = _args(qI, kI, None, 1.0, causal, causal_offset, cu, qm, None, chunk_len, None, None)
+    lib = _lib.load()
+    ws_bytes = lib.cpattn_workspace_size(_lib.OP_DSA_INDEXER, ctypes.byref(a), topk, 1)
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _lib.check(lib.cpattn_dsa_indexer(ctypes.byref(a), w.data_ptr(), int(topk), out.data_ptr(),
+                                      _ptr(workspace), ws_bytes, _stream(stream)))
+    return out
 
 
 def cpattn_workspace_size(op, q, k, v=None, topk=0, block_size=1):

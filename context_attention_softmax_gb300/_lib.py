@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(HERE, "libcpattn.so")
 
 CPATTN_FP32 = 0
 CPATTN_BF16 = 1
-OP_CHUNK_FWD, OP_TOPK_SPARSE_FWD, OP_BLOCK_GATE = 0, 1, 2
+OP_CHUNK_FWD, OP_TOPK_SPARSE_FWD, OP_BLOCK_GATE, OP_DSA_INDEXER = 0, 1, 2, 3
 
 STATUS = {
     0: "CPATTN_OK",
@@ -33,6 +33,7 @@ EXPORTS = (
     "cpattn_topk_sparse_fwd",
     "cpattn_block_gate",
     "cpattn_block_gate_static",
+    "cpattn_dsa_indexer",
     "cpattn_workspace_size",
     "cpattn_last_error",
     "cpattn_version",
@@ -86,10 +87,11 @@ def load(path: str = LIB_PATH):
     lib.cpattn_topk_sparse_fwd.argtypes = [P, c_p, c_i32, c_i32, c_i32, c_p, ctypes.c_size_t, c_p]
     lib.cpattn_block_gate.argtypes = [P, c_i32, c_i32, c_p, c_p, ctypes.c_size_t, c_p]
     lib.cpattn_block_gate_static.argtypes = [P, c_i32, c_i32, c_p, c_p]
+    lib.cpattn_dsa_indexer.argtypes = [P, c_p, c_i32, c_p, c_p, ctypes.c_size_t, c_p]
     lib.cpattn_workspace_size.argtypes = [c_i32, P, c_i32, c_i32]
     lib.cpattn_workspace_size.restype = ctypes.c_size_t
     for name in ("cpattn_chunk_fwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd",
-                 "cpattn_block_gate", "cpattn_block_gate_static"):
+                 "cpattn_block_gate", "cpattn_block_gate_static", "cpattn_dsa_indexer"):
         getattr(lib, name).restype = c_i32
     lib.cpattn_last_error.argtypes = []
     lib.cpattn_last_error.restype = ctypes.c_char_p

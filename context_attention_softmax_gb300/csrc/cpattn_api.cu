@@ -204,9 +204,33 @@ cpattn_status cpattn_block_gate(const cpattn_attn_args* a, int32_t block_size, i
                      "cpattn_block_gate launch");
 }
 
+cpattn_status cpattn_dsa_indexer(const cpattn_attn_args* a, const float* w, int32_t topk,
+                                 int32_t* indices, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  TRY(check_attn(a, false, false));
+  CHECK(a->dtype == CPATTN_FP32, CPATTN_ERR_UNSUPPORTED, "the indexer takes CPATTN_FP32 qI and kI");
+  CHECK(a->Hkv == 1, CPATTN_ERR_INVALID_ARG, "the indexer's keys have one head (Hkv=%d)", a->Hkv);
+  CHECK(a->Hq <= 16, CPATTN_ERR_UNSUPPORTED, "Hq=%d indexer heads exceed 16", a->Hq);
+  CHECK(a->Dqk <= 256, CPATTN_ERR_UNSUPPORTED, "Dqk=%d exceeds 256", a->Dqk);
+  CHECK(a->kv_chunk_map == nullptr, CPATTN_ERR_UNSUPPORTED,
+        "the indexer takes keys in logical order (kv_chunk_map NULL)");
+  CHECK(topk >= 1 && (a->Tk == 0 || topk <= a->Tk), CPATTN_ERR_INVALID_ARG,
+        "topk=%d must be in [1, Tk=%d]", topk, a->Tk);
+  CHECK(w != nullptr, CPATTN_ERR_INVALID_ARG, "w is NULL");
+  if (a->Tq > 0) CHECK(indices != nullptr, CPATTN_ERR_INVALID_ARG, "indices is NULL");
+  const size_t need = a->Tq > 0 ? dsa_indexer_workspace(*a, dsa_indexer_grid(*a)) : 0;
+  CHECK(workspace_bytes >= need && (need == 0 || workspace != nullptr), CPATTN_ERR_WORKSPACE,
+        "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  if (need > 0) CHECK(aligned16(workspace), CPATTN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  return cuda_status(launch_dsa_indexer(*a, w, topk, indices, workspace,
+                                        reinterpret_cast<cudaStream_t>(stream)),
+                     "cpattn_dsa_indexer launch");
+}
+
 size_t cpattn_workspace_size(int32_t op, const cpattn_attn_args* a, int32_t topk, int32_t block_size) {
   if (a == nullptr) return 0;
   if (op == CPATTN_OP_BLOCK_GATE) return block_size > 0 ? block_gate_workspace(*a, block_size) : 0;
+  if (op == CPATTN_OP_DSA_INDEXER) return a->Tq > 0 ? dsa_indexer_workspace(*a, dsa_indexer_grid(*a)) : 0;
   if (op == CPATTN_OP_CHUNK_FWD) return a->kv_chunk_len == 0 ? dense_tc_bal_workspace(*a) : 0;
   if (op == CPATTN_OP_TOPK_SPARSE_FWD && block_size > 1 && topk > 0 &&
       moba_tc_supported(*a, 1, block_size, topk))

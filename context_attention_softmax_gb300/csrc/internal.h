@@ -31,6 +31,13 @@ cudaError_t launch_lse_merge(int32_t n_parts, const float* part_o, const float* 
                              int32_t Tq, int32_t H, int32_t Dv, void* o, int32_t o_dtype,
                              int64_t o_stride_t, int64_t o_stride_h, float* lse,
                              cudaStream_t stream);
+// DSA indexer (fp32 qI [Tq, Hq, D], kI [Tk, 1, D]): workspace bytes for a
+// given grid, the grid the launcher uses, and the launch (scores, norms,
+// per-row certified top-k).
+size_t dsa_indexer_workspace(const cpattn_attn_args& a, int grid);
+int dsa_indexer_grid(const cpattn_attn_args& a);
+cudaError_t launch_dsa_indexer(const cpattn_attn_args& a, const float* w, int topk, int32_t* out,
+                               void* ws, cudaStream_t stream);
 // The same merge over bf16 parts (the MoBA slot summaries).
 cudaError_t launch_lse_merge_bf16parts(int32_t n_parts, const __nv_bfloat16* part_o,
                                        const float* part_lse, int32_t Tq, int32_t H, int32_t Dv,

@@ -224,7 +224,8 @@ def dsa_absorbed(seed=0, Tq=4096, Tk=32768, offset=16384, Hq=128, d_latent=512,
     idx = indexer_topk(qI, kI, w, qpos, topk).cpu()
     return Workload(f"dsa_absorbed_{Tq}x{Tk}_h{Hq}_top{topk}", "bf16", q, kv, kv[:, :, :d_latent],
                     scale=1.0 / np.sqrt(Dqk), causal=True, causal_offset=offset,
-                    indices=idx, block_size=1, topk=topk)
+                    indices=idx, block_size=1, topk=topk,
+                    extra={"qI": qI.cpu(), "kI": kI.cpu(), "w": w.cpu()})
 
 
 def moba(seed=0, Tq=8192, Tk=65536, offset=57344, H=32, D=128, block_size=512, topk=3):

@@ -70,7 +70,8 @@ typedef enum {
 
 enum { CPATTN_FP32 = 0, CPATTN_BF16 = 1 };
 
-enum { CPATTN_OP_CHUNK_FWD = 0, CPATTN_OP_TOPK_SPARSE_FWD = 1, CPATTN_OP_BLOCK_GATE = 2 };
+enum { CPATTN_OP_CHUNK_FWD = 0, CPATTN_OP_TOPK_SPARSE_FWD = 1, CPATTN_OP_BLOCK_GATE = 2,
+       CPATTN_OP_DSA_INDEXER = 3 };
 
 /*
  * Arguments of one attention call (shared by chunk_fwd, topk_sparse_fwd and
@@ -239,6 +240,35 @@ cpattn_status cpattn_block_gate(const cpattn_attn_args* args, int32_t block_size
  */
 cpattn_status cpattn_block_gate_static(const cpattn_attn_args* args, int32_t block_size,
                                        int32_t topk, int32_t* sel, void* stream);
+
+/*
+ * cpattn_dsa_indexer - token selection of the DSA indexer for every query.
+ * Source: "[1/2] Enable DSA CP, THD with absorbed MLA - #3674", sequence
+ * diagram (index mask and varlen bounds, then the indexer's QK scores, then
+ * top-k, then the sparse gather); "[Feature-request] Context Parallel
+ * support for DSAttention" (indices in global coordinates).  The score is
+ * this library's stated reading of the indexer:
+ *   score(i, j) = sum_h w[h] * max(0, <qI[i, h], kI[j]>)
+ * over the keys the layout permits (allowed(i, j) above).  The `topk` keys
+ * with the largest score are chosen, equal scores going to the lower key; a
+ * row with fewer permitted keys takes all of them.
+ * Output indices: device int32 [Tq, topk] contiguous, each row ascending and
+ * padded with -1 - directly usable as `indices` of cpattn_topk_sparse_fwd
+ * with index_heads = 1 and block_size = 1.  The selection equals the one an
+ * exact (float64) evaluation of the scores makes: fp32 scores carry a
+ * certified error bound, and only keys whose bound reaches the k-th
+ * boundary are ranked again in float64.
+ * Uses args->dtype (CPATTN_FP32), q = qI [Tq, Hq, Dqk] (Hq = indexer heads),
+ * k = kI [Tk, 1, Dqk] (Hkv = 1), causal, causal_offset, cu_seqlens and
+ * q_chunk_map/chunk_len for positions; keys are in logical order
+ * (kv_chunk_map NULL).  w: device fp32 [Hq].  Limits: Dqk <= 256, Hq <= 16,
+ * 1 <= topk <= Tk.
+ * Workspace: cpattn_workspace_size(CPATTN_OP_DSA_INDEXER, ...) bytes (the
+ * fp32 scores of every query and permitted key, key norms, scratch).
+ */
+cpattn_status cpattn_dsa_indexer(const cpattn_attn_args* args, const float* w, int32_t topk,
+                                 int32_t* indices, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /* Bytes of device workspace the call needs (0 if none; for
  * CPATTN_OP_CHUNK_FWD the bytes that enable the SM-balanced schedule).

@@ -12,7 +12,7 @@ import torch
 
 import oracle as orc
 import context_attention_softmax_gb300 as pkg
-from context_attention_softmax_gb300 import (cpattn_block_gate, cpattn_chunk_fwd,
+from context_attention_softmax_gb300 import (cpattn_block_gate, cpattn_chunk_fwd, cpattn_dsa_indexer,
                                              cpattn_lse_merge, cpattn_topk_sparse_fwd, inputs)
 
 from helpers import assert_matches, f64, layout_of, sample_rows, to_gpu
@@ -386,3 +386,56 @@ def test_dense_per_unit_schedule_without_workspace():
     _lib.check(lib.cpattn_chunk_fwd(ctypes.byref(a), None, 0, torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()
     assert_matches(o, lse, O, L, "bf16", "per-unit schedule")
+
+
+# ---------------------------------------------------------------- DSA indexer
+def _indexer_case(seed, Tq, Tk, H, D, offset, dup=None, cu=None):
+    rng = np.random.default_rng(seed)
+    qI = rng.standard_normal((Tq, H, D)).astype(np.float32)
+    kI = rng.standard_normal((Tk, D)).astype(np.float32)
+    w = rng.uniform(0.0, 1.0, H).astype(np.float32)
+    if dup is not None:                         # equal keys: equal scores
+        for j in dup[1:]:
+            kI[j] = kI[dup[0]]
+        qI[:, :, :] = kI[dup[0]] * 2.0           # and favoured by every query and head
+    lay = orc.make_layout(Tq, Tk, True, offset, cu_seqlens=cu)
+    return qI, kI, w, lay
+
+
+@pytest.mark.parametrize("Tq,Tk,H,D,offset,topk", [
+    (37, 700, 4, 64, 600, 50),       # every row has more permitted keys than k
+    (40, 300, 3, 32, 0, 64),         # early rows: fewer permitted keys than k
+    (9, 2000, 4, 128, 1990, 512),    # large k, D = 128
+])
+def test_dsa_indexer_matches_float64_oracle(Tq, Tk, H, D, offset, topk):
+    qI, kI, w, lay = _indexer_case(31 + Tq, Tq, Tk, H, D, offset)
+    ref = orc.dsa_indexer_topk(qI, kI, w, lay, topk)[:, 0, :]
+    got = cpattn_dsa_indexer(torch.from_numpy(qI).cuda(), torch.from_numpy(kI).cuda(),
+                             torch.from_numpy(w).cuda(), topk, causal_offset=offset)
+    np.testing.assert_array_equal(got.cpu().numpy(), ref)
+
+
+def test_dsa_indexer_ties_and_packed_sequences():
+    """Keys 3, 130, 150, 300 and 390 are equal and favoured by every query: with
+    k = 2 the two lowest permitted ones (130, 150) win - key 3 lies in the
+    first packed sequence, which the queries of the second never see."""
+    cu = np.array([0, 120, 400], dtype=np.int32)
+    qI, kI, w, lay = _indexer_case(5, 50, 400, 2, 32, 350, dup=(130, 3, 150, 300, 390), cu=cu)
+    ref = orc.dsa_indexer_topk(qI, kI, w, lay, 2)[:, 0, :]
+    got = cpattn_dsa_indexer(torch.from_numpy(qI).cuda(), torch.from_numpy(kI).cuda(),
+                             torch.from_numpy(w).cuda(), 2, causal_offset=350,
+                             cu_seqlens=torch.from_numpy(cu))
+    np.testing.assert_array_equal(got.cpu().numpy(), ref)
+    assert (got.cpu().numpy() == [130, 150]).all()
+
+
+def test_dsa_indexer_full_size_sampled():
+    """The DSA workload's indexer (4096 queries at offset 16384 over 32768
+    keys, 4 heads of 128, k = 2048): sampled rows equal the float64 oracle."""
+    w = inputs.dsa_absorbed()
+    qI, kI, wt = w.extra["qI"], w.extra["kI"], w.extra["w"]
+    got = cpattn_dsa_indexer(qI.cuda(), kI.cuda(), wt.cuda(), w.topk, causal_offset=w.causal_offset)
+    rows = sample_rows(qI.shape[0], 12, seed=3, edges=(1,))
+    lay = orc.make_layout(qI.shape[0], kI.shape[0], True, w.causal_offset)
+    ref = orc.dsa_indexer_topk(qI.numpy(), kI.numpy(), wt.numpy(), lay, w.topk, rows=rows)[:, 0, :]
+    np.testing.assert_array_equal(got.cpu().numpy()[rows], ref)

@@ -22,6 +22,7 @@ host (pinned) inputs copied in and outputs copied out inside each step.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -246,7 +247,50 @@ class MobaRunner:
                                lse=self.lse, workspace=self.ws_sparse)
 
 
-RUNNERS = {"dense_gqa": DenseRunner, "zigzag": ZigzagRunner, "dsa": DsaRunner, "moba": MobaRunner}
+class IndexerRunner:
+    """The DSA indexer: top-2048 keys of 4096 queries at offset 16384 over 32768
+    keys, 4 fp32 indexer heads of 128 (the indices the DSA workload attends to)."""
+
+    name = "dsa_indexer"
+
+    def __init__(self, device):
+        self.w = w = inputs.dsa_absorbed(device=device)
+        self.qI, self.kI, self.wt = (w.extra[k].to(device) for k in ("qI", "kI", "w"))
+        Tq, H, D = self.qI.shape
+        Tk = self.kI.shape[0]
+        self.out = torch.empty((Tq, w.topk), dtype=torch.int32, device=device)
+        from context_attention_softmax_gb300 import _lib, _args
+        a = _args(self.qI, self.kI.unsqueeze(1), None, 1.0, True, w.causal_offset, None, None, None,
+                  0, None, None)
+        nbytes = _lib.load().cpattn_workspace_size(_lib.OP_DSA_INDEXER, ctypes.byref(a), w.topk, 1)
+        self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+        n_keys = np.minimum(w.causal_offset + np.arange(Tq) + 1, Tk)     # causal, one sequence
+        self.flops = 2.0 * float(n_keys.sum()) * H * D
+        self.launches_per_step = 3   # norms, scores, selection
+        self.bound = "alu"
+        self.config = {"workload": "DSA indexer top-2048: 4096 q (offset 16384) x 32768 keys, "
+                                   "4 fp32 indexer heads x 128, scores sum_h w_h relu(qI.kI)",
+                       "permitted_pairs": int(n_keys.sum())}
+
+    def step(self):
+        from context_attention_softmax_gb300 import cpattn_dsa_indexer
+        cpattn_dsa_indexer(self.qI, self.kI, self.wt, self.w.topk, causal_offset=self.w.causal_offset,
+                           out=self.out, workspace=self.ws)
+
+    def oracle_sample(self, rows):
+        import oracle as orc
+        w = self.w
+        if not hasattr(self, "_np"):
+            self._np = tuple(w.extra[k].numpy() for k in ("qI", "kI", "w"))
+            self._lay = orc.make_layout(self._np[0].shape[0], self._np[1].shape[0], True, w.causal_offset)
+        qI, kI, wt = self._np
+        orc.dsa_indexer_topk(qI, kI, wt, self._lay, w.topk, rows=rows)
+        n_keys = np.minimum(w.causal_offset + np.asarray(rows) + 1, kI.shape[0])
+        return 2.0 * float(n_keys.sum()) * qI.shape[1] * qI.shape[2]
+
+
+RUNNERS = {"dense_gqa": DenseRunner, "zigzag": ZigzagRunner, "dsa": DsaRunner, "moba": MobaRunner,
+           "dsa_indexer": IndexerRunner}
 
 
 # ---------------------------------------------------------------------------
@@ -457,12 +501,22 @@ def run_ours(args, world, rank, local):
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": None, "peak_source": f"{src} bf16 burst"}
+    elif runner.bound == "alu":
+        # fp32 FMA pipes: SMs x 128 lanes x 2 FLOP x the maximum SM clock
+        achieved = runner.flops / (mean_ms * 1e-3) / 1e12
+        sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = n_sm * 128 * 2 * sm_mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"fp32 FMA: {n_sm} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz"}
     else:
         achieved = runner.hbm_bytes / (mean_ms * 1e-3) / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": None, "peak_source": f"{src} copy"}
-    roof["kernel"] = "cpattn_chunk_fwd" if runner.name != "moba" else "moba step"
+    roof["kernel"] = {"moba": "moba step", "dsa_indexer": "dsa indexer (scores + selection)"}.get(
+        runner.name, "cpattn_chunk_fwd")
     traffic, what = measured_traffic(runner.name)
     if traffic is not None:
         roof["traffic"] = traffic

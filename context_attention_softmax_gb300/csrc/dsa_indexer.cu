@@ -17,7 +17,8 @@
 //  1. idx_norm_kernel: ||kI_j|| and a_i = sum_h |w_h| ||qI_ih||, in float64
 //     and rounded up to fp32.
 //  2. idx_score_kernel: the fp32 scores of 128 queries x 128 keys per CTA
-//     (register-tiled: 8 x 8 per thread), every dot product accumulated by
+//     (register-tiled: 8 x 8 per thread; the next d-chunk's loads in flight
+//     while the current one is multiplied), every dot product accumulated by
 //     fma over d in order, then relu, then fma over the heads in order.  So
 //       |S_ij - score_ij| <= (D + H) 2^-24 (1 + tiny) ||kI_j|| a_i,
 //     and e_ij = c ||kI_j|| a_i with c = (D + H + 4) 2^-24 * 1.02 bounds it.
@@ -87,9 +88,9 @@ __global__ void idx_norm_kernel(const cpattn_attn_args a, const float* __restric
 // Thread (ty, tx) of 16 x 16 owns query rows ty*4 + {0..3}, 64 + ty*4 + {0..3}
 // and key columns tx*4 + {0..3}, 64 + tx*4 + {0..3} of the 128 x 128 tile.
 struct ScoreSmem {
-  float a[kTD][kTQ + 4];   // qI chunk, d-major (padding spreads the transposed stores)
-  float b[kTD][kTK + 4];   // kI chunk, d-major
-  long long lo, hi;        // permitted key range of the tile's query rows
+  float a[2][kTD][kTQ + 4];   // qI chunks, d-major, double-buffered
+  float b[2][kTD][kTK + 4];   // kI chunks, d-major
+  long long lo, hi;           // permitted key range of the tile's query rows
 };
 
 __global__ void __launch_bounds__(kScoreThreads)
@@ -116,54 +117,70 @@ idx_score_kernel(const cpattn_attn_args a, const float* __restrict__ w, float* _
   __syncthreads();
   if (s.lo > s.hi || s.hi < k0 || s.lo > k0 + kTK - 1) return;   // no permitted key in the tile
 
-  float sc[8][8];
+  // chunk c = (head c / nd, d-chunk c % nd); the next chunk's global loads
+  // are in flight while the current one is multiplied
+  const int nd = (D + kTD - 1) / kTD, nc = H * nd;
+  float4 ra[2], rb[2];
+  auto load = [&](int c) {
+    const int h = c / nd, d0 = (c - h * nd) * kTD;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {   // 512 float4 of each operand, two per thread
+      const int idx = tid + kScoreThreads * t, r = idx >> 2, c4 = idx & 3;
+      const int d = d0 + 4 * c4;
+      ra[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      rb[t] = ra[t];
+      if (q0 + r < a.Tq && d < D)
+        ra[t] = *reinterpret_cast<const float4*>(qI + (int64_t)(q0 + r) * a.q_stride_t +
+                                                 (int64_t)h * a.q_stride_h + d);
+      if (k0 + r < a.Tk && d < D)
+        rb[t] = *reinterpret_cast<const float4*>(kI + (int64_t)(k0 + r) * a.k_stride_t + d);
+    }
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int idx = tid + kScoreThreads * t, r = idx >> 2, c4 = idx & 3;
+      s.a[buf][4 * c4 + 0][r] = ra[t].x; s.a[buf][4 * c4 + 1][r] = ra[t].y;
+      s.a[buf][4 * c4 + 2][r] = ra[t].z; s.a[buf][4 * c4 + 3][r] = ra[t].w;
+      s.b[buf][4 * c4 + 0][r] = rb[t].x; s.b[buf][4 * c4 + 1][r] = rb[t].y;
+      s.b[buf][4 * c4 + 2][r] = rb[t].z; s.b[buf][4 * c4 + 3][r] = rb[t].w;
+    }
+  };
+
+  float sc[8][8], acc[8][8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sc[i][j] = 0.f;
-  for (int h = 0; h < H; ++h) {
-    float acc[8][8];
+    for (int j = 0; j < 8; ++j) sc[i][j] = acc[i][j] = 0.f;
+  load(0);
+  for (int c = 0; c < nc; ++c) {
+    const int buf = c & 1;
+    store(buf);
+    __syncthreads();
+    if (c + 1 < nc) load(c + 1);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int d = 0; d < kTD; ++d) {   // d ascending: every dot accumulates in order
+      const float4 a0 = *reinterpret_cast<const float4*>(&s.a[buf][d][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&s.a[buf][d][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&s.b[buf][d][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&s.b[buf][d][64 + tx * 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-    for (int d0 = 0; d0 < D; d0 += kTD) {
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {   // 512 float4 of each operand, two per thread
-        const int idx = tid + kScoreThreads * t, r = idx >> 2, c4 = idx & 3;
-        const int d = d0 + 4 * c4;
-        float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-        if (q0 + r < a.Tq && d < D)
-          va = *reinterpret_cast<const float4*>(qI + (int64_t)(q0 + r) * a.q_stride_t +
-                                                (int64_t)h * a.q_stride_h + d);
-        if (k0 + r < a.Tk && d < D)
-          vb = *reinterpret_cast<const float4*>(kI + (int64_t)(k0 + r) * a.k_stride_t + d);
-        s.a[4 * c4 + 0][r] = va.x; s.a[4 * c4 + 1][r] = va.y;
-        s.a[4 * c4 + 2][r] = va.z; s.a[4 * c4 + 3][r] = va.w;
-        s.b[4 * c4 + 0][r] = vb.x; s.b[4 * c4 + 1][r] = vb.y;
-        s.b[4 * c4 + 2][r] = vb.z; s.b[4 * c4 + 3][r] = vb.w;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int d = 0; d < kTD; ++d) {   // d ascending: every dot accumulates in order
-        const float4 a0 = *reinterpret_cast<const float4*>(&s.a[d][ty * 4]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&s.a[d][64 + ty * 4]);
-        const float4 b0 = *reinterpret_cast<const float4*>(&s.b[d][tx * 4]);
-        const float4 b1 = *reinterpret_cast<const float4*>(&s.b[d][64 + tx * 4]);
-        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-      }
-      __syncthreads();
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
-    const float wh = w[h];
+    if ((c + 1) % nd == 0) {   // a head's dots are complete: relu, weight, add
+      const float wh = w[c / nd];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sc[i][j] = fmaf(wh, fmaxf(acc[i][j], 0.f), sc[i][j]);
+        for (int j = 0; j < 8; ++j) {
+          sc[i][j] = fmaf(wh, fmaxf(acc[i][j], 0.f), sc[i][j]);
+          acc[i][j] = 0.f;
+        }
+    }
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {

@@ -9,7 +9,11 @@
 //
 // Each CTA owns two 128-row blocks A and B that read the same KV head: two
 // query heads of one GQA group at the same query tile, or (one KV head per
-// query head) two adjacent query tiles of one head.  The blocks ping-pong on
+// query head) two adjacent query tiles of one head.  For one causal sequence
+// the GQA pair is folded instead: query tile t of one head with tile
+// n_qtiles-1-t of the other, so every CTA has the same number of block-tiles;
+// the block with fewer live KV tiles drops out of the ping-pong when its tiles
+// end.  The blocks ping-pong on
 // the tensor core so that each softmax warpgroup has the other block's MMAs
 // to hide behind:
 //
@@ -53,6 +57,7 @@ struct TcParams {
   int n_qtiles;
   int n_ktiles;
   int head_pairs;   // 1: blocks are two heads of a GQA group; 0: two query tiles
+  int fold;         // 1: head pairs at query tiles t and n_qtiles-1-t
   int n_units;      // CTAs
 };
 
@@ -66,8 +71,8 @@ struct Smem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int n_live;
-  long long min_lo, max_hi;
+  int n_blk[2];     // live-list entries block X runs (a prefix of the list)
+  long long min_lo[2], max_hi[2];
   uint16_t live_kt[kMaxKTiles];
 };
 
@@ -82,8 +87,9 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const cpattn_attn_args& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
-  const Block blk[2] = {block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 0),
-                        block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 1)};
+  const Block blk[2] = {
+      p.fold ? folded_block_of(a.Hq, p.n_qtiles, u, 0) : block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 0),
+      p.fold ? folded_block_of(a.Hq, p.n_qtiles, u, 1) : block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 1)};
   const int g = blk[0].head / (a.Hq / a.Hkv);
   volatile int* abort_flag = &s.abort;
 
@@ -102,8 +108,8 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     mbar_init(&s.drain, 1);
     s.abort = 0;
-    s.min_lo = LLONG_MAX;
-    s.max_hi = LLONG_MIN;
+    s.min_lo[0] = s.min_lo[1] = LLONG_MAX;
+    s.max_hi[0] = s.max_hi[1] = LLONG_MIN;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -136,15 +142,18 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       hi = max(hi, __shfl_xor_sync(kFullMask, hi, o));
     }
     if (lane == 0 && lo <= hi) {
-      atomicMin(&s.min_lo, lo);
-      atomicMax(&s.max_hi, hi);
+      atomicMin(&s.min_lo[X], lo);
+      atomicMax(&s.max_hi[X], hi);
     }
   }
   __syncthreads();
-  const int64_t min_lo = s.min_lo, max_hi = s.max_hi;
+  const int64_t min_lo = min(s.min_lo[0], s.min_lo[1]), max_hi = max(s.max_hi[0], s.max_hi[1]);
 
   // Live KV tiles (those whose logical key range meets some row's interval),
-  // listed once by warp 3 for every role.
+  // listed once by warp 3 for every role.  Block X stops after n_blk[X]
+  // entries when the tiles live for its own rows are a prefix of the list
+  // (one causal sequence: every block starts at key 0); otherwise it runs the
+  // whole list and its rows mask what they do not permit.
   if (warp == 3) {
     int base = 0;
     for (int kt0 = 0; kt0 < p.n_ktiles; kt0 += 32) {
@@ -160,10 +169,29 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (live) s.live_kt[base + __popc(m & ((1u << lane) - 1))] = (uint16_t)kt;
       base += __popc(m);
     }
-    if (lane == 0) s.n_live = base;
+    __syncwarp();
+    for (int x = 0; x < 2; ++x) {
+      const long long lo_x = s.min_lo[x], hi_x = s.max_hi[x];
+      int cnt = 0, last = -1;
+      for (int i0 = 0; i0 < base; i0 += 32) {
+        const int i = i0 + lane;
+        bool live = false;
+        if (i < base && lo_x <= hi_x) {
+          const int64_t j0 = (int64_t)s.live_kt[i] * BN;
+          const int64_t kb = logical_pos(a.kv_chunk_map, a.chunk_len, j0);
+          const int64_t kv = min((int64_t)BN, (int64_t)a.Tk - j0);
+          live = kb <= hi_x && kb + kv - 1 >= lo_x;
+        }
+        const unsigned m = __ballot_sync(kFullMask, live);
+        cnt += __popc(m);
+        if (m) last = i0 + 31 - __clz(m);
+      }
+      if (lane == 0) s.n_blk[x] = (cnt == last + 1) ? cnt : base;
+    }
   }
   __syncthreads();
-  const int n_live = s.n_live;
+  const int nx[2] = {s.n_blk[0], s.n_blk[1]};
+  const int n_run = max(nx[0], nx[1]);   // list entries loaded and multiplied
 
   if (warp < 4) {
   regs_dec<kRegsControl>();
@@ -172,7 +200,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
       bool q_issued = false;
-      for (int i = 0; i < n_live; ++i) {
+      for (int i = 0; i < n_run; ++i) {
         const int kt = s.live_kt[i];
         if (!q_issued) {
           mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
@@ -219,7 +247,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t q_lo0 = desc_lo(smem_u32(s.q[0]), 16), q_lo1 = desc_lo(smem_u32(s.q[1]), 16);
       const uint32_t k_lo0 = desc_lo(smem_u32(s.k[0]), 16), k_lo1 = desc_lo(smem_u32(s.k[1]), 16);
       const uint32_t v_lo0 = desc_lo(smem_u32(s.v[0]), kHalf), v_lo1 = desc_lo(smem_u32(s.v[1]), kHalf);
-      const int n = n_live;
+      const int n = n_run;
       auto issue_s = [&](int j, int x) {   // S_x(j) = Q_x K_j^T
         umma8_ss_kmajor(tmem + kColS + x * BN, x ? q_lo1 : q_lo0, (j & 1) ? k_lo1 : k_lo0, idesc_qk);
         umma_commit(&s.s_full[x]);
@@ -233,34 +261,35 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       bool ok = n > 0 && mbar_wait(&s.q_full, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(0, 1);
+        for (int x = 0; x < 2; ++x)
+          if (nx[x] > 0) issue_s(0, x);
         umma_commit(&s.k_empty[0]);
       }
+      // Step jt: for each block still running, PV_X(jt) then S_X(jt+1).  A
+      // block past its last tile drops out; the V stage is released after the
+      // step's last PV, the next K stage after the step's last S.
       for (int jt = 0; jt < n && ok; ++jt) {
         const int st = jt & 1, st1 = (jt + 1) & 1;
-        const bool more = jt + 1 < n;
-        // block A: PV_A(jt), then S_A(jt+1)
-        if (!mbar_wait(&s.v_full[st], (jt >> 1) & 1, abort_flag) ||
-            !mbar_wait(&s.p_full[0], jt & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        issue_pv(jt, 0);
-        if (!more) umma_commit(&s.o_ready[0]);
-        if (more) {
-          if (!mbar_wait(&s.k_full[st1], ((jt + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&s.v_full[st], (jt >> 1) & 1, abort_flag)) { ok = false; break; }
+        bool k_ready = false;
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (jt >= nx[x]) continue;
+          if (!mbar_wait(&s.p_full[x], jt & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          issue_s(jt + 1, 0);
+          issue_pv(jt, x);
+          if (x == 1 || jt >= nx[1]) umma_commit(&s.v_empty[st]);
+          if (jt + 1 == nx[x]) {
+            umma_commit(&s.o_ready[x]);
+          } else {
+            if (!k_ready) {
+              if (!mbar_wait(&s.k_full[st1], ((jt + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(jt + 1, x);
+          }
         }
-        // block B: PV_B(jt), then S_B(jt+1)
-        if (!mbar_wait(&s.p_full[1], jt & 1, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        issue_pv(jt, 1);
-        umma_commit(&s.v_empty[st]);
-        if (!more) umma_commit(&s.o_ready[1]);
-        if (more) {
-          issue_s(jt + 1, 1);
-          umma_commit(&s.k_empty[st1]);
-        }
+        if (ok && k_ready) umma_commit(&s.k_empty[st1]);
       }
       // every MMA issued so far must finish before TMEM is released
       umma_commit(&s.drain);
@@ -278,7 +307,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float m2 = -CUDART_INF_F, l = 0.f;
     int jt = 0;
     bool ok = true;
-    for (int i = 0; i < n_live; ++i) {
+    for (int i = 0; i < nx[X]; ++i) {
       const int kt = s.live_kt[i];
       const int64_t kbase = logical_pos(a.kv_chunk_map, a.chunk_len, (int64_t)kt * BN);
       const int kvalid = min(BN, a.Tk - kt * BN);
@@ -429,6 +458,10 @@ cudaError_t launch_dense_tc(const cpattn_attn_args& a, cudaStream_t stream, bool
   p.n_qtiles = (a.Tq + BM - 1) / BM;
   p.n_ktiles = (a.Tk + BN - 1) / BN;
   p.head_pairs = ((a.Hq / a.Hkv) % 2 == 0) ? 1 : 0;
+  // One causal sequence without chunk maps: later query tiles see more keys,
+  // so fold the tiles to give every unit the same number of block-tiles.
+  p.fold = (p.head_pairs && a.causal && a.cu_seqlens == nullptr && a.q_chunk_map == nullptr &&
+            a.kv_chunk_map == nullptr) ? 1 : 0;
   p.n_units = p.head_pairs ? p.n_qtiles * (a.Hq / 2) : ((p.n_qtiles + 1) / 2) * a.Hq;
   cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);

@@ -76,6 +76,16 @@ __device__ __forceinline__ Block block_of(int Hq, int head_pairs, int n_qtiles, 
   return Block{u % Hq, (2 * pi + X) * BM};
 }
 
+// Folded head pairs (even GQA groups, one causal sequence): unit u holds query
+// tile t of head 2p and query tile n_qtiles-1-t of head 2p+1.  Under a causal
+// mask tile t sees about t + offset/128 key tiles, so every unit carries the
+// same total; both heads read the same KV head.
+__device__ __forceinline__ Block folded_block_of(int Hq, int n_qtiles, int u, int X) {
+  const int hp = Hq / 2;
+  const int t = u / hp, pr = u % hp;
+  return Block{2 * pr + X, (X ? n_qtiles - 1 - t : t) * BM};
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (fn == nullptr) {

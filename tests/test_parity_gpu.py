@@ -368,20 +368,33 @@ def test_lse_merge_128_channels_neutral_parts_hold_garbage(n_parts, out):
     assert (o[30].float() == 0).all() and torch.isneginf(lse[30]).all()
 
 
-def test_dense_per_unit_schedule_without_workspace():
-    """Without a workspace the one-unit-per-CTA kernel runs; same answer."""
+@pytest.mark.parametrize("Tq,Tk,off,Hq,Hkv,cu", [
+    (640, 1500, 900, 4, 2, None),      # folded head pairs, odd number of query tiles
+    (1000, 1100, 300, 2, 1, None),     # folded, ragged last tile, rows clipped at Tk
+    (128, 4000, 3000, 4, 2, None),     # one query tile: both heads at tile 0
+    (1000, 1000, 0, 8, 2, None),       # offset 0: tile 0 sees one KV tile, tile 7 eight
+    (700, 900, 200, 2, 2, [0, 250, 610, 900]),   # adjacent tiles, packed sequences
+    (700, 900, 200, 4, 2, [0, 250, 610, 900]),   # head pairs, packed sequences
+])
+def test_dense_per_unit_schedule_without_workspace(Tq, Tk, off, Hq, Hkv, cu):
+    """Without a workspace the one-unit-per-CTA kernel runs; same answer.  A
+    block whose live KV tiles are a prefix of its CTA's list stops early (one
+    causal sequence); otherwise it runs the list and masks."""
     import ctypes
     from context_attention_softmax_gb300 import _lib
-    w = inputs.dense_gqa(seed=3, global_seq=640, cp_size=1, rank=0, Hq=4, Hkv=2, Tk=1500,
+    w = inputs.dense_gqa(seed=3, global_seq=Tq, cp_size=1, rank=0, Hq=Hq, Hkv=Hkv, Tk=Tk,
                          kv_chunks=0)
-    w.causal_offset = 900
+    w.causal_offset = off
+    if cu is not None:
+        w.cu_seqlens = np.array(cu, dtype=np.int32)
     q, k, v = f64(w)
     O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w))
     dev = torch.device("cuda")
     qd, kd, vd = w.q.to(dev), w.k.to(dev), w.v.to(dev)
     o = torch.empty((qd.shape[0], qd.shape[1], vd.shape[2]), dtype=qd.dtype, device=dev)
     lse = torch.empty((qd.shape[0], qd.shape[1]), dtype=torch.float32, device=dev)
-    a = pkg._args(qd, kd, vd, w.scale, True, w.causal_offset, None, None, None, 0, o, lse)
+    cu_d = None if cu is None else torch.tensor(cu, dtype=torch.int32, device=dev)
+    a = pkg._args(qd, kd, vd, w.scale, True, w.causal_offset, cu_d, None, None, 0, o, lse)
     lib = _lib.load()
     _lib.check(lib.cpattn_chunk_fwd(ctypes.byref(a), None, 0, torch.cuda.current_stream().cuda_stream))
     torch.cuda.synchronize()

@@ -68,7 +68,7 @@ struct Smem {
   uint64_t q_full;
   uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
   uint64_t s_full[2], p_full[2], o_ready[2];
-  uint64_t drain;
+  uint64_t drain, pv_done;
   uint32_t tmem_base;
   int abort;
   int n_blk[2];     // live-list entries block X runs (a prefix of the list)
@@ -107,6 +107,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(&s.o_ready[x], 1);
     }
     mbar_init(&s.drain, 1);
+    mbar_init(&s.pv_done, 1);
     s.abort = 0;
     s.min_lo[0] = s.min_lo[1] = LLONG_MAX;
     s.max_hi[0] = s.max_hi[1] = LLONG_MIN;
@@ -192,6 +193,14 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   const int nx[2] = {s.n_blk[0], s.n_blk[1]};
   const int n_run = max(nx[0], nx[1]);   // list entries loaded and multiplied
+  // Tail: once the short block Sb has run its n_short tiles, the long block
+  // Lb alternates its S between its own S columns and Sb's, so S(j+1) runs on
+  // the tensor core while softmax(j) runs.  Tail tile n_short + u uses Lb's
+  // columns for even u, Sb's for odd u; both barriers have then completed
+  // n_short + u/2 phases before it.
+  const int Sb = nx[0] < nx[1] ? 0 : 1, Lb = 1 - Sb;
+  const int n_short = nx[Sb];
+  const bool tail2 = n_short >= 1 && nx[Lb] > n_short;
 
   if (warp < 4) {
   regs_dec<kRegsControl>();
@@ -268,9 +277,29 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // Step jt: for each block still running, PV_X(jt) then S_X(jt+1).  A
       // block past its last tile drops out; the V stage is released after the
       // step's last PV, the next K stage after the step's last S.
+      const uint32_t q_lo_l = Lb ? q_lo1 : q_lo0;
       for (int jt = 0; jt < n && ok; ++jt) {
         const int st = jt & 1, st1 = (jt + 1) & 1;
         if (!mbar_wait(&s.v_full[st], (jt >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (tail2 && jt >= n_short) {
+          // tail step: PV(jt) from the buffer holding P(jt), then S(jt+2) into it
+          const int u = jt - n_short, xb = (u & 1) ? Sb : Lb;
+          if (!mbar_wait(&s.p_full[xb], (n_short + (u >> 1)) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          umma8_ts_mnmajor<1>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
+                              idesc_pv);
+          umma_commit(&s.v_empty[st]);
+          umma_commit(&s.pv_done);
+          if (jt + 1 == n) umma_commit(&s.o_ready[Lb]);
+          if (jt + 2 < n) {
+            if (!mbar_wait(&s.k_full[st], ((jt + 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            umma8_ss_kmajor(tmem + kColS + xb * BN, q_lo_l, st ? k_lo1 : k_lo0, idesc_qk);
+            umma_commit(&s.s_full[xb]);
+            umma_commit(&s.k_empty[st]);
+          }
+          continue;
+        }
         bool k_ready = false;
         for (int x = 0; x < 2 && ok; ++x) {
           if (jt >= nx[x]) continue;
@@ -290,6 +319,15 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         }
         if (ok && k_ready) umma_commit(&s.k_empty[st1]);
+        if (ok && tail2 && jt + 1 == n_short && n_short + 1 < n) {
+          // first tail tile's successor: S(n_short+1) into Sb's columns, which
+          // PV_Sb(n_short-1), issued before it, has finished reading
+          if (!mbar_wait(&s.k_full[st], ((n_short + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          umma8_ss_kmajor(tmem + kColS + Sb * BN, q_lo_l, st ? k_lo1 : k_lo0, idesc_qk);
+          umma_commit(&s.s_full[Sb]);
+          umma_commit(&s.k_empty[st]);
+        }
       }
       // every MMA issued so far must finish before TMEM is released
       umma_commit(&s.drain);
@@ -316,13 +354,23 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         lo_c = (int)max((int64_t)0, min((int64_t)BN, iv.lo - kbase));
         hi_c = (int)max((int64_t)-1, min((int64_t)kvalid - 1, iv.hi - kbase));
       }
-      ok = __all_sync(kFullMask, mbar_wait(&s.s_full[X], jt & 1, abort_flag));
+      // S buffer of this tile and the phase its barriers are in
+      int xb = X;
+      uint32_t ph = jt & 1;
+      const bool in_tail = tail2 && X == Lb && i >= n_short;
+      if (in_tail) {
+        const int u = i - n_short;
+        xb = (u & 1) ? Sb : Lb;
+        ph = (n_short + (u >> 1)) & 1;
+      }
+      const uint32_t sb_col = s_col + (uint32_t)((xb - X) * BN);
+      ok = __all_sync(kFullMask, mbar_wait(&s.s_full[xb], ph, abort_flag));
       if (!ok) break;
       tc_fence_after();
       float sv[BN];
       {
         uint32_t rr[BN];
-        tmem_ld128_sync(s_col, rr);
+        tmem_ld128_sync(sb_col, rr);
 #pragma unroll
         for (int c = 0; c < BN; ++c) sv[c] = __uint_as_float(rr[c]);
       }
@@ -334,11 +382,11 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // row max: four independent chains of 3-input max
       float pm[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) pm[i] = fmaxf(sv[2 * i], sv[2 * i + 1]);
+      for (int q = 0; q < 4; ++q) pm[q] = fmaxf(sv[2 * q], sv[2 * q + 1]);
 #pragma unroll
       for (int c = 8; c < BN; c += 8) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) pm[i] = fmax3(pm[i], sv[c + 2 * i], sv[c + 2 * i + 1]);
+        for (int q = 0; q < 4; ++q) pm[q] = fmax3(pm[q], sv[c + 2 * q], sv[c + 2 * q + 1]);
       }
       float mx = fmax3(pm[0], pm[1], fmaxf(pm[2], pm[3])) * sl2;
       float alpha = 1.f;
@@ -370,25 +418,32 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           rs2[c & 1] = f2_add(rs2[c & 1], f2_pack(p0, p1));
           pk[c] = pack_bf16(p0, p1);
         }
-        tmem_st32(s_col + 32 * half, pk);
+        tmem_st32(sb_col + 32 * half, pk);
       }
       float a0, a1;
       f2_unpack(f2_add(rs2[0], rs2[1]), a0, a1);
       l = l * alpha + (a0 + a1);
       // PV_X(jt-1) has finished: S_X(jt) was issued after it and has landed.
+      // In the tail S(jt) follows only PV(jt-2): wait for PV(jt-1), the
+      // (jt - n_short)-th tail PV, unless jt is the first tail tile.
       if (__any_sync(kFullMask, rescale)) {
+        if (in_tail && i > n_short) {
+          ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (i - n_short - 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+        }
 #pragma unroll
         for (int c4 = 0; c4 < HD / 32; ++c4) {
           uint32_t oo[32];
           tmem_ld32_sync(o_col + c4 * 32, oo);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
+          for (int q = 0; q < 32; ++q) oo[q] = __float_as_uint(__uint_as_float(oo[q]) * alpha);
           tmem_st32(o_col + c4 * 32, oo);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&s.p_full[X]);
+      mbar_arrive(&s.p_full[xb]);
       ++jt;
     }
     if (ok && jt > 0) {

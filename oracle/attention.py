@@ -33,7 +33,7 @@ Every function cites the passage it follows, by page title and paragraph:
 [MoBA-CP] "Question on Implementing Context Parallelism with MoBA Efficient
           Attention": gating scores Q x K^T choose the top-k KV blocks.
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
   * neutral summary = (m=-inf, l=0, z=0); no permitted key -> O = 0, LSE = -inf;
   * LSE is a natural log of the scaled scores: LSE = m + ln(l);
   * GQA: query head h reads KV head h // (Hq // Hkv);

@@ -26,6 +26,7 @@ import ctypes
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -409,6 +410,27 @@ def time_steps(fn, steps, warmup, flush, world):
 # arms
 # ---------------------------------------------------------------------------
 
+def host_info():
+    """CPU model and the BLAS numpy was built against, for the oracle timings."""
+    model = platform.machine()
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for ln in fh:
+                key = ln.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part"):
+                    model = ln.split(":", 1)[1].strip() if key == "model name" else \
+                        f"{platform.machine()} part {ln.split(':', 1)[1].strip()}"
+                    break
+    except OSError:
+        pass
+    blas = "unknown"
+    try:
+        blas = np.show_config(mode="dicts")["Build Dependencies"]["blas"]["name"]
+    except Exception:
+        pass
+    return {"cpu_model": model, "blas": blas}
+
+
 def cpu_baseline(runner, budget_s=12.0, batch=32):
     """Time the oracle as it stands on a bounded sample of query rows."""
     rng = np.random.default_rng(123)
@@ -422,7 +444,7 @@ def cpu_baseline(runner, budget_s=12.0, batch=32):
         rows_done += batch
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle",
+            "kind": "oracle", **host_info(),
             "sample": f"{rows_done} query rows drawn at random ({rows_done / n:.1f}x the "
                       f"{n}-row problem; all heads, all permitted keys), float64 numpy, "
                       f"{dt:.1f} s"}
@@ -451,7 +473,7 @@ def run_reference(args, world, rank):
         "dtype": "f64", "data": "synthetic (seeded N(0,1)*0.5, bf16-rounded)",
         "config": runner.config,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle",
-                         "cores": len(os.sched_getaffinity(0)),
+                         "cores": len(os.sched_getaffinity(0)), **host_info(),
                          "sample": f"each step: {per_step_rows} random query rows x all heads of "
                                    "the workload; ms_per_step extrapolated to the full problem "
                                    "by permitted pairs"},
@@ -532,6 +554,7 @@ def run_ours(args, world, rank, local):
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": mean_ms,
         "ms_min": min(times), "ms_median": statistics.median(times),
+        "ms_p90": float(np.percentile(times, 90)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16-rounded; no dataset)",
         "config": runner.config, "roofline": roof, "clocks": clk,

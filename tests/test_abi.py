@@ -126,3 +126,48 @@ def test_sparse_and_gate_validation(lib):
     assert lib.cpattn_block_gate(ctypes.byref(g), 64, 3, 0x8000, 0x9000, need, None) == 2
     assert lib.cpattn_lse_merge(2, 0x1000, 0x2000, 4, 2, 12, 0x3000, 1, 24, 12, None, None) == 1
     assert lib.cpattn_lse_merge(2, 0x1000, 0x2000, 4, 2, 16, 0x3000, 5, 32, 16, None, None) == 1
+
+
+def _indexer_args():
+    a = _lib.AttnArgs()
+    a.dtype = _lib.CPATTN_FP32
+    a.q, a.q_stride_t, a.q_stride_h, a.Tq, a.Hq, a.Dqk = 0x10000, 4 * 128, 128, 64, 4, 128
+    a.k, a.k_stride_t, a.k_stride_h, a.Tk, a.Hkv = 0x20000, 128, 128, 256, 1
+    a.scale, a.causal = 1.0, 1
+    return a
+
+
+@pytest.mark.parametrize("mutate,topk,status,msg", [
+    (lambda a: setattr(a, "dtype", _lib.CPATTN_BF16), 16, 2, "CPATTN_FP32"),
+    (lambda a: (setattr(a, "Hq", 4), setattr(a, "Hkv", 2)), 16, 1, "one head"),
+    (lambda a: (setattr(a, "Hq", 32), setattr(a, "q_stride_t", 32 * 128)), 16, 2, "exceed 16"),
+    (lambda a: (setattr(a, "Dqk", 512), setattr(a, "q_stride_h", 512), setattr(a, "q_stride_t", 4 * 512),
+                setattr(a, "k_stride_t", 512), setattr(a, "k_stride_h", 512)), 16, 2, "exceeds 256"),
+    (lambda a: (setattr(a, "kv_chunk_map", 0x5000), setattr(a, "chunk_len", 128),
+                setattr(a, "n_kv_chunks", 2)), 16, 2, "logical order"),
+    (lambda a: None, 0, 1, "topk=0"),
+    (lambda a: None, 257, 1, "topk=257"),
+])
+def test_indexer_rejects_bad_arguments(lib, mutate, topk, status, msg):
+    """Host validation of the indexer call: nothing is launched on rejection."""
+    a = _indexer_args()
+    mutate(a)
+    assert lib.cpattn_dsa_indexer(ctypes.byref(a), 0x7000, topk, 0x8000, None, 0, None) == status
+    assert msg in lib.cpattn_last_error().decode()
+
+
+def test_indexer_needs_weights_outputs_and_its_workspace(lib):
+    a = _indexer_args()
+    assert lib.cpattn_dsa_indexer(ctypes.byref(a), None, 16, 0x8000, None, 0, None) == 1
+    assert "w is NULL" in lib.cpattn_last_error().decode()
+    assert lib.cpattn_dsa_indexer(ctypes.byref(a), 0x7000, 16, None, None, 0, None) == 1
+    assert "indices is NULL" in lib.cpattn_last_error().decode()
+    need = lib.cpattn_workspace_size(_lib.OP_DSA_INDEXER, ctypes.byref(a), 16, 1)
+    # fp32 scores [Tq, Tk] and the two norm vectors come first
+    assert need >= 64 * 256 * 4 + 256 * 4 + 64 * 4
+    assert lib.cpattn_dsa_indexer(ctypes.byref(a), 0x7000, 16, 0x8000, None, 0, None) == 4
+    assert lib.cpattn_dsa_indexer(ctypes.byref(a), 0x7000, 16, 0x8000, 0x9000, need - 1, None) == 4
+    assert lib.cpattn_dsa_indexer(ctypes.byref(a), 0x7000, 16, 0x8000, 0x9008, need, None) == 1
+    assert "aligned" in lib.cpattn_last_error().decode()
+    a.Tq = 0     # nothing to select: no workspace needed
+    assert lib.cpattn_workspace_size(_lib.OP_DSA_INDEXER, ctypes.byref(a), 16, 1) == 0

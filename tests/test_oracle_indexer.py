@@ -119,3 +119,46 @@ def test_weight_scale_and_head_order_do_not_change_the_selection():
     np.testing.assert_array_equal(_sel(qI, kI, w * 4.0, lay, 7), base)   # power-of-two scale is exact
     perm = np.array([2, 0, 3, 1])
     np.testing.assert_array_equal(_sel(qI[:, perm], kI, w[perm], lay, 7), base)
+
+
+def _brute_topk(qI, kI, w, qpos, kpos, seq_q, seq_k, causal, topk):
+    """Scalar loops with math.fsum: the score definition, the permitted
+    relation, then a full sort of (score desc, j asc) per row."""
+    import math
+    Tq, H, D = qI.shape
+    out = []
+    for i in range(Tq):
+        cands = []
+        for j in range(kI.shape[0]):
+            if seq_q[i] < 0 or seq_q[i] != seq_k[j] or (causal and kpos[j] > qpos[i]):
+                continue
+            sc = math.fsum(float(w[h]) * max(0.0, math.fsum(float(qI[i, h, d]) * float(kI[j, d])
+                                                             for d in range(D)))
+                           for h in range(H))
+            cands.append((-sc, j))
+        cands.sort()
+        row = sorted(j for _, j in cands[:topk])
+        out.append(row + [-1] * (topk - len(row)))
+    return np.array(out)
+
+
+def test_brute_force_with_mixed_sign_weights_packed_and_offset():
+    """A negative head weight turns that head's ReLU into a penalty; two
+    packed sequences, a causal offset and a query past the last sequence
+    (it selects nothing).  The oracle equals scalar brute force."""
+    rng = np.random.default_rng(8)
+    Tq, Tk, H, D, k = 14, 40, 3, 6, 5
+    qI = rng.standard_normal((Tq, H, D))
+    kI = rng.standard_normal((Tk, D))
+    w = np.array([0.8, -0.5, 0.3])
+    cu = np.array([0, 17, 38])
+    lay = orc.make_layout(Tq, Tk, causal=True, causal_offset=25, cu_seqlens=cu)
+    got = _sel(qI, kI, w, lay, k)
+    qpos = 25 + np.arange(Tq)
+    kpos = np.arange(Tk)
+    seq = lambda p: np.searchsorted(cu, p, side="right") - 1 if p < cu[-1] else -1
+    seq_q = [seq(p) for p in qpos]
+    seq_k = [seq(p) for p in kpos]
+    ref = _brute_topk(qI, kI, w, qpos, kpos, seq_q, seq_k, True, k)
+    np.testing.assert_array_equal(got, ref)
+    assert (got[qpos >= 38] == -1).all()            # positions 38.. are in no sequence

@@ -397,15 +397,25 @@ def sparse_attention(q, k, v, scale, layout, indices, block_size=1, rows=None):
 # MoBA block gate  ([MoBA-CP]: gating scores Q x K^T choose top-k KV blocks)
 # ---------------------------------------------------------------------------
 
-def block_means(k, block_size):
-    """Mean of the keys of every complete block, per KV head: [n_blocks, Hkv, D]."""
+def block_means(k, block_size, kpos=None):
+    """Mean of the keys of every complete block, per KV head: [n_blocks, Hkv, D].
+
+    Blocks are runs of LOGICAL key positions [b*B, (b+1)*B) ([MoBA-CP] blocks
+    of the sequence; [CP] ¶5 a chunk map changes where a key is stored, not
+    its position).  ``kpos`` gives the logical position of each stored KV row
+    (None: stored in logical order); the rows are put back in logical order
+    before pooling.
+    """
     k = np.asarray(k, np.float64)
+    if kpos is not None:
+        order = np.argsort(np.asarray(kpos, dtype=np.int64), kind="stable")
+        k = k[order]
     n_blocks = k.shape[0] // block_size
     kb = k[: n_blocks * block_size].reshape(n_blocks, block_size, k.shape[1], k.shape[2])
     return kb.sum(axis=1) / block_size
 
 
-def moba_block_gate(q, k, qpos, block_size, topk, rows=None):
+def moba_block_gate(q, k, qpos, block_size, topk, rows=None, kpos=None):
     """Block selection of every (query, head) pair.
 
     gate(i, h, b) = <q_ih, mean of block b's keys of KV head g(h)> (unscaled).
@@ -414,13 +424,15 @@ def moba_block_gate(q, k, qpos, block_size, topk, rows=None):
     with the largest gate are chosen, equal gates going to the lower block;
     fewer candidates -> all of them.  The own block is always added.  The
     row is returned in ascending block order, padded with -1 to topk + 1.
+    Blocks are blocks of logical positions; ``kpos`` (logical position of
+    each stored KV row, None = logical order) is passed to ``block_means``.
 
     Returns sel int32 [R, Hq, topk + 1].
     """
     q = np.asarray(q, np.float64)
     Tq, Hq, _ = q.shape
     Hkv = k.shape[1]
-    mu = block_means(k, block_size)
+    mu = block_means(k, block_size, kpos)
     n_blocks = mu.shape[0]
     rows = np.arange(Tq) if rows is None else np.asarray(rows, dtype=np.int64)
     own = np.asarray(qpos, dtype=np.int64)[rows] // block_size
@@ -461,10 +473,13 @@ def dsa_indexer_topk(qI, kI, w, layout, topk, rows=None):
         score(i, j) = sum_h w_h * max(0, <qI[i, h], kI[j]>),
 
     taken over the keys the layout permits (same sequence, kpos_j <= qpos_i
-    when causal), in float64 from the exact inputs.  The ``topk`` keys with
-    the largest score are chosen, equal scores going to the lower j; a row
-    with fewer permitted keys takes all of them.  Each row is returned in
-    ascending j and padded with -1.
+    when causal), in float64 from the exact inputs.  Keys are named by their
+    LOGICAL position ([DSA-CP]: global coordinates; [CP] ¶5: a chunk map
+    changes where a key is stored, not its position): kI row j is stored at
+    physical row j and sits at logical position layout.kpos[j].  The
+    ``topk`` keys with the largest score are chosen, equal scores going to
+    the lower logical position; a row with fewer permitted keys takes all of
+    them.  Each row is returned as ascending logical positions padded with -1.
 
     qI: [Tq, H, D], kI: [Tk, D], w: [H].  Returns int32 [R, 1, topk].
     """
@@ -480,9 +495,10 @@ def dsa_indexer_topk(qI, kI, w, layout, topk, rows=None):
         A = layout.allowed(np.array([i]))[0]
         dots = qI[i] @ kI.T                               # [H, Tk]
         score = (w[:, None] * np.maximum(dots, 0.0)).sum(axis=0)
-        cand = j[A]
-        # descending score, ties to the lower j: sort by (-score, j)
-        order = np.lexsort((cand, -score[cand]))
-        chosen = np.sort(cand[order[:topk]])
+        phys = j[A]
+        logical = layout.kpos[A]
+        # descending score, ties to the lower logical position
+        order = np.lexsort((logical, -score[phys]))
+        chosen = np.sort(logical[order[:topk]])
         out[r, 0, :len(chosen)] = chosen
     return out

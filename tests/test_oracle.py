@@ -478,3 +478,45 @@ def test_moba_with_all_blocks_equals_dense_causal():
     Od, Ld = orc.dense_attention(q, k, v, 0.3, lay)
     np.testing.assert_allclose(O, Od, atol=1e-13, rtol=0)
     np.testing.assert_allclose(LSE, Ld, atol=1e-13, rtol=0)
+
+
+def brute_gate_logical(q, k, kpos, qpos, B, topk):
+    """Scalar gate whose blocks are runs of LOGICAL key positions: block b
+    pools the stored rows j with kpos[j] // B == b (complete blocks only)."""
+    Tq, Hq, D = q.shape
+    Hkv = k.shape[1]
+    nb = len(kpos) // B
+    sel = np.full((Tq, Hq, topk + 1), -1, np.int32)
+    for i in range(Tq):
+        own = qpos[i] // B
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            gates = []
+            for b in range(min(own, nb)):
+                rows = [j for j in range(len(kpos)) if kpos[j] // B == b]
+                mu = [math.fsum(k[j, g, d] for j in rows) / B for d in range(D)]
+                gates.append((-math.fsum(q[i, h, d] * mu[d] for d in range(D)), b))
+            chosen = sorted([b for _, b in sorted(gates)[:topk]] + [own])
+            sel[i, h, :len(chosen)] = chosen
+    return sel
+
+
+def test_gate_with_a_kv_chunk_map_pools_logical_blocks():
+    """Keys stored in zigzag order with blocks smaller than a chunk: the
+    means pool logical blocks, so the selection equals scalar brute force
+    over logical positions and equals the gate on the same keys stored in
+    logical order ([CP] para 5)."""
+    rng = np.random.default_rng(17)
+    L, n_chunks, B, topk = 8, 6, 4, 2
+    Tk = L * n_chunks
+    cmap = np.array([0, 5, 1, 4, 2, 3])
+    k_log = rnd(rng, Tk, 2, 5)
+    q = rnd(rng, 7, 4, 5)
+    phys_to_log = cmap[np.arange(Tk) // L] * L + np.arange(Tk) % L
+    k_phys = k_log[phys_to_log]
+    lay = orc.make_layout(7, Tk, True, 41, kv_chunk_map=cmap, chunk_len=L)
+    sel = orc.moba_block_gate(q, k_phys, lay.qpos, B, topk, kpos=lay.kpos)
+    np.testing.assert_array_equal(sel, brute_gate_logical(q, k_phys, lay.kpos, lay.qpos, B, topk))
+    np.testing.assert_array_equal(sel, orc.moba_block_gate(q, k_log, lay.qpos, B, topk))
+    # pooling physical rows instead would pick other blocks for this seed
+    assert not np.array_equal(sel, orc.moba_block_gate(q, k_phys, lay.qpos, B, topk))

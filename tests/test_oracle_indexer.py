@@ -135,7 +135,7 @@ def _brute_topk(qI, kI, w, qpos, kpos, seq_q, seq_k, causal, topk):
             sc = math.fsum(float(w[h]) * max(0.0, math.fsum(float(qI[i, h, d]) * float(kI[j, d])
                                                              for d in range(D)))
                            for h in range(H))
-            cands.append((-sc, j))
+            cands.append((-sc, int(kpos[j])))     # a key is named by its logical position
         cands.sort()
         row = sorted(j for _, j in cands[:topk])
         out.append(row + [-1] * (topk - len(row)))
@@ -162,3 +162,32 @@ def test_brute_force_with_mixed_sign_weights_packed_and_offset():
     ref = _brute_topk(qI, kI, w, qpos, kpos, seq_q, seq_k, True, k)
     np.testing.assert_array_equal(got, ref)
     assert (got[qpos >= 38] == -1).all()            # positions 38.. are in no sequence
+
+
+def test_brute_force_with_a_kv_chunk_map():
+    """Keys stored in zigzag order (physical chunk c holds logical chunk
+    map[c]): the oracle names each chosen key by its LOGICAL position, ranks
+    equal scores by logical position, and equals scalar brute force over the
+    logical positions.  Storing the same keys in logical order gives the same
+    selection ([CP] para 5: the layout changes ownership, not the relation)."""
+    rng = np.random.default_rng(9)
+    L, n_chunks, H, D, k = 8, 6, 2, 5, 7
+    Tk, Tq = L * n_chunks, 11
+    cmap = np.array([0, 5, 1, 4, 2, 3])
+    kI_logical = rng.standard_normal((Tk, D))
+    kI_logical[33] = kI_logical[9]                    # equal keys in different chunks
+    qI = rng.standard_normal((Tq, H, D))
+    qI[4] = np.stack([kI_logical[9] * 4.0, kI_logical[9]])   # favours keys 9 and 33
+    w = np.array([0.6, 0.4])
+    phys_to_log = (cmap[np.arange(Tk) // L] * L + np.arange(Tk) % L)
+    kI_phys = np.empty_like(kI_logical)
+    kI_phys[np.arange(Tk)] = kI_logical[phys_to_log]
+    lay = orc.make_layout(Tq, Tk, causal=True, causal_offset=36, kv_chunk_map=cmap, chunk_len=L)
+    got = _sel(qI, kI_phys, w, lay, k)
+    qpos = 36 + np.arange(Tq)
+    ref = _brute_topk(qI, kI_phys, w, qpos, lay.kpos, [0] * Tq, [0] * Tk, True, k)
+    np.testing.assert_array_equal(got, ref)
+    lay_log = orc.make_layout(Tq, Tk, causal=True, causal_offset=36)
+    np.testing.assert_array_equal(got, _sel(qI, kI_logical, w, lay_log, k))
+    assert {9, 33} <= set(got[4].tolist())
+    assert got.max() <= qpos.max()

@@ -1,30 +1,39 @@
 #!/usr/bin/env python
 """Throughput of CP-chunk attention on one GB300 (or N replicas under torchrun).
 
-Default workload (the headline): dense causal CP chunk, bf16 in / fp32
+Headline (the top-level `value`): dense causal CP chunk, bf16 in / fp32
 accumulate, rank 2 of 4 of an 8192-token sequence -> 2048 queries at
 causal_offset 4096 against 8192 keys, 16 query heads over 4 KV heads, d = 128,
 scale 1/sqrt(128), N(0,1) * 0.5 inputs (seed 0).  One step = one
 cpattn_chunk_fwd call over the whole problem (all KV chunks folded and
-merged in the kernel).  The metric is algorithmic TFLOP/s: 4 * d FLOPs per
+merged in the kernel).  Metric: algorithmic TFLOP/s, 4 * d FLOPs per
 permitted (query, key) pair per head (QK^T and PV), masked work not counted.
 
-Other workloads (--workload zigzag | dsa | moba) are measurement aids.
+The same JSON line carries one record per other workload under "workloads",
+each timed the same way with its own roofline, oracle baseline and
+end-to-end figure:
+  dense_gqa_4chunks  the headline problem as 4 KV-chunk summaries + merge
+  zigzag             packed THD varlen, zigzag cp=8, all 8 rank calls (TFLOP/s)
+  dsa                DSA top-2048 sparse attention, absorbed MLA (TFLOP/s and
+                     gathered GB/s)
+  moba               MoBA gate + block-sparse attention (compulsory GB/s)
+  dsa_indexer        the DSA indexer's exact top-2048 (fp32 TFLOP/s)
+`--workload NAME` times one of them alone as the top-level record.
 
 Timing: W untimed warm-up steps, then exactly K timed steps; before each
 timed step a 256 MiB buffer is written to flush the 129 MB L2; each step is
 bracketed by CUDA events on the launching stream; barrier + synchronize
-around the timed region; max over ranks.  `e2e` times the same call with
-host (pinned) inputs copied in and outputs copied out inside each step.
+around the timed region; max over ranks.  Before the first timed step the
+GPU is given a short backlog of flush writes so that it never waits for the
+host to enqueue a step.  `e2e` times the same public call with pinned host
+inputs copied in and the outputs copied out inside each step.
 `--impl reference` times the float64 CPU oracle instead (bounded samples).
 """
 
 from __future__ import annotations
 
 import argparse
-import ctypes
 import json
-import math
 import os
 import platform
 import statistics
@@ -44,15 +53,16 @@ from context_attention_softmax_gb300 import inputs  # noqa: E402
 L2_FLUSH_BYTES = 256 << 20
 METRIC = "CP-chunk attention fwd TFLOP/s (dense) & GB/s (top-k sparse) vs GB300 peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+L2_NOTE = "flushed by a 256 MiB write before every timed step"
 
 
 # ---------------------------------------------------------------------------
-# workloads
+# recorded DRAM traffic of the dominant kernels
 # ---------------------------------------------------------------------------
 
-# DRAM bytes per launch of the dominant kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture, summarised under profiles/),
-# valid only while the kernel's sources hash to the value they had then.
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of a workload's
+# dominant kernel from one ncu capture (summarised under profiles/), valid
+# only while the kernel's sources hash to the value they had then.
 TRAFFIC = {
     "dense_gqa": {"bytes": 21_066_496 + 0, "kernel": "dense_tc_kernel",
                   "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
@@ -68,8 +78,7 @@ def measured_traffic(name):
     t = TRAFFIC.get(name)
     if t is None:
         return None, "no ncu capture recorded for this workload"
-    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "context_attention_softmax_gb300",
-                        "csrc")
+    csrc = os.path.join(ROOT, "context_attention_softmax_gb300", "csrc")
     m = hashlib.sha256()
     for f in t["sources"]:
         with open(os.path.join(csrc, f), "rb") as fh:
@@ -79,56 +88,100 @@ def measured_traffic(name):
     return t["bytes"], t["kernel"]
 
 
-class DenseRunner:
-    """The headline workload: one dense GQA CP-chunk call."""
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+class Runner:
+    """One workload: device inputs, one step through the public API, its
+    algorithmic work per step, and the oracle on a sample of its query rows.
+
+    work / seconds / scale = value in `unit`.
+    """
+
+    name = ""
+    unit = "TFLOP/s"
+    scale = 1e12
+    bound = "tensor"
+    kernel = "cpattn_chunk_fwd"
+    launches_per_step = 1
+    work = 0.0
+    n_rows = 0
+    extras: dict = {}
+
+    def device_inputs(self):
+        raise NotImplementedError
+
+    def step(self, *ins):
+        raise NotImplementedError
+
+    def outputs(self):
+        raise NotImplementedError
+
+    def oracle_sample(self, rows):
+        """Run the oracle on query rows `rows`; return the work units done."""
+        raise NotImplementedError
+
+    def extra_figures(self, seconds):
+        return {}
+
+
+class DenseRunner(Runner):
+    """The headline workload: one dense GQA CP-chunk call (KV folded in-kernel)."""
 
     name = "dense_gqa"
 
-    def __init__(self, device=None):
+    def __init__(self, device=None, kv_chunks=False):
         self.w = w = inputs.dense_gqa()
+        self.kv_chunks = kv_chunks
         Tq, Hq, D = w.q.shape
         qpos = w.causal_offset + np.arange(Tq)
         pairs = int(np.minimum(qpos + 1, w.Tk).sum())          # causal, one sequence
         self.pairs_per_head = pairs
-        self.flops = 4.0 * D * pairs * Hq
-        self.launches_per_step = 1
-        self.bound = "tensor"
+        self.work = 4.0 * D * pairs * Hq
+        self.n_rows = Tq
+        if kv_chunks:
+            self.name = "dense_gqa_4chunks"
+            self.launches_per_step = 2                        # chunk summaries, LSE merge
+            how = ("KV as 4 chunks of 2048: per-chunk finalised summaries (O_c, LSE_c), then "
+                   "cpattn_lse_merge (chunk 3 fully masked, neutral)")
+        else:
+            how = "KV folded in-kernel (4 chunks of 2048, chunk 3 fully masked)"
         self.config = {
             "workload": "dense causal CP chunk, bf16 in / fp32 acc: 2048 queries (rank 2 of 4, "
-                        "causal_offset 4096) x 8192 keys, 16 q heads / 4 kv heads, d=128, "
-                        "KV folded in-kernel (4 chunks of 2048, chunk 3 fully masked)",
+                        "causal_offset 4096) x 8192 keys, 16 q heads / 4 kv heads, d=128, " + how,
             "Tq": Tq, "Tk": w.Tk, "Hq": Hq, "Hkv": w.k.shape[1], "D": D,
             "causal_offset": w.causal_offset, "permitted_pairs_per_head": pairs,
-            "l2": "flushed by a 256 MiB write before every timed step",
-            "seed": 0,
+            "l2": L2_NOTE, "seed": 0,
         }
         if device is not None:
-            self.dev = device
             self.q, self.k, self.v = (t.to(device) for t in (w.q, w.k, w.v))
             self.o = torch.empty((Tq, Hq, w.v.shape[2]), dtype=torch.bfloat16, device=device)
             self.lse = torch.empty((Tq, Hq), dtype=torch.float32, device=device)
             self.ws = torch.empty(64 << 20, dtype=torch.uint8, device=device)   # per-piece summaries
+            if kv_chunks:
+                n = -(-w.Tk // w.kv_chunk_len)
+                self.po = torch.empty((n, Tq, Hq, D), dtype=torch.float32, device=device)
+                self.pl = torch.empty((n, Tq, Hq), dtype=torch.float32, device=device)
 
-    def step(self, q=None, k=None, v=None):
-        from context_attention_softmax_gb300 import cpattn_chunk_fwd
+    def device_inputs(self):
+        return [self.q, self.k, self.v]
+
+    def step(self, q, k, v):
+        from context_attention_softmax_gb300 import cpattn_chunk_fwd, cpattn_lse_merge
         w = self.w
-        cpattn_chunk_fwd(q if q is not None else self.q, k if k is not None else self.k,
-                         v if v is not None else self.v, scale=w.scale, causal=True,
-                         causal_offset=w.causal_offset, out=self.o, lse=self.lse,
-                         workspace=self.ws)
-
-    # host buffers for the end-to-end measurement
-    def host_inputs(self):
-        return [self.w.q.pin_memory(), self.w.k.pin_memory(), self.w.v.pin_memory()]
-
-    def host_outputs(self):
-        return [torch.empty_like(self.o, device="cpu").pin_memory(),
-                torch.empty_like(self.lse, device="cpu").pin_memory()]
+        if self.kv_chunks:
+            cpattn_chunk_fwd(q, k, v, scale=w.scale, causal=True, causal_offset=w.causal_offset,
+                             kv_chunk_len=w.kv_chunk_len, out=self.o, lse=self.lse,
+                             partial_o=self.po, partial_lse=self.pl, workspace=self.ws)
+            cpattn_lse_merge(self.po, self.pl, out=self.o, lse=self.lse)
+        else:
+            cpattn_chunk_fwd(q, k, v, scale=w.scale, causal=True, causal_offset=w.causal_offset,
+                             out=self.o, lse=self.lse, workspace=self.ws)
 
     def outputs(self):
         return [self.o, self.lse]
 
-    # the oracle on a bounded sample of query rows
     def oracle_sample(self, rows):
         import oracle as orc
         w = self.w
@@ -136,18 +189,20 @@ class DenseRunner:
             self._f64 = (inputs.as_f64(w.q), inputs.as_f64(w.k), inputs.as_f64(w.v))
             self._lay = orc.make_layout(w.Tq, w.Tk, True, w.causal_offset)
         q, k, v = self._f64
-        orc.dense_attention(q, k, v, w.scale, self._lay, rows=rows)
+        if self.kv_chunks:
+            orc.summarised_attention(q, k, v, w.scale, self._lay, w.kv_chunk_len, rows=rows)
+        else:
+            orc.dense_attention(q, k, v, w.scale, self._lay, rows=rows)
         qpos = w.causal_offset + rows
         return 4.0 * w.q.shape[2] * float(np.minimum(qpos + 1, w.Tk).sum()) * w.q.shape[1]
 
 
-class ZigzagRunner:
+class ZigzagRunner(Runner):
     """All 8 zigzag ranks of the packed THD varlen workload (8 calls per step)."""
 
     name = "zigzag"
 
     def __init__(self, device):
-        from context_attention_softmax_gb300 import _lib  # noqa: F401
         self.z = z = inputs.zigzag_varlen()
         self.dev = device
         self.k, self.v = z.k_gathered.to(device), z.v_gathered.to(device)
@@ -162,56 +217,116 @@ class ZigzagRunner:
         lens = np.diff(z.cu_seqlens.astype(np.int64))
         pairs = int((lens * (lens + 1) // 2).sum())
         H, D = z.q_global.shape[1], z.q_global.shape[2]
-        self.flops = 4.0 * D * pairs * H
+        self.work = 4.0 * D * pairs * H
+        self.n_rows = z.q_global.shape[0]
         self.launches_per_step = z.cp_size
-        self.bound = "tensor"
         self.config = {"workload": "packed THD varlen, zigzag cp=8, 16384 tokens / 8 seqs, "
                                    "32 heads, d=128, causal; all 8 rank calls",
-                       "lengths": lens.tolist(), "permitted_pairs_per_head": pairs,
-                       "l2": "flushed by a 256 MiB write before every timed step"}
+                       "lengths": lens.tolist(), "permitted_pairs_per_head": pairs, "l2": L2_NOTE}
 
-    def step(self):
+    def device_inputs(self):
+        return self.qs + [self.k, self.v]
+
+    def step(self, *ins):
         from context_attention_softmax_gb300 import cpattn_chunk_fwd
         z = self.z
+        qs, k, v = ins[:z.cp_size], ins[z.cp_size], ins[z.cp_size + 1]
         for r in range(z.cp_size):
-            cpattn_chunk_fwd(self.qs[r], self.k, self.v, scale=z.scale, causal=True,
-                             cu_seqlens=self.cu, q_chunk_map=self.maps[r], kv_chunk_map=self.kvmap,
+            cpattn_chunk_fwd(qs[r], k, v, scale=z.scale, causal=True, cu_seqlens=self.cu,
+                             q_chunk_map=self.maps[r], kv_chunk_map=self.kvmap,
                              chunk_len=z.chunk_len, out=self.o[r], lse=self.lse[r],
                              workspace=self.ws)
 
+    def outputs(self):
+        return self.o + self.lse
 
-class DsaRunner:
+    def oracle_sample(self, rows):
+        """rows: logical positions of the packed stream (whatever rank owns them)."""
+        import oracle as orc
+        z = self.z
+        if not hasattr(self, "_f64"):
+            self._f64 = tuple(inputs.as_f64(t) for t in (z.q_global, z.k_global, z.v_global))
+            T = z.q_global.shape[0]
+            self._lay = orc.make_layout(T, T, True, 0, z.cu_seqlens)
+        q, k, v = self._f64
+        orc.dense_attention(q, k, v, z.scale, self._lay, rows=rows)
+        cu = z.cu_seqlens.astype(np.int64)
+        s = np.searchsorted(cu, rows, side="right") - 1
+        keys = rows - cu[s] + 1
+        return 4.0 * q.shape[2] * q.shape[1] * float(keys.sum())
+
+
+_DSA_INPUTS = {}
+
+
+def dsa_inputs(device):
+    """The DSA workload's inputs, drawn once per process (the attention and
+    the indexer workloads share them)."""
+    if device not in _DSA_INPUTS:
+        _DSA_INPUTS[device] = inputs.dsa_absorbed(device=device)
+    return _DSA_INPUTS[device]
+
+
+class DsaRunner(Runner):
     """DSA top-2048 sparse attention on absorbed-MLA shapes."""
 
     name = "dsa"
 
     def __init__(self, device):
-        self.w = w = inputs.dsa_absorbed(device=device)
+        self.w = w = dsa_inputs(device)
         self.q, self.kv = w.q.to(device), w.k.to(device)
-        self.v = self.kv[:, :, :512]
         self.idx = w.indices.to(device)
         Tq, Hq, Dqk = w.q.shape
         self.o = torch.empty((Tq, Hq, 512), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((Tq, Hq), dtype=torch.float32, device=device)
-        self.flops = 2.0 * Tq * Hq * w.topk * (Dqk + 512)
+        self.work = 2.0 * Tq * Hq * w.topk * (Dqk + 512)
         self.gathered_bytes = Tq * w.topk * Dqk * 2
-        self.launches_per_step = 1
-        self.bound = "tensor"
-        self.config = {"workload": "DSA top-2048 sparse, absorbed MLA: 4096 q x 32768 kv, "
-                                   "128 heads / 1 kv head, dqk 576, dv 512",
-                       "gathered_bytes": self.gathered_bytes}
+        self.n_rows = Tq
+        self.kernel = "cpattn_topk_sparse_fwd"
+        self.config = {"workload": "DSA top-2048 sparse, absorbed MLA: 4096 q (causal_offset 16384) "
+                                   "x 32768 kv, 128 heads / 1 kv head, dqk 576, dv 512 (v = first "
+                                   "512 channels of k), indices from the seeded indexer",
+                       "gathered_bytes": self.gathered_bytes, "l2": L2_NOTE}
 
-    def step(self):
+    def device_inputs(self):
+        return [self.q, self.kv, self.idx]
+
+    def step(self, q, kv, idx):
         from context_attention_softmax_gb300 import cpattn_topk_sparse_fwd
         w = self.w
-        cpattn_topk_sparse_fwd(self.q, self.kv, self.v, self.idx, block_size=1, scale=w.scale,
+        cpattn_topk_sparse_fwd(q, kv, kv[:, :, :512], idx, block_size=1, scale=w.scale,
                                causal_offset=w.causal_offset, out=self.o, lse=self.lse)
 
+    def outputs(self):
+        return [self.o, self.lse]
 
-class MobaRunner:
-    """MoBA gate + block-sparse attention (2+1 launches per step)."""
+    def extra_figures(self, seconds):
+        return {"gathered_gbs": self.gathered_bytes / seconds / 1e9,
+                "gathered_frac_of_hbm": self.gathered_bytes / seconds / 1e9 / hbm_peak()[0]}
+
+    def oracle_sample(self, rows):
+        import oracle as orc
+        w = self.w
+        if not hasattr(self, "_f64"):
+            self._f64 = (inputs.as_f64(w.q), inputs.as_f64(w.k))
+            self._lay = orc.make_layout(w.Tq, w.Tk, True, w.causal_offset)
+            self._idx = w.indices.numpy()
+        q, kv = self._f64
+        orc.sparse_attention(q, kv, kv[:, :, :512], w.scale, self._lay, self._idx, rows=rows)
+        n_keys = (self._idx[rows, 0, :] >= 0).sum()
+        return 2.0 * w.q.shape[1] * (w.q.shape[2] + 512) * float(n_keys)
+
+
+class MobaRunner(Runner):
+    """MoBA gate + block-sparse attention (gate, then the attention call)."""
 
     name = "moba"
+    unit = "GB/s"
+    scale = 1e9
+    bound = "hbm"
+    kernel = "moba step (cpattn_block_gate + cpattn_topk_sparse_fwd)"
+    launches_per_step = 8   # gate: means, split, tensor-core gate; attention: count, scan,
+    #                         scatter, attend, merge
 
     def __init__(self, device):
         self.w = w = inputs.moba()
@@ -231,67 +346,110 @@ class MobaRunner:
         qpos = w.causal_offset + np.arange(Tq)
         keys = 3 * B + (qpos % B) + 1
         self.flops = 4.0 * D * H * float(keys.sum())
-        self.hbm_bytes = (2 * w.k.numel() + 2 * w.q.numel() * 2 + w.v.numel() * 2 + self.o.numel() * 2)
-        self.launches_per_step = 7   # gate: 2; attention: count, scan, scatter, attend, merge
-        self.bound = "hbm"
+        kb, qb, vb, ob = (t.numel() * t.element_size() for t in (self.k, self.q, self.v, self.o))
+        selb, lseb = self.sel.numel() * 4, self.lse.numel() * 4
+        # gate: K, Q read, sel written; attention: Q, K, V, sel read, O, LSE written
+        self.work = float((kb + qb + selb) + (qb + kb + vb + selb + ob + lseb))
+        self.n_rows = Tq
         self.config = {"workload": "MoBA gate (top-3 + own of 512-key blocks) + block-sparse "
-                                   "attention: 8192 q x 65536 kv, 32 heads, d=128",
-                       "compulsory_bytes": self.hbm_bytes}
+                                   "attention: 8192 q (causal_offset 57344) x 65536 kv, 32 heads, "
+                                   "d=128",
+                       "compulsory_bytes": int(self.work),
+                       "compulsory_bytes_note": "gate reads K and Q and writes sel; attention "
+                                                "reads Q, K, V and sel and writes O and LSE "
+                                                "(K counted twice)",
+                       "attention_flops": self.flops, "l2": L2_NOTE}
 
-    def step(self):
+    def device_inputs(self):
+        return [self.q, self.k, self.v]
+
+    def step(self, q, k, v):
         from context_attention_softmax_gb300 import cpattn_block_gate, cpattn_topk_sparse_fwd
         w = self.w
-        cpattn_block_gate(self.q, self.k, w.block_size, w.topk, causal_offset=w.causal_offset,
+        cpattn_block_gate(q, k, w.block_size, w.topk, causal_offset=w.causal_offset,
                           sel=self.sel, workspace=self.ws)
-        cpattn_topk_sparse_fwd(self.q, self.k, self.v, self.sel, block_size=w.block_size,
-                               scale=w.scale, causal_offset=w.causal_offset, out=self.o,
-                               lse=self.lse, workspace=self.ws_sparse)
+        cpattn_topk_sparse_fwd(q, k, v, self.sel, block_size=w.block_size, scale=w.scale,
+                               causal_offset=w.causal_offset, out=self.o, lse=self.lse,
+                               workspace=self.ws_sparse)
+
+    def outputs(self):
+        return [self.o, self.lse, self.sel]
+
+    def extra_figures(self, seconds):
+        return {"attention_tflops": self.flops / seconds / 1e12}
+
+    def oracle_sample(self, rows):
+        import oracle as orc
+        w = self.w
+        if not hasattr(self, "_f64"):
+            self._f64 = (inputs.as_f64(w.q), inputs.as_f64(w.k), inputs.as_f64(w.v))
+            self._lay = orc.make_layout(w.Tq, w.Tk, True, w.causal_offset)
+        q, k, v = self._f64
+        sel = orc.moba_block_gate(q, k, self._lay.qpos, w.block_size, w.topk, rows=rows)
+        full = np.full((w.Tq,) + sel.shape[1:], -1, dtype=np.int32)
+        full[rows] = sel
+        orc.moba_attention(q, k, v, w.scale, self._lay, full, w.block_size, rows=rows)
+        return self.work * len(rows) / w.Tq
 
 
-class IndexerRunner:
+class IndexerRunner(Runner):
     """The DSA indexer: top-2048 keys of 4096 queries at offset 16384 over 32768
     keys, 4 fp32 indexer heads of 128 (the indices the DSA workload attends to)."""
 
     name = "dsa_indexer"
+    bound = "alu"
+    kernel = "cpattn_dsa_indexer (norms, scores, selection)"
+    launches_per_step = 3   # norms, scores, selection
 
     def __init__(self, device):
-        self.w = w = inputs.dsa_absorbed(device=device)
+        self.w = w = dsa_inputs(device)
         self.qI, self.kI, self.wt = (w.extra[k].to(device) for k in ("qI", "kI", "w"))
         Tq, H, D = self.qI.shape
         Tk = self.kI.shape[0]
         self.out = torch.empty((Tq, w.topk), dtype=torch.int32, device=device)
+        import ctypes
         from context_attention_softmax_gb300 import _lib, _args
         a = _args(self.qI, self.kI.unsqueeze(1), None, 1.0, True, w.causal_offset, None, None, None,
                   0, None, None)
         nbytes = _lib.load().cpattn_workspace_size(_lib.OP_DSA_INDEXER, ctypes.byref(a), w.topk, 1)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
         n_keys = np.minimum(w.causal_offset + np.arange(Tq) + 1, Tk)     # causal, one sequence
-        self.flops = 2.0 * float(n_keys.sum()) * H * D
-        self.launches_per_step = 3   # norms, scores, selection
-        self.bound = "alu"
+        self.work = 2.0 * float(n_keys.sum()) * H * D
+        self.n_rows = Tq
         self.config = {"workload": "DSA indexer top-2048: 4096 q (offset 16384) x 32768 keys, "
-                                   "4 fp32 indexer heads x 128, scores sum_h w_h relu(qI.kI)",
-                       "permitted_pairs": int(n_keys.sum())}
+                                   "4 fp32 indexer heads x 128, scores sum_h w_h relu(qI.kI), "
+                                   "selection exact against float64",
+                       "permitted_pairs": int(n_keys.sum()), "l2": L2_NOTE}
 
-    def step(self):
+    def device_inputs(self):
+        return [self.qI, self.kI, self.wt]
+
+    def step(self, qI, kI, wt):
         from context_attention_softmax_gb300 import cpattn_dsa_indexer
-        cpattn_dsa_indexer(self.qI, self.kI, self.wt, self.w.topk, causal_offset=self.w.causal_offset,
+        cpattn_dsa_indexer(qI, kI, wt, self.w.topk, causal_offset=self.w.causal_offset,
                            out=self.out, workspace=self.ws)
+
+    def outputs(self):
+        return [self.out]
 
     def oracle_sample(self, rows):
         import oracle as orc
         w = self.w
         if not hasattr(self, "_np"):
             self._np = tuple(w.extra[k].numpy() for k in ("qI", "kI", "w"))
-            self._lay = orc.make_layout(self._np[0].shape[0], self._np[1].shape[0], True, w.causal_offset)
+            self._lay = orc.make_layout(self._np[0].shape[0], self._np[1].shape[0], True,
+                                        w.causal_offset)
         qI, kI, wt = self._np
         orc.dsa_indexer_topk(qI, kI, wt, self._lay, w.topk, rows=rows)
         n_keys = np.minimum(w.causal_offset + np.asarray(rows) + 1, kI.shape[0])
         return 2.0 * float(n_keys.sum()) * qI.shape[1] * qI.shape[2]
 
 
-RUNNERS = {"dense_gqa": DenseRunner, "zigzag": ZigzagRunner, "dsa": DsaRunner, "moba": MobaRunner,
+RUNNERS = {"dense_gqa": DenseRunner,
+           "dense_gqa_4chunks": lambda dev: DenseRunner(dev, kv_chunks=True),
+           "zigzag": ZigzagRunner, "dsa": DsaRunner, "moba": MobaRunner,
            "dsa_indexer": IndexerRunner}
+ALL_ORDER = ["dense_gqa", "dense_gqa_4chunks", "zigzag", "dsa", "moba", "dsa_indexer"]
 
 
 # ---------------------------------------------------------------------------
@@ -306,6 +464,11 @@ def load_peaks():
         return p, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def hbm_peak():
+    p, src = load_peaks()
+    return float(p.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), src
 
 
 class ClockSampler:
@@ -387,15 +550,18 @@ def max_over_ranks(x, world):
 
 
 def time_steps(fn, steps, warmup, flush, world):
+    """Per-step device times (ms) of `steps` timed calls of fn, L2 flushed before each."""
     for _ in range(warmup):
         fn()
-    torch.cuda.synchronize()
-    barrier(world)
     stream = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     torch.cuda.synchronize()
     barrier(world)
+    # a backlog of flush writes (~0.6 ms of GPU work) so that the host has
+    # enqueued the first step before the GPU reaches it
+    for _ in range(16):
+        flush.zero_()
     for s in range(steps):
         flush.zero_()
         ev[s][0].record(stream)
@@ -405,10 +571,6 @@ def time_steps(fn, steps, warmup, flush, world):
     barrier(world)
     return [a.elapsed_time(b) for a, b in ev]
 
-
-# ---------------------------------------------------------------------------
-# arms
-# ---------------------------------------------------------------------------
 
 def host_info():
     """CPU model and the BLAS numpy was built against, for the oracle timings."""
@@ -431,24 +593,104 @@ def host_info():
     return {"cpu_model": model, "blas": blas}
 
 
-def cpu_baseline(runner, budget_s=12.0, batch=32):
+def cpu_baseline(runner, budget_s=8.0, batch=16):
     """Time the oracle as it stands on a bounded sample of query rows."""
     rng = np.random.default_rng(123)
-    n = runner.w.Tq
+    n = runner.n_rows
+    runner.oracle_sample(np.array([n - 1]))   # untimed: widens the inputs to float64 once
     t0 = time.perf_counter()
-    flops = 0.0
+    work = 0.0
     rows_done = 0
     while time.perf_counter() - t0 < budget_s:
-        rows = np.sort(rng.choice(n, size=batch, replace=False))
-        flops += runner.oracle_sample(rows)
-        rows_done += batch
+        rows = np.sort(rng.choice(n, size=min(batch, n), replace=False))
+        work += runner.oracle_sample(rows)
+        rows_done += len(rows)
     dt = time.perf_counter() - t0
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle", **host_info(),
-            "sample": f"{rows_done} query rows drawn at random ({rows_done / n:.1f}x the "
-                      f"{n}-row problem; all heads, all permitted keys), float64 numpy, "
-                      f"{dt:.1f} s"}
+    return {"value": work / dt / runner.scale, "unit": runner.unit,
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle", **host_info(),
+            "sample": f"{rows_done} query rows drawn at random out of {n} (all heads, every "
+                      f"permitted or selected key of each row), float64 numpy, {dt:.1f} s; "
+                      "value = the rows' share of the workload's work / time"}
 
+
+def roofline(runner, mean_ms, dev):
+    peaks, src = load_peaks()
+    sec = mean_ms * 1e-3
+    if runner.bound == "tensor":
+        achieved = runner.work / sec / 1e12
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "peak_source": f"{src} bf16 burst"}
+    elif runner.bound == "alu":
+        # fp32 FMA pipes: SMs x 128 lanes x 2 FLOP x the maximum SM clock
+        achieved = runner.work / sec / 1e12
+        sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = n_sm * 128 * 2 * sm_mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "peak_source": f"fp32 FMA: {n_sm} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz"}
+    else:
+        achieved = runner.work / sec / 1e9
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None, "peak_source": f"{src} copy"}
+    roof["kernel"] = runner.kernel
+    traffic, what = measured_traffic(runner.name)
+    if traffic is not None:
+        roof["traffic"] = traffic
+        roof["kernel"] = what
+        roof["traffic_note"] = "ncu dram bytes read + written per launch, see profiles/"
+    else:
+        roof["traffic_note"] = what
+    return roof
+
+
+def measure(runner, args, world, dev, flush, with_cpu):
+    """Timed steps, e2e steps and the oracle baseline of one workload."""
+    ins = runner.device_inputs()
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    times = time_steps(lambda: runner.step(*ins), args.steps, args.warmup, flush, world)
+    clk = clocks.stop()
+    mean_ms = max_over_ranks(statistics.mean(times), world)
+    rec = {
+        "value": world * runner.work / (mean_ms * 1e-3) / runner.scale, "unit": runner.unit,
+        "ms_per_step": mean_ms, "ms_min": min(times), "ms_median": statistics.median(times),
+        "ms_p90": float(np.percentile(times, 90)),
+        "config": runner.config, "roofline": roofline(runner, mean_ms, dev), "clocks": clk,
+        "gpu_launches": runner.launches_per_step * args.steps,
+    }
+    rec.update(runner.extra_figures(mean_ms * 1e-3))
+
+    # end to end through the public API: pinned host inputs in, outputs out
+    hin = [t.detach().to("cpu").pin_memory() for t in ins]
+    din = [torch.empty_like(t) for t in ins]
+    outs = runner.outputs()
+    hout = [torch.empty(t.shape, dtype=t.dtype, device="cpu").pin_memory() for t in outs]
+
+    def e2e_step():
+        for h, d in zip(hin, din):
+            d.copy_(h, non_blocking=True)
+        runner.step(*din)
+        for d, h in zip(outs, hout):
+            h.copy_(d, non_blocking=True)
+
+    et = time_steps(e2e_step, args.steps, max(args.warmup, 3), flush, world)
+    e_ms = max_over_ranks(statistics.mean(et), world)
+    rec["e2e"] = {"value": world * runner.work / (e_ms * 1e-3) / runner.scale, "unit": runner.unit,
+                  "ms_per_step": e_ms,
+                  "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hin)),
+                  "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hout))}
+    del hin, din, hout
+    if with_cpu:
+        rec["cpu_baseline"] = cpu_baseline(runner)
+    return rec
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
 
 def run_reference(args, world, rank):
     if rank != 0:
@@ -458,18 +700,19 @@ def run_reference(args, world, rank):
     per_step_rows = 16
     for _ in range(args.warmup):
         runner.oracle_sample(np.sort(rng.choice(runner.w.Tq, per_step_rows, replace=False)))
-    times, flops = [], []
+    times, work = [], []
     for _ in range(args.steps):
         rows = np.sort(rng.choice(runner.w.Tq, per_step_rows, replace=False))
         t0 = time.perf_counter()
-        flops.append(runner.oracle_sample(rows))
+        work.append(runner.oracle_sample(rows))
         times.append(time.perf_counter() - t0)
-    value = sum(flops) / sum(times) / 1e12
-    ms_full = runner.flops / (value * 1e12) * 1e3
+    value = sum(work) / sum(times) / 1e12
+    ms_full = runner.work / (value * 1e12) * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": value,
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * statistics.mean(times), "ms_full_problem_extrapolated": ms_full, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": 1e3 * statistics.mean(times), "ms_full_problem_extrapolated": ms_full,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded N(0,1)*0.5, bf16-rounded)",
         "config": runner.config,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle",
@@ -486,83 +729,34 @@ def run_ours(args, world, rank, local):
     from context_attention_softmax_gb300 import build as _build
     _build.build()
     dev = torch.device("cuda", local)
-    runner = RUNNERS[args.workload](dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    times = time_steps(runner.step, args.steps, args.warmup, flush, world)
-    clk = clocks.stop()
-    mean_ms = statistics.mean(times)
-    mean_ms = max_over_ranks(mean_ms, world)
-    value = world * runner.flops / (mean_ms * 1e-3) / 1e12
-
-    # end to end through the public API with pinned host buffers
-    e2e = None
-    if hasattr(runner, "host_inputs"):
-        hin, hout = runner.host_inputs(), runner.host_outputs()
-        din = [torch.empty_like(t, device=dev) for t in hin]
-        dout = runner.outputs()
-
-        def e2e_step():
-            for h, d in zip(hin, din):
-                d.copy_(h, non_blocking=True)
-            runner.step(*din)
-            for d, h in zip(dout, hout):
-                h.copy_(d, non_blocking=True)
-
-        et = time_steps(e2e_step, args.steps, max(args.warmup, 3), flush, world)
-        e_ms = max_over_ranks(statistics.mean(et), world)
-        e2e = {"value": world * runner.flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hin)),
-               "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hout))}
-
-    peaks, src = load_peaks()
-    if runner.bound == "tensor":
-        achieved = runner.flops / (mean_ms * 1e-3) / 1e12
-        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None, "peak_source": f"{src} bf16 burst"}
-    elif runner.bound == "alu":
-        # fp32 FMA pipes: SMs x 128 lanes x 2 FLOP x the maximum SM clock
-        achieved = runner.flops / (mean_ms * 1e-3) / 1e12
-        sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
-        n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-        peak = n_sm * 128 * 2 * sm_mhz * 1e6 / 1e12
-        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None,
-                "peak_source": f"fp32 FMA: {n_sm} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz"}
-    else:
-        achieved = runner.hbm_bytes / (mean_ms * 1e-3) / 1e9
-        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None, "peak_source": f"{src} copy"}
-    roof["kernel"] = {"moba": "moba step", "dsa_indexer": "dsa indexer (scores + selection)"}.get(
-        runner.name, "cpattn_chunk_fwd")
-    traffic, what = measured_traffic(runner.name)
-    if traffic is not None:
-        roof["traffic"] = traffic
-        roof["kernel"] = what
-        roof["traffic_note"] = "ncu dram bytes read + written per launch, see profiles/"
-    else:
-        roof["traffic_note"] = what
-
+    with_cpu = world == 1 and not args.no_cpu_baseline
+    names = ALL_ORDER if args.workload == "all" else [args.workload]
+    records = {}
+    for name in names:
+        runner = RUNNERS[name](dev)
+        records[name] = measure(runner, args, world, dev, flush, with_cpu)
+        del runner
+        torch.cuda.empty_cache()
     if rank != 0:
         return
+    head_name = names[0]
+    head = records.pop(head_name)
     line = {
         "metric": METRIC,
-        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": mean_ms,
-        "ms_min": min(times), "ms_median": statistics.median(times),
-        "ms_p90": float(np.percentile(times, 90)),
+        "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "ms_min": head["ms_min"], "ms_median": head["ms_median"], "ms_p90": head["ms_p90"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), bf16-rounded; no dataset)",
-        "config": runner.config, "roofline": roof, "clocks": clk,
-        "gpu_launches": runner.launches_per_step * args.steps,
-        "e2e": e2e,
+        "config": head["config"], "roofline": head["roofline"], "clocks": head["clocks"],
+        "gpu_launches": head["gpu_launches"] + sum(r["gpu_launches"] for r in records.values()),
+        "e2e": head["e2e"],
     }
-    if world == 1 and not args.no_cpu_baseline and hasattr(runner, "oracle_sample"):
-        line["cpu_baseline"] = cpu_baseline(runner)
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if records:
+        line["workloads"] = records
     print(json.dumps(line), flush=True)
 
 
@@ -570,17 +764,18 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: 2000 for our arm, so the clock sampler sees the "
-                         "timed region; 20 for the reference arm)")
-    ap.add_argument("--warmup", type=int, default=10)
+                    help="timed steps per workload (default: 100 for our arm, 20 for the "
+                         "reference arm)")
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(RUNNERS), default="dense_gqa")
+    ap.add_argument("--workload", choices=["all"] + sorted(RUNNERS), default="all",
+                    help="all (default): the headline plus one record per other workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.steps is None:
-        args.steps = 20 if args.impl == "reference" else 2000
+        args.steps = 20 if args.impl == "reference" else 100
     world, rank, local = dist_setup()
     try:
         if args.impl == "reference":

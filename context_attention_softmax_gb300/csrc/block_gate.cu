@@ -342,7 +342,7 @@ cudaError_t launch_gate_t(const cpattn_attn_args& a, int B, int topk, int32_t* s
   }
   const size_t smem = block_gate_smem(n_blocks, D);
   auto kern = gate_select_kernel<T>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Tq + kGQ - 1) / kGQ, a.Hq);
   kern<<<grid, kGThreads, smem, stream>>>(a, B, n_blocks, topk, mu64, mu32, sel);

@@ -1,6 +1,7 @@
 // cpattn_block_gate_static: the MoBA block gate with its scratch memory (the
-// per-block key means) held in a fixed array inside this library instead of
-// a caller-supplied workspace.
+// per-block key means and, for the tensor-core gate, their bf16 split terms)
+// held in a fixed array inside this library instead of a caller-supplied
+// workspace.
 //
 // Who needs it: callers that cannot allocate device memory at the point of
 // the call - code that runs while a caching allocator must not grow, inside
@@ -18,6 +19,11 @@
 // each other's block means.  Calls in stream order are safe.  Nothing in the
 // array needs to start at zero: each call overwrites every block mean it
 // reads.  No cudaMalloc, cudaFree or allocating library routine is called.
+//
+// A shape is accepted only when the whole workspace cpattn_block_gate would
+// ask for (cpattn_workspace_size(CPATTN_OP_BLOCK_GATE, ...)) fits the array,
+// so this entry always takes the same kernels as cpattn_block_gate given that
+// workspace; the MoBA shape of 128 blocks x 32 KV heads x d 128 needs 9.4 MB.
 #include <cstdio>
 #include <mutex>
 
@@ -27,7 +33,7 @@
 namespace cpattn {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_gate_scratch[kStaticScratchBytes];
@@ -62,11 +68,11 @@ extern "C" cpattn_status cpattn_block_gate_static(const cpattn_attn_args* args,
   if (args == nullptr || block_size < 1 || args->Tk < 0 || args->Hkv < 1 || args->Dqk < 1)
     // malformed arguments: the regular entry point rejects them with its message
     return cpattn_block_gate(args, block_size, topk, sel, nullptr, 0, stream);
-  const size_t need = block_gate_workspace_min(*args, block_size);
+  const size_t need = block_gate_workspace(*args, block_size);
   if (need > kStaticScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),
-             "cpattn_block_gate_static: the block means need %zu bytes of scratch, more than "
+             "cpattn_block_gate_static: the gate needs %zu bytes of scratch, more than "
              "its fixed %zu-byte array; use cpattn_block_gate with a workspace",
              need, kStaticScratchBytes);
     return report_error(CPATTN_ERR_UNSUPPORTED, msg);

@@ -518,8 +518,7 @@ cudaError_t launch_dense_tc(const cpattn_attn_args& a, cudaStream_t stream, bool
   p.fold = (p.head_pairs && a.causal && a.cu_seqlens == nullptr && a.q_chunk_map == nullptr &&
             a.kv_chunk_map == nullptr) ? 1 : 0;
   p.n_units = p.head_pairs ? p.n_qtiles * (a.Hq / 2) : ((p.n_qtiles + 1) / 2) * a.Hq;
-  cudaError_t e = cudaFuncSetAttribute(dense_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(dense_tc_kernel), (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   dense_tc_kernel<<<(unsigned)p.n_units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   *launched = true;

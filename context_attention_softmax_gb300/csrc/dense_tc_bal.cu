@@ -891,9 +891,7 @@ size_t dense_tc_bal_part_bytes(int grid) {
 }
 
 int dense_tc_grid() {
-  int dev = 0, n_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const int n_sm = device_sm_count();
   return n_sm > 0 ? n_sm : 1;
 }
 
@@ -941,8 +939,7 @@ cudaError_t launch_dense_tc_bal(const cpattn_attn_args& a, void* ws, size_t ws_b
   p.part = static_cast<float4*>(ws);
   p.pieces = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + dense_tc_bal_part_bytes(grid));
   p.tag = next_tag.fetch_add(1u);
-  cudaError_t e = cudaFuncSetAttribute(dense_tc_bal_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kBalSmemBytes);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(dense_tc_bal_kernel), (int)kBalSmemBytes);
   if (e != cudaSuccess) return e;
   dense_tc_bal_kernel<<<grid, kThreads, kBalSmemBytes, stream>>>(tq, tk, tv, p);
   *launched = true;

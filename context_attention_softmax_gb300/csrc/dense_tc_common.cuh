@@ -2,7 +2,6 @@
 // the (head, query tile) blocks of a work unit and the TMA descriptors.
 #pragma once
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <climits>
 
@@ -86,31 +85,13 @@ __device__ __forceinline__ Block folded_block_of(int Hq, int n_qtiles, int u, in
   return Block{2 * pr + X, (X ? n_qtiles - 1 - t : t) * BM};
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // [rows, heads, 128] bf16 with element strides (st_t, st_h); box = 64 x 1 x 128.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int64_t st_t,
               int64_t st_h) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)st_h * 2, (cuuint64_t)st_t * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)BM};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)heads, (uint64_t)rows};
+  const uint64_t strides[2] = {(uint64_t)st_h * 2, (uint64_t)st_t * 2};
+  const uint32_t box[3] = {64, 1, (uint32_t)BM};
+  return encode_bf16_3d(m, base, dims, strides, box);
 }
 
 }  // namespace

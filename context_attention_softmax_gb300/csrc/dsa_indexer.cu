@@ -463,9 +463,7 @@ size_t dsa_indexer_workspace(const cpattn_attn_args& a, int grid) {
 }
 
 int dsa_indexer_grid(const cpattn_attn_args& a) {
-  int dev = 0, n_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const int n_sm = device_sm_count();
   const int g = 2 * (n_sm > 0 ? n_sm : 1);
   return a.Tq < g ? (a.Tq > 0 ? a.Tq : 1) : g;
 }
@@ -509,7 +507,7 @@ cudaError_t launch_dsa_indexer(const cpattn_attn_args& a, const float* w, int to
   sp.words = (a.Tk + 31) / 32;
   const size_t smem = (size_t)sp.words * 2 * 4;
   if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(idx_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_smem_attr(reinterpret_cast<const void*>(idx_select_kernel), (int)smem);
     if (e != cudaSuccess) return e;
   }
   idx_select_kernel<<<grid, kSelThreads, smem, stream>>>(sp);

@@ -463,19 +463,6 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
   if (threadIdx.x == 0 && s.abort) report_status(a.dev_status, CPATTN_ERR_TIMEOUT);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    cudaDriverEntryPointQueryResult qr;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 }  // namespace
 
 bool dsa_tc_supported(const cpattn_attn_args& a, int32_t index_heads, int32_t block_size) {
@@ -491,28 +478,19 @@ bool dsa_tc_supported(const cpattn_attn_args& a, int32_t index_heads, int32_t bl
 cudaError_t launch_dsa_tc(const cpattn_attn_args& a, const int32_t* indices, int32_t topk,
                           cudaStream_t stream, bool* launched) {
   *launched = false;
-  auto fn = encode_fn();
-  if (fn == nullptr) return cudaSuccess;
   CUtensorMap tq;
-  cuuint64_t dims[3] = {(cuuint64_t)DQK, (cuuint64_t)HQ, (cuuint64_t)a.Tq};
-  cuuint64_t strides[2] = {(cuuint64_t)a.q_stride_h * 2, (cuuint64_t)a.q_stride_t * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)HQ, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.q), dims, strides, box, estr,
-         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaSuccess;
+  const uint64_t dims[3] = {(uint64_t)DQK, (uint64_t)HQ, (uint64_t)a.Tq};
+  const uint64_t strides[2] = {(uint64_t)a.q_stride_h * 2, (uint64_t)a.q_stride_t * 2};
+  const uint32_t box[3] = {64, (uint32_t)HQ, 1};
+  if (!encode_bf16_3d(&tq, a.q, dims, strides, box)) return cudaSuccess;
   DsaParams p;
   p.a = a;
   p.idx = indices;
   p.topk = topk;
   p.n_tiles = (topk + BNK - 1) / BNK;
   p.n_items = 2 * a.Tq;
-  int dev = 0, n_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t e = cudaFuncSetAttribute(dsa_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kDSmemBytes);
+  const int n_sm = device_sm_count();
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(dsa_attn_kernel), (int)kDSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < n_sm ? p.n_items : n_sm;
   dsa_attn_kernel<<<grid, kThreads, kDSmemBytes, stream>>>(tq, p);

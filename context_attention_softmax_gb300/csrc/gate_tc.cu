@@ -420,27 +420,12 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (threadIdx.x == 0 && s.abort) report_status(a.dev_status, CPATTN_ERR_TIMEOUT);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 gate_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    cudaDriverEntryPointQueryResult q;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 bool gate_map(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[3],
               const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
-  auto fn = gate_encode_fn();
-  if (fn == nullptr) return false;
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const uint64_t s[2] = {strides[0], strides[1]};
+  const uint32_t b[3] = {box[0], box[1], box[2]};
+  return encode_bf16_3d(m, base, d, s, b);
 }
 
 }  // namespace
@@ -490,11 +475,8 @@ cudaError_t launch_gate_tc(const cpattn_attn_args& a, int32_t block_size, int32_
   p.mu64 = mu64;
   p.mnorm = mnorm;
   p.sel = sel;
-  int dev = 0, n_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  e = cudaFuncSetAttribute(gate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kGateSmemBytes);
+  const int n_sm = device_sm_count();
+  e = ensure_smem_attr(reinterpret_cast<const void*>(gate_tc_kernel), (int)kGateSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < n_sm ? p.n_items : n_sm;
   gate_tc_kernel<<<grid, kGateThreads, kGateSmemBytes, stream>>>(tq, tmu, p);

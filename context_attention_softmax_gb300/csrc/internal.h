@@ -1,6 +1,7 @@
 // Host-side declarations shared by the API layer and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -23,6 +24,16 @@ struct SparseArgs {
 
 // Sets the calling thread's cpattn_last_error() message and returns s.
 cpattn_status report_error(cpattn_status s, const char* msg);
+
+// Host caches (host_cache.cu).  encode_bf16_3d: a 3-D bf16 TMA map with
+// 128-byte swizzle (dims innermost first, strides in bytes), reused while
+// the pointer, shape, strides and box repeat; false if it cannot be encoded.
+// ensure_smem_attr: sets a kernel's dynamic shared-memory limit once per
+// device.  device_sm_count: SMs of the current device.
+bool encode_bf16_3d(CUtensorMap* out, const void* base, const uint64_t (&dims)[3],
+                    const uint64_t (&strides)[2], const uint32_t (&box)[3]);
+cudaError_t ensure_smem_attr(const void* func, int bytes);
+int device_sm_count();
 
 // Launchers return the cudaError_t of the launch (no synchronisation).
 cudaError_t launch_rowwise(const cpattn_attn_args& a, KeyMode mode, const SparseArgs& sp,

@@ -592,31 +592,13 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   if (threadIdx.x == 0 && s.abort) report_status(a.dev_status, CPATTN_ERR_TIMEOUT);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    cudaDriverEntryPointQueryResult qr;
-    void* ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &qr) == cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 // [rows, heads, 128] bf16 with element strides; box = 64 x 1 x box_rows.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int64_t st_t,
               int64_t st_h, int box_rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)st_h * 2, (cuuint64_t)st_t * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)heads, (uint64_t)rows};
+  const uint64_t strides[2] = {(uint64_t)st_h * 2, (uint64_t)st_t * 2};
+  const uint32_t box[3] = {64, 1, (uint32_t)box_rows};
+  return encode_bf16_3d(m, base, dims, strides, box);
 }
 
 }  // namespace
@@ -672,11 +654,8 @@ cudaError_t launch_moba_tc(const cpattn_attn_args& a, const int32_t* sel, int32_
   p.n_units = w.n_units;
   p.part_o = w.part_o;
   p.part_lse = w.part_lse;
-  int dev = 0, n_sm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-  e = cudaFuncSetAttribute(moba_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kMSmemBytes);
+  const int n_sm = device_sm_count();
+  e = ensure_smem_attr(reinterpret_cast<const void*>(moba_attn_kernel), (int)kMSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = (int)(d.max_units < (int64_t)n_sm ? d.max_units : (int64_t)n_sm);
   moba_attn_kernel<<<grid, kThreads, kMSmemBytes, stream>>>(tk, tv, p);

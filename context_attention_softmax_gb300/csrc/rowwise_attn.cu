@@ -239,7 +239,7 @@ cudaError_t launch_t(const RowParams& p, cudaStream_t stream) {
   if (MODE != kDense && p.a.kv_chunk_map) smem += (size_t)p.a.n_kv_chunks * sizeof(int);
   auto kern = rowwise_attn_kernel<T, VPL, MODE, PARTIALS>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)smem);
     if (e != cudaSuccess) return e;
   }
   kern<<<(unsigned)blocks, kWarps * 32, smem, stream>>>(p);

@@ -31,8 +31,11 @@
  *     contiguous; strides are in ELEMENTS; base pointers and every stride
  *     times the element size must be multiples of 16 bytes.
  *   Memory: every pointer is a DEVICE pointer owned by the caller.  The
- *     library never allocates or frees device memory and keeps no state
- *     between calls (apart from a per-device cache of kernel attributes).
+ *     library never allocates or frees device memory.  Between calls it
+ *     keeps per-device caches of kernel attributes and TMA descriptors
+ *     (host memory, refreshed whenever a pointer, shape or stride changes)
+ *     and one piece of device state: the fixed scratch array of
+ *     cpattn_block_gate_static, shared by every call of that entry point.
  *   Execution: every call only enqueues work on `stream` (a cudaStream_t /
  *     CUstream handle; NULL = legacy default stream) and returns; nothing
  *     synchronises.
@@ -223,13 +226,15 @@ cpattn_status cpattn_block_gate(const cpattn_attn_args* args, int32_t block_size
  * Some callers cannot call cudaMalloc or grow a memory pool when they make
  * this call: a plugin handed only its input and output buffers, code running
  * inside a host callback, or a runtime that owns every allocation.  This
- * variant takes no workspace: the block means live in a fixed 8 MiB array
+ * variant takes no workspace: the block means live in a fixed 16 MiB array
  * compiled into the library, which every GPU that loads the library holds
  * until the process exits.  Arguments, output and selection are those of
- * cpattn_block_gate.  The call allocates nothing.
+ * cpattn_block_gate, and so are the kernels it runs (those that
+ * cpattn_block_gate runs with a workspace of cpattn_workspace_size bytes).
+ * The call allocates nothing.
  * Limits and behaviour:
  *   - shapes whose workspace (cpattn_workspace_size(CPATTN_OP_BLOCK_GATE,
- *     ...)) exceeds 8 MiB are rejected with CPATTN_ERR_UNSUPPORTED and a
+ *     ...)) exceeds 16 MiB are rejected with CPATTN_ERR_UNSUPPORTED and a
  *     message; nothing is launched;
  *   - the first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress) and caches it; make that

@@ -80,17 +80,27 @@ def test_dense_gqa_small(Tq, Tk, off, Hq, Hkv, kvc):
     assert_matches(o, lse, O, L, "bf16", "final")
 
 
-def test_dense_gqa_full_size_sampled():
+def test_dense_gqa_full_size_every_row():
+    """The headline workload in the bench's launch configuration: every row,
+    head and channel against the oracle; then the four-chunk summary form,
+    whose per-chunk summaries are checked on sampled rows and merged by
+    cpattn_lse_merge."""
     w = inputs.dense_gqa()
-    o, lse = _chunk(w)
-    rows = sample_rows(w.Tq, 48, edges=(1, 127, 128, 1023, 2047))
+    o, lse = _chunk(w, workspace=torch.empty(64 << 20, dtype=torch.uint8, device="cuda"))
     q, k, v = f64(w)
-    O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w), rows=rows)
-    assert_matches(o[rows.tolist()], lse[rows.tolist()], O, L, "bf16", "cfg full")
-    # the four-chunk summary form reaches the same result
+    O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w))
+    assert_matches(o, lse, O, L, "bf16", "cfg full")
     o4, l4, po, pl = _chunk(w, kv_chunk_len=w.kv_chunk_len)
     assert torch.isneginf(pl[3]).all()          # chunk 3 (keys 6144..) is fully masked
-    assert_matches(o4[rows.tolist()], l4[rows.tolist()], O, L, "bf16", "cfg 4 chunks")
+    assert_matches(o4, l4, O, L, "bf16", "cfg 4 chunks")
+    om, lm = cpattn_lse_merge(po, pl, out_dtype=torch.bfloat16)
+    assert_matches(om, lm, O, L, "bf16", "cfg 4 chunks merged")
+    rows = sample_rows(w.Tq, 64, edges=(1, 127, 128, 1023, 2047))
+    _, _, PO, PL = orc.summarised_attention(q, k, v, w.scale, layout_of(w), w.kv_chunk_len,
+                                            rows=rows)
+    for c in range(po.shape[0]):
+        assert_matches(po[c][rows.tolist()], pl[c][rows.tolist()], PO[c], PL[c], "bf16",
+                       f"cfg chunk {c}")
 
 
 @pytest.mark.parametrize("factor", [3.0, 8.0])
@@ -137,14 +147,14 @@ def test_empty_inputs():
 # packed THD varlen + zigzag
 # ---------------------------------------------------------------------------
 
-def _zigzag_check(z, rows_per_rank=None):
+def _zigzag_check(z, rows_per_rank=None, all_rows_ranks=()):
     qg, kg, vg = (inputs.as_f64(t) for t in (z.q_global, z.k_global, z.v_global))
     lay_full = orc.make_layout(qg.shape[0], qg.shape[0], True, 0, z.cu_seqlens)
     L = z.chunk_len
     for r in range(z.cp_size):
         w = z.rank_workload(r)
         o, lse = _chunk(w)
-        if rows_per_rank is None:
+        if rows_per_rank is None or r in all_rows_ranks:
             rows = np.arange(w.Tq)
         else:
             rows = sample_rows(w.Tq, rows_per_rank, seed=r, edges=(L - 1, L, 2 * L - 1))
@@ -192,9 +202,12 @@ def test_zigzag_schedules_agree():
     assert_matches(o2, l2, O, L, "bf16", "per unit")
 
 
-def test_zigzag_varlen_full_size_sampled():
+def test_zigzag_varlen_full_size():
+    """All 8 rank calls of the packed zigzag workload: every row of ranks 0
+    and 7 (the earliest and the latest chunk pairs), 64 sampled rows of the
+    others."""
     z = inputs.zigzag_varlen()
-    _zigzag_check(z, rows_per_rank=12)
+    _zigzag_check(z, rows_per_rank=64, all_rows_ranks=(0, 7))
 
 
 # ---------------------------------------------------------------------------
@@ -245,12 +258,78 @@ def test_dsa_tensor_core_small():
 
 
 def test_dsa_full_size_sampled():
+    """The DSA workload: rows 0..79 (their two items are the first items of
+    every persistent CTA, one CTA per SM) plus 200 random rows and the last."""
     w = inputs.dsa_absorbed(device="cuda")
     o, lse = _dsa_run(w)
-    rows = sample_rows(w.Tq, 10, edges=(4095,))
+    rows = np.union1d(np.arange(80), sample_rows(w.Tq, 200, edges=(4095,)))
+    assert len(rows) >= 256
     q, k, v = f64(w)
     O, L, _ = orc.sparse_attention(q, k, v, w.scale, layout_of(w), w.indices.numpy(), rows=rows)
     assert_matches(o[rows.tolist()], lse[rows.tolist()], O, L, "bf16", "dsa full")
+
+
+def _dsa_layout_case(seed, Tq, Tk, topk, qpos, cu=None):
+    """Absorbed-MLA inputs (128 heads, 576 / 512) whose indices are a mix:
+    rows chosen by the float64 indexer under the packed layout (within the
+    query's sequence) and rows chosen ignoring the packing (so they name keys
+    of other sequences, which the kernel must mask again)."""
+    rng = np.random.default_rng(seed)
+    q = inputs.to_device_dtype((rng.standard_normal((Tq, 128, 576))).astype(np.float32), "bf16")
+    kv = inputs.to_device_dtype((rng.standard_normal((Tk, 1, 576))).astype(np.float32), "bf16")
+    qI = rng.standard_normal((Tq, 2, 32))
+    kI = rng.standard_normal((Tk, 32))
+    wI = rng.uniform(0.0, 1.0, 2)
+    lay_seq = orc.Layout(np.asarray(qpos, np.int64), np.arange(Tk, dtype=np.int64),
+                         orc.sequence_index(qpos, cu), orc.sequence_index(np.arange(Tk), cu),
+                         True, cu)
+    lay_one = orc.Layout(np.asarray(qpos, np.int64), np.arange(Tk, dtype=np.int64),
+                         np.zeros(Tq, np.int64), np.zeros(Tk, np.int64), True, None)
+    packed = orc.dsa_indexer_topk(qI, kI, wI, lay_seq, topk)
+    crossing = orc.dsa_indexer_topk(qI, kI, wI, lay_one, topk)
+    idx = np.where((np.arange(Tq) % 2 == 0)[:, None, None], packed, crossing)
+    return q, kv, torch.from_numpy(idx.astype(np.int32))
+
+
+def test_dsa_tensor_core_packed_sequences():
+    """Packed THD sequences on the tensor-core DSA kernel: sequence ends fall
+    inside 64-key tiles and inside the index lists; odd rows name keys of
+    earlier sequences, which the kernel masks again; query rows past the last
+    sequence select nothing; rows just after a sequence start see one or two
+    keys."""
+    Tq, Tk, topk, off = 40, 2600, 300, 2300
+    cu = np.array([0, 1000, 2301, 2333, 2335], dtype=np.int32)
+    qpos = off + np.arange(Tq)
+    q, kv, idx = _dsa_layout_case(41, Tq, Tk, topk, qpos, cu)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qd, kd = q.cuda(), kv.cuda()
+    o, lse = cpattn_topk_sparse_fwd(qd, kd, kd[:, :, :512], idx, block_size=1,
+                                    scale=1 / np.sqrt(576), causal_offset=off,
+                                    cu_seqlens=torch.from_numpy(cu), dev_status=status)
+    lay = orc.make_layout(Tq, Tk, True, off, cu_seqlens=cu)
+    qf, kf = inputs.as_f64(q), inputs.as_f64(kv)
+    O, L, bad = orc.sparse_attention(qf, kf, kf[:, :, :512], 1 / np.sqrt(576), lay, idx.numpy())
+    assert bad == 0 and int(status.item()) == 0
+    assert np.isneginf(L[qpos >= 2335]).all() and np.isfinite(L[qpos < 2335]).any(axis=1).sum() > 20
+    assert_matches(o, lse, O, L, "bf16", "dsa tensor-core packed")
+
+
+def test_dsa_tensor_core_query_chunk_map():
+    """A zigzag query chunk map on the tensor-core DSA kernel: local rows
+    0..47 hold logical chunk 1 and rows 48..95 logical chunk 6 (chunks of
+    48); the indices were chosen for those logical positions."""
+    L, Tk, topk = 48, 340, 200
+    cmap = np.array([1, 6], dtype=np.int32)
+    qpos = np.concatenate([np.arange(c * L, (c + 1) * L) for c in cmap])
+    q, kv, idx = _dsa_layout_case(42, 2 * L, Tk, topk, qpos)
+    qd, kd = q.cuda(), kv.cuda()
+    o, lse = cpattn_topk_sparse_fwd(qd, kd, kd[:, :, :512], idx, block_size=1,
+                                    scale=1 / np.sqrt(576), q_chunk_map=torch.from_numpy(cmap),
+                                    chunk_len=L)
+    lay = orc.make_layout(2 * L, Tk, True, 0, q_chunk_map=cmap, chunk_len=L)
+    qf, kf = inputs.as_f64(q), inputs.as_f64(kv)
+    O, LS, _ = orc.sparse_attention(qf, kf, kf[:, :, :512], 1 / np.sqrt(576), lay, idx.numpy())
+    assert_matches(o, lse, O, LS, "bf16", "dsa tensor-core q chunk map")
 
 
 # ---------------------------------------------------------------------------
@@ -323,7 +402,7 @@ def test_moba_full_size():
     lay = layout_of(w)
     ref_sel = orc.moba_block_gate(q, k, lay.qpos, w.block_size, w.topk)
     np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)   # every (query, head), bit-exact
-    rows = sample_rows(w.Tq, 24, edges=(511, 512, 8191))
+    rows = sample_rows(w.Tq, 256, edges=(511, 512, 8191))
     O, L, _ = orc.sparse_attention(q, k, v, w.scale, lay, ref_sel, w.block_size, rows=rows)
     assert_matches(o[rows.tolist()], lse[rows.tolist()], O, L, "bf16", "moba full")
 
@@ -442,13 +521,13 @@ def test_dsa_indexer_ties_and_packed_sequences():
     assert (got.cpu().numpy() == [130, 150]).all()
 
 
-def test_dsa_indexer_full_size_sampled():
+def test_dsa_indexer_full_size_every_row():
     """The DSA workload's indexer (4096 queries at offset 16384 over 32768
-    keys, 4 heads of 128, k = 2048): sampled rows equal the float64 oracle."""
+    keys, 4 heads of 128, k = 2048): every row equals the float64 oracle's,
+    bit for bit."""
     w = inputs.dsa_absorbed()
     qI, kI, wt = w.extra["qI"], w.extra["kI"], w.extra["w"]
     got = cpattn_dsa_indexer(qI.cuda(), kI.cuda(), wt.cuda(), w.topk, causal_offset=w.causal_offset)
-    rows = sample_rows(qI.shape[0], 12, seed=3, edges=(1,))
     lay = orc.make_layout(qI.shape[0], kI.shape[0], True, w.causal_offset)
-    ref = orc.dsa_indexer_topk(qI.numpy(), kI.numpy(), wt.numpy(), lay, w.topk, rows=rows)[:, 0, :]
-    np.testing.assert_array_equal(got.cpu().numpy()[rows], ref)
+    ref = orc.dsa_indexer_topk(qI.numpy(), kI.numpy(), wt.numpy(), lay, w.topk)[:, 0, :]
+    np.testing.assert_array_equal(got.cpu().numpy(), ref)

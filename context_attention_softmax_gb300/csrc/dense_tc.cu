@@ -44,6 +44,16 @@
 // column bounds.  Tiles outside every row's interval are skipped by all
 // roles, so an all-masked chunk costs nothing and stays neutral.
 //
+// Per-KV-chunk summaries (kv_chunk_len > 0, a multiple of 128): the CHUNKS
+// instantiation closes the running summary whenever the next KV tile belongs
+// to another chunk of kv_chunk_len physical rows.  The softmax thread reads
+// z_c from TMEM (the PV that finished it completed before the next S), writes
+// the finalised (z_c / l_c, m_c + ln l_c) to partial_o / partial_lse, and
+// starts the next chunk from (m, l) = (-inf, 0) while the MMA issuer
+// overwrites O with that chunk's first PV.  Chunks a row never reaches are
+// written neutral (0, -inf).  The row's o / lse are the merge of its own
+// partials, read back at the end ("... merge softmax globally", para 3-4).
+//
 // Every wait is bounded (2 s).  On expiry the CTA raises an abort flag, all
 // roles stop, in-flight TMA and MMA work is drained with bounded waits, TMEM
 // is freed, and CPATTN_ERR_TIMEOUT is written to dev_status.
@@ -59,6 +69,8 @@ struct TcParams {
   int head_pairs;   // 1: blocks are two heads of a GQA group; 0: two query tiles
   int fold;         // 1: head pairs at query tiles t and n_qtiles-1-t
   int n_units;      // CTAs
+  int part_tiles;   // KV tiles per partial-summary chunk (CHUNKS)
+  int n_parts;      // partial summaries per row (CHUNKS)
 };
 
 struct Smem {
@@ -78,6 +90,36 @@ struct Smem {
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
 
+// Finalised summary of one chunk for this thread's row: z from the 128 O
+// columns at o_col (every lane of the warp loads; rows past Tq store nothing).
+__device__ __forceinline__ void write_partial(const cpattn_attn_args& a, int c, int64_t tok, int h,
+                                              uint32_t o_col, float l, float m2, bool from_tmem) {
+  const bool live = from_tmem && l > 0.f;
+  const float inv = live ? 1.f / l : 0.f;
+  const int64_t row = ((int64_t)c * a.Tq + tok) * a.Hq + h;
+  float* po = a.partial_o + row * HD;
+#pragma unroll
+  for (int c4 = 0; c4 < HD / 32; ++c4) {
+    uint32_t oo[32];
+    if (from_tmem) {
+      tmem_ld32_sync(o_col + c4 * 32, oo);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) oo[i] = 0u;
+    }
+    if (tok < a.Tq) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(po + c4 * 32 + i) =
+            make_float4(__uint_as_float(oo[i]) * inv, __uint_as_float(oo[i + 1]) * inv,
+                        __uint_as_float(oo[i + 2]) * inv, __uint_as_float(oo[i + 3]) * inv);
+    }
+  }
+  if (tok < a.Tq)
+    a.partial_lse[row] = live ? (m2 + log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+}
+
+template <bool CHUNKS>
 __global__ void __launch_bounds__(kThreads, 1)
 dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -257,6 +299,12 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t k_lo0 = desc_lo(smem_u32(s.k[0]), 16), k_lo1 = desc_lo(smem_u32(s.k[1]), 16);
       const uint32_t v_lo0 = desc_lo(smem_u32(s.v[0]), kHalf), v_lo1 = desc_lo(smem_u32(s.v[1]), kHalf);
       const int n = n_run;
+      // PV(j) overwrites O when tile j opens a partial-summary chunk
+      auto opens_chunk = [&](int j) {
+        if (j == 0) return true;
+        if (!CHUNKS) return false;
+        return s.live_kt[j] / p.part_tiles != s.live_kt[j - 1] / p.part_tiles;
+      };
       auto issue_s = [&](int j, int x) {   // S_x(j) = Q_x K_j^T
         umma8_ss_kmajor(tmem + kColS + x * BN, x ? q_lo1 : q_lo0, (j & 1) ? k_lo1 : k_lo0, idesc_qk);
         umma_commit(&s.s_full[x]);
@@ -264,7 +312,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       auto issue_pv = [&](int j, int x) {  // O_x += P_x(j) V_j
         const uint32_t d = tmem + kColO + x * HD, pa = tmem + kColS + x * BN;
         const uint32_t vb = (j & 1) ? v_lo1 : v_lo0;
-        if (j > 0) umma8_ts_mnmajor<1>(d, pa, vb, idesc_pv);
+        if (!opens_chunk(j)) umma8_ts_mnmajor<1>(d, pa, vb, idesc_pv);
         else umma8_ts_mnmajor<0>(d, pa, vb, idesc_pv);
       };
       bool ok = n > 0 && mbar_wait(&s.q_full, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
@@ -286,8 +334,12 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int u = jt - n_short, xb = (u & 1) ? Sb : Lb;
           if (!mbar_wait(&s.p_full[xb], (n_short + (u >> 1)) & 1, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          umma8_ts_mnmajor<1>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
-                              idesc_pv);
+          if (CHUNKS && opens_chunk(jt))
+            umma8_ts_mnmajor<0>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
+                                idesc_pv);
+          else
+            umma8_ts_mnmajor<1>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
+                                idesc_pv);
           umma_commit(&s.v_empty[st]);
           umma_commit(&s.pv_done);
           if (jt + 1 == n) umma_commit(&s.o_ready[Lb]);
@@ -345,6 +397,8 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float m2 = -CUDART_INF_F, l = 0.f;
     int jt = 0;
     bool ok = true;
+    const int64_t tok_row = (int64_t)blk[X].q0 + r;
+    int cur_c = 0;                       // CHUNKS: the chunk being summarised
     for (int i = 0; i < nx[X]; ++i) {
       const int kt = s.live_kt[i];
       const int64_t kbase = logical_pos(a.kv_chunk_map, a.chunk_len, (int64_t)kt * BN);
@@ -367,6 +421,25 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ok = __all_sync(kFullMask, mbar_wait(&s.s_full[xb], ph, abort_flag));
       if (!ok) break;
       tc_fence_after();
+      if constexpr (CHUNKS) {
+        const int c_tile = kt / p.part_tiles;
+        if (c_tile != cur_c || jt == 0) {
+          if (jt > 0) {
+            // PV(jt-1) closed chunk cur_c; in the tail S(jt) follows only PV(jt-2)
+            if (in_tail && i > n_short) {
+              ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (i - n_short - 1) & 1, abort_flag));
+              if (!ok) break;
+              tc_fence_after();
+            }
+            write_partial(a, cur_c, tok_row, blk[X].head, o_col, l, m2, true);
+            ++cur_c;
+          }
+          for (; cur_c < c_tile; ++cur_c)
+            write_partial(a, cur_c, tok_row, blk[X].head, o_col, 0.f, 0.f, false);
+          m2 = -CUDART_INF_F;
+          l = 0.f;
+        }
+      }
       float sv[BN];
       {
         uint32_t rr[BN];
@@ -450,9 +523,62 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ok = __all_sync(kFullMask, mbar_wait(&s.o_ready[X], 0, abort_flag));
       if (ok) tc_fence_after();
     }
-    // epilogue: O = z / l, LSE = m + ln l (natural log); no key -> (0, -inf)
-    const int64_t tok = (int64_t)blk[X].q0 + r;
+    const int64_t tok = tok_row;
     const int h = blk[X].head;
+    if constexpr (CHUNKS) {
+      // close the last chunk, write the unreached ones neutral, then merge
+      // this row's partials: L = max_c LSE_c, w_c = exp(LSE_c - L),
+      // O = sum_c w_c O_c / sum_c w_c, LSE = L + ln sum_c w_c
+      if (ok && jt > 0) {
+        write_partial(a, cur_c, tok, h, o_col, l, m2, true);
+        ++cur_c;
+      }
+      for (; cur_c < p.n_parts; ++cur_c) write_partial(a, cur_c, tok, h, o_col, 0.f, 0.f, false);
+      if (tok < a.Tq) {
+        const int64_t stride = (int64_t)a.Tq * a.Hq;
+        const int64_t row0 = tok * a.Hq + h;
+        float L = -CUDART_INF_F;
+        for (int c = 0; c < p.n_parts; ++c) L = fmaxf(L, a.partial_lse[row0 + c * stride]);
+        const bool any = L > -CUDART_INF_F;
+        float wsum = 0.f;
+        for (int c = 0; c < p.n_parts; ++c) {
+          const float lc = a.partial_lse[row0 + c * stride];
+          wsum += lc > -CUDART_INF_F ? exp2f((lc - L) * 1.4426950408889634f) : 0.f;
+        }
+        const float inv = any ? 1.f / wsum : 0.f;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + tok * a.o_stride_t + (int64_t)h * a.o_stride_h;
+        for (int c4 = 0; c4 < HD / 32; ++c4) {
+          float acc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+          for (int c = 0; c < p.n_parts; ++c) {
+            const float lc = a.partial_lse[row0 + c * stride];
+            if (!(lc > -CUDART_INF_F)) continue;
+            const float wc = exp2f((lc - L) * 1.4426950408889634f) * inv;
+            const float4* src = reinterpret_cast<const float4*>(a.partial_o + (row0 + c * stride) * HD + c4 * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 v4 = src[i];
+              acc[4 * i] += wc * v4.x;
+              acc[4 * i + 1] += wc * v4.y;
+              acc[4 * i + 2] += wc * v4.z;
+              acc[4 * i + 3] += wc * v4.w;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 val;
+            val.x = pack_bf16(acc[i + 0], acc[i + 1]);
+            val.y = pack_bf16(acc[i + 2], acc[i + 3]);
+            val.z = pack_bf16(acc[i + 4], acc[i + 5]);
+            val.w = pack_bf16(acc[i + 6], acc[i + 7]);
+            *reinterpret_cast<uint4*>(orow + c4 * 32 + i) = val;
+          }
+        }
+        if (a.lse != nullptr) a.lse[row0] = any ? L + logf(wsum) : -CUDART_INF_F;
+      }
+    } else {
+    // epilogue: O = z / l, LSE = m + ln l (natural log); no key -> (0, -inf)
     const bool live = ok && jt > 0 && l > 0.f;
     const float inv = live ? 1.f / l : 0.f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + tok * a.o_stride_t + (int64_t)h * a.o_stride_h;
@@ -479,6 +605,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if (tok < a.Tq && a.lse != nullptr)
       a.lse[tok * a.Hq + h] = live ? (m2 + log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+    }
   }
 
   tc_fence_before();
@@ -492,7 +619,10 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
 bool dense_tc_supported(const cpattn_attn_args& a) {
   if (a.dtype != CPATTN_BF16 || a.Dqk != HD || a.Dv != HD) return false;
-  if (a.kv_chunk_len != 0 || a.Tq <= 0 || a.Tk <= 0) return false;
+  if (a.Tq <= 0 || a.Tk <= 0) return false;
+  if (a.kv_chunk_len != 0 && (a.kv_chunk_len % BN != 0 || a.partial_o == nullptr ||
+                              a.partial_lse == nullptr))
+    return false;
   if (!(a.scale > 0.f)) return false;   // the row max is taken on unscaled scores
   if ((a.q_chunk_map || a.kv_chunk_map) && a.chunk_len % BN != 0) return false;
   if ((a.Tk + BN - 1) / BN > kMaxKTiles) return false;
@@ -518,9 +648,12 @@ cudaError_t launch_dense_tc(const cpattn_attn_args& a, cudaStream_t stream, bool
   p.fold = (p.head_pairs && a.causal && a.cu_seqlens == nullptr && a.q_chunk_map == nullptr &&
             a.kv_chunk_map == nullptr) ? 1 : 0;
   p.n_units = p.head_pairs ? p.n_qtiles * (a.Hq / 2) : ((p.n_qtiles + 1) / 2) * a.Hq;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(dense_tc_kernel), (int)kSmemBytes);
+  p.part_tiles = a.kv_chunk_len > 0 ? a.kv_chunk_len / BN : 1;
+  p.n_parts = a.kv_chunk_len > 0 ? (a.Tk + a.kv_chunk_len - 1) / a.kv_chunk_len : 1;
+  auto kern = a.kv_chunk_len > 0 ? dense_tc_kernel<true> : dense_tc_kernel<false>;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  dense_tc_kernel<<<(unsigned)p.n_units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  kern<<<(unsigned)p.n_units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
   *launched = true;
   return cudaGetLastError();
 }

@@ -904,7 +904,7 @@ int dense_units(const cpattn_attn_args& a, int* head_pairs) {
 }  // namespace
 
 size_t dense_tc_bal_workspace(const cpattn_attn_args& a) {
-  if (!dense_tc_supported(a)) return 0;
+  if (!dense_tc_supported(a) || a.kv_chunk_len != 0) return 0;   // no partial summaries here
   int hp = 0;
   const int nu = dense_units(a, &hp);
   if (nu > kMaxUnits) return 0;

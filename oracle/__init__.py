@@ -2,9 +2,12 @@
 
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline legs of
 ``bench.py`` may import this package.  It is independent of the CUDA library:
-neither imports the other.  See ``oracle/attention.py`` for the passages each
-function follows.
+neither imports the other.  See ``oracle/attention.py`` (attention, merge,
+gates, indexer) and ``oracle/mla.py`` (the MLA value up-projection and the
+K/V materialisation from latents) for the passages each function follows.
 """
+
+from . import mla  # noqa: F401
 
 from .attention import (  # noqa: F401
     NEG_INF,

@@ -18,6 +18,8 @@ end-to-end figure:
                      gathered GB/s)
   moba               MoBA gate + block-sparse attention (compulsory GB/s)
   dsa_indexer        the DSA indexer's exact top-2048 (fp32 TFLOP/s)
+  mla_v_up           absorbed-MLA value up-projection of the DSA output (GB/s)
+  mla_kv             MLA K/V materialisation from gathered latents (TFLOP/s)
 `--workload NAME` times one of them alone as the top-level record.
 
 Timing: W untimed warm-up steps, then exactly K timed steps; before each
@@ -445,11 +447,105 @@ class IndexerRunner(Runner):
         return 2.0 * float(n_keys.sum()) * qI.shape[1] * qI.shape[2]
 
 
+class MlaVUpRunner(Runner):
+    """Value up-projection after absorbed attention: [4096, 128, 512] latent
+    outputs x up_v_weight [128, 512, 128] (the DSA workload's shapes)."""
+
+    name = "mla_v_up"
+    unit = "GB/s"
+    scale = 1e9
+    bound = "hbm"
+    kernel = "mla_gemm_kernel (cpattn_mla_v_up)"
+
+    def __init__(self, device):
+        self.w = w = inputs.mla_v_up()
+        self.o, self.wt = w.o_latent.to(device), w.up_v_weight.to(device)
+        T, H, L = self.o.shape
+        V = self.wt.shape[2]
+        self.out = torch.empty((T, H, V), dtype=torch.bfloat16, device=device)
+        self.flops = 2.0 * T * H * L * V
+        self.work = float(self.o.numel() * 2 + self.wt.numel() * 2 + self.out.numel() * 2)
+        self.n_rows = T
+        self.config = {"workload": "absorbed-MLA value up-projection: o_latent [4096, 128, 512] "
+                                   "x up_v_weight [128, 512, 128] -> [4096, 128, 128], bf16 in, "
+                                   "fp32 accumulate",
+                       "compulsory_bytes": int(self.work), "flops": self.flops, "l2": L2_NOTE}
+
+    def device_inputs(self):
+        return [self.o, self.wt]
+
+    def step(self, o, wt):
+        from context_attention_softmax_gb300 import cpattn_mla_v_up
+        cpattn_mla_v_up(o, wt, out=self.out)
+
+    def outputs(self):
+        return [self.out]
+
+    def extra_figures(self, seconds):
+        return {"tflops": self.flops / seconds / 1e12}
+
+    def oracle_sample(self, rows):
+        from oracle import mla
+        if not hasattr(self, "_f64"):
+            self._f64 = (inputs.as_f64(self.w.o_latent), inputs.as_f64(self.w.up_v_weight))
+        o, wt = self._f64
+        mla.absorbed_v_up(o[rows], wt)
+        return self.work * len(rows) / self.n_rows
+
+
+class MlaKvRunner(Runner):
+    """K/V materialisation from gathered latents: 32768 tokens, latent 512,
+    128 heads x (128 key + 128 value) channels, shared rope key 64."""
+
+    name = "mla_kv"
+    kernel = "mla_gemm_kernel (cpattn_mla_kv_materialise)"
+
+    def __init__(self, device):
+        self.w = w = inputs.mla_kv()
+        self.c, self.ks, self.wb = (t.to(device) for t in (w.kv_c, w.k_shared, w.wkv_b))
+        T, L = self.c.shape
+        R = self.ks.shape[1]
+        self.k = torch.empty((T, w.H, w.N + R), dtype=torch.bfloat16, device=device)
+        self.v = torch.empty((T, w.H, w.V), dtype=torch.bfloat16, device=device)
+        self.work = 2.0 * T * L * w.H * (w.N + w.V)
+        self.bytes = float(sum(t.numel() * 2 for t in (self.c, self.ks, self.wb, self.k, self.v)))
+        self.n_rows = T
+        self.config = {"workload": "MLA K/V materialisation from gathered latents: kv_c [32768, 512] "
+                                   "x wkv_b^T [512, 128 x 256] -> K [32768, 128, 128 + 64] "
+                                   "(shared rope key appended), V [32768, 128, 128], bf16 in, "
+                                   "fp32 accumulate",
+                       "compulsory_bytes": int(self.bytes), "l2": L2_NOTE}
+
+    def device_inputs(self):
+        return [self.c, self.ks, self.wb]
+
+    def step(self, c, ks, wb):
+        from context_attention_softmax_gb300 import cpattn_mla_kv_materialise
+        w = self.w
+        cpattn_mla_kv_materialise(c, ks, wb, w.H, w.N, w.V, k_out=self.k, v_out=self.v)
+
+    def outputs(self):
+        return [self.k, self.v]
+
+    def extra_figures(self, seconds):
+        return {"gbs": self.bytes / seconds / 1e9}
+
+    def oracle_sample(self, rows):
+        from oracle import mla
+        w = self.w
+        if not hasattr(self, "_f64"):
+            self._f64 = tuple(inputs.as_f64(t) for t in (w.kv_c, w.k_shared, w.wkv_b))
+        c, ks, wb = self._f64
+        mla.materialise_kv(c[rows], ks[rows], wb, w.H, w.N, w.V)
+        return self.work * len(rows) / self.n_rows
+
+
 RUNNERS = {"dense_gqa": DenseRunner,
            "dense_gqa_4chunks": lambda dev: DenseRunner(dev, kv_chunks=True),
            "zigzag": ZigzagRunner, "dsa": DsaRunner, "moba": MobaRunner,
-           "dsa_indexer": IndexerRunner}
-ALL_ORDER = ["dense_gqa", "dense_gqa_4chunks", "zigzag", "dsa", "moba", "dsa_indexer"]
+           "dsa_indexer": IndexerRunner, "mla_v_up": MlaVUpRunner, "mla_kv": MlaKvRunner}
+ALL_ORDER = ["dense_gqa", "dense_gqa_4chunks", "zigzag", "dsa", "moba", "dsa_indexer", "mla_v_up",
+             "mla_kv"]
 
 
 # ---------------------------------------------------------------------------

@@ -18,7 +18,8 @@ from ._lib import CPATTN_BF16, CPATTN_FP32, CpattnError  # noqa: F401
 
 __all__ = [
     "cpattn_chunk_fwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd", "cpattn_block_gate",
-    "cpattn_dsa_indexer", "cpattn_workspace_size", "cpattn_version", "CpattnError",
+    "cpattn_dsa_indexer", "cpattn_mla_v_up", "cpattn_mla_kv_materialise",
+    "cpattn_workspace_size", "cpattn_version", "CpattnError",
 ]
 
 
@@ -209,3 +210,47 @@ def cpattn_workspace_size(op, q, k, v=None, topk=0, block_size=1):
 
 def cpattn_version():
     return _lib.load().cpattn_version()
+
+
+def cpattn_mla_v_up(o_latent, up_v_weight, out=None, dev_status=None, stream=None):
+    """Value up-projection after absorbed attention: out[t, h] = o_latent[t, h] @ W[h].
+
+    o_latent: bf16 [T, H, L] (last dim contiguous), up_v_weight: bf16 [H, L, V]
+    contiguous; returns bf16 [T, H, V].
+    """
+    _thd("o_latent", o_latent)
+    T, H, L = o_latent.shape
+    w = up_v_weight.contiguous()
+    V = w.shape[2]
+    if out is None:
+        out = torch.empty((T, H, V), dtype=torch.bfloat16, device=o_latent.device)
+    _thd("out", out)
+    _lib.check(_lib.load().cpattn_mla_v_up(o_latent.data_ptr(), o_latent.stride(0),
+                                           o_latent.stride(1), w.data_ptr(), T, H, L, V,
+                                           out.data_ptr(), out.stride(0), out.stride(1),
+                                           _ptr(dev_status), 0, _stream(stream)))
+    return out
+
+
+def cpattn_mla_kv_materialise(kv_c, k_shared, wkv_b, H, N, V, k_out=None, v_out=None,
+                              dev_status=None, stream=None):
+    """Per-head K [T, H, N + R] and V [T, H, V] (bf16) from gathered latents.
+
+    kv_c: bf16 [T, L], k_shared: bf16 [T, R], wkv_b: bf16 [H * (N + V), L]
+    (a linear layer's weight, contiguous).
+    """
+    T, L = kv_c.shape
+    R = k_shared.shape[1]
+    wb = wkv_b.contiguous()
+    dev = kv_c.device
+    if k_out is None:
+        k_out = torch.empty((T, H, N + R), dtype=torch.bfloat16, device=dev)
+    if v_out is None:
+        v_out = torch.empty((T, H, V), dtype=torch.bfloat16, device=dev)
+    _thd("k_out", k_out)
+    _thd("v_out", v_out)
+    _lib.check(_lib.load().cpattn_mla_kv_materialise(
+        kv_c.data_ptr(), kv_c.stride(0), k_shared.data_ptr(), k_shared.stride(0), wb.data_ptr(),
+        T, L, H, N, R, V, k_out.data_ptr(), k_out.stride(0), k_out.stride(1), v_out.data_ptr(),
+        v_out.stride(0), v_out.stride(1), _ptr(dev_status), 0, _stream(stream)))
+    return k_out, v_out

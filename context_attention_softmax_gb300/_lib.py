@@ -34,6 +34,8 @@ EXPORTS = (
     "cpattn_block_gate",
     "cpattn_block_gate_static",
     "cpattn_dsa_indexer",
+    "cpattn_mla_v_up",
+    "cpattn_mla_kv_materialise",
     "cpattn_workspace_size",
     "cpattn_last_error",
     "cpattn_version",
@@ -64,6 +66,7 @@ class AttnArgs(ctypes.Structure):
         ("kv_chunk_len", c_i32),
         ("partial_o", c_p), ("partial_lse", c_p),
         ("dev_status", c_p),
+        ("wait_limit_ns", c_i64),
     ]
 
 
@@ -88,10 +91,16 @@ def load(path: str = LIB_PATH):
     lib.cpattn_block_gate.argtypes = [P, c_i32, c_i32, c_p, c_p, ctypes.c_size_t, c_p]
     lib.cpattn_block_gate_static.argtypes = [P, c_i32, c_i32, c_p, c_p]
     lib.cpattn_dsa_indexer.argtypes = [P, c_p, c_i32, c_p, c_p, ctypes.c_size_t, c_p]
+    lib.cpattn_mla_v_up.argtypes = [c_p, c_i64, c_i64, c_p, c_i32, c_i32, c_i32, c_i32, c_p, c_i64,
+                                    c_i64, c_p, c_i64, c_p]
+    lib.cpattn_mla_kv_materialise.argtypes = [c_p, c_i64, c_p, c_i64, c_p, c_i32, c_i32, c_i32,
+                                              c_i32, c_i32, c_i32, c_p, c_i64, c_i64, c_p, c_i64,
+                                              c_i64, c_p, c_i64, c_p]
     lib.cpattn_workspace_size.argtypes = [c_i32, P, c_i32, c_i32]
     lib.cpattn_workspace_size.restype = ctypes.c_size_t
     for name in ("cpattn_chunk_fwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd",
-                 "cpattn_block_gate", "cpattn_block_gate_static", "cpattn_dsa_indexer"):
+                 "cpattn_block_gate", "cpattn_block_gate_static", "cpattn_dsa_indexer",
+                 "cpattn_mla_v_up", "cpattn_mla_kv_materialise"):
         getattr(lib, name).restype = c_i32
     lib.cpattn_last_error.argtypes = []
     lib.cpattn_last_error.restype = ctypes.c_char_p

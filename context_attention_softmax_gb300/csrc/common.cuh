@@ -101,6 +101,11 @@ __device__ __forceinline__ double warp_sum_f64(double x) {
   return x;
 }
 
+// Limit of every bounded wait of a call: wait_limit_ns, or 2 s when 0.
+__device__ __forceinline__ uint64_t wait_limit(const cpattn_attn_args& a) {
+  return a.wait_limit_ns > 0 ? (uint64_t)a.wait_limit_ns : 2000000000ull;
+}
+
 // First device-side error wins; the caller zeroes the word before the call.
 __device__ __forceinline__ void report_status(int32_t* status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);

@@ -227,6 +227,54 @@ cpattn_status cpattn_dsa_indexer(const cpattn_attn_args* a, const float* w, int3
                      "cpattn_dsa_indexer launch");
 }
 
+cpattn_status cpattn_mla_v_up(const void* o_latent, int64_t o_stride_t, int64_t o_stride_h,
+                              const void* up_v_weight, int32_t T, int32_t H, int32_t L, int32_t V,
+                              void* out, int64_t out_stride_t, int64_t out_stride_h,
+                              int32_t* dev_status, int64_t wait_limit_ns, void* stream) {
+  CHECK(T >= 0 && H >= 1, CPATTN_ERR_INVALID_ARG, "T=%d must be >= 0 and H=%d >= 1", T, H);
+  CHECK(L >= 64 && L % 64 == 0, CPATTN_ERR_UNSUPPORTED, "L=%d must be a positive multiple of 64", L);
+  CHECK(V >= 128 && V % 128 == 0, CPATTN_ERR_UNSUPPORTED, "V=%d must be a positive multiple of 128", V);
+  CHECK(wait_limit_ns >= 0, CPATTN_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
+  if (T == 0) return ok();
+  TRY(check_tensor("o_latent", o_latent, o_stride_t, o_stride_h, T, 2));
+  TRY(check_tensor("out", out, out_stride_t, out_stride_h, T, 2));
+  CHECK(up_v_weight != nullptr && aligned16(up_v_weight), CPATTN_ERR_INVALID_ARG,
+        "up_v_weight is NULL or not 16-byte aligned");
+  const cpattn_status st = mla_v_up_impl(o_latent, o_stride_t, o_stride_h, up_v_weight, T, H, L, V,
+                                         out, out_stride_t, out_stride_h, dev_status, wait_limit_ns,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  return st == CPATTN_OK ? ok() : st;
+}
+
+cpattn_status cpattn_mla_kv_materialise(const void* kv_c, int64_t c_stride_t, const void* k_shared,
+                                        int64_t ks_stride_t, const void* wkv_b, int32_t T, int32_t L,
+                                        int32_t H, int32_t N, int32_t R, int32_t V, void* k_out,
+                                        int64_t k_stride_t, int64_t k_stride_h, void* v_out,
+                                        int64_t v_stride_t, int64_t v_stride_h, int32_t* dev_status,
+                                        int64_t wait_limit_ns, void* stream) {
+  CHECK(T >= 0 && H >= 1, CPATTN_ERR_INVALID_ARG, "T=%d must be >= 0 and H=%d >= 1", T, H);
+  CHECK(L >= 64 && L % 64 == 0, CPATTN_ERR_UNSUPPORTED, "L=%d must be a positive multiple of 64", L);
+  CHECK(N >= 128 && N % 128 == 0 && V >= 128 && V % 128 == 0, CPATTN_ERR_UNSUPPORTED,
+        "N=%d and V=%d must be positive multiples of 128", N, V);
+  CHECK(R >= 0 && R % 8 == 0, CPATTN_ERR_UNSUPPORTED, "R=%d must be a multiple of 8", R);
+  CHECK(wait_limit_ns >= 0, CPATTN_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
+  CHECK((int64_t)H * (N + V) <= (int64_t)1 << 30, CPATTN_ERR_UNSUPPORTED, "H*(N+V) too large");
+  if (T == 0) return ok();
+  CHECK(kv_c != nullptr && aligned16(kv_c) && c_stride_t >= L && c_stride_t % 8 == 0,
+        CPATTN_ERR_INVALID_ARG, "kv_c must be 16-byte aligned with a row stride >= L, a multiple of 8");
+  CHECK(wkv_b != nullptr && aligned16(wkv_b), CPATTN_ERR_INVALID_ARG, "wkv_b is NULL or not 16-byte aligned");
+  if (R > 0)
+    CHECK(k_shared != nullptr && aligned16(k_shared) && ks_stride_t >= R && ks_stride_t % 8 == 0,
+          CPATTN_ERR_INVALID_ARG, "k_shared must be 16-byte aligned with a row stride >= R, a multiple of 8");
+  TRY(check_tensor("k_out", k_out, k_stride_t, k_stride_h, T, 2));
+  TRY(check_tensor("v_out", v_out, v_stride_t, v_stride_h, T, 2));
+  const cpattn_status st = mla_kv_impl(kv_c, c_stride_t, k_shared, ks_stride_t, wkv_b, T, L, H, N,
+                                       R, V, k_out, k_stride_t, k_stride_h, v_out, v_stride_t,
+                                       v_stride_h, dev_status, wait_limit_ns,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return st == CPATTN_OK ? ok() : st;
+}
+
 size_t cpattn_workspace_size(int32_t op, const cpattn_attn_args* a, int32_t topk, int32_t block_size) {
   if (a == nullptr) return 0;
   if (op == CPATTN_OP_BLOCK_GATE) return block_size > 0 ? block_gate_workspace(*a, block_size) : 0;

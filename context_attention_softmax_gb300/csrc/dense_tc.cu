@@ -134,6 +134,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       p.fold ? folded_block_of(a.Hq, p.n_qtiles, u, 1) : block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 1)};
   const int g = blk[0].head / (a.Hq / a.Hkv);
   volatile int* abort_flag = &s.abort;
+  const uint64_t lim = wait_limit(a);
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
@@ -263,18 +264,18 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         const int jt = k_issued, st = jt % NS;
         const uint32_t ph = (jt / NS) & 1;
-        if (!mbar_wait(&s.k_empty[st], ph ^ 1, abort_flag)) break;
+        if (!mbar_wait(&s.k_empty[st], ph ^ 1, abort_flag, lim)) break;
         mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
         tma_load_3d(s.k[st], &tm_k, &s.k_full[st], 0, g, kt * BN);
         tma_load_3d(s.k[st] + kHalf, &tm_k, &s.k_full[st], 64, g, kt * BN);
         ++k_issued;
-        if (!mbar_wait(&s.v_empty[st], ph ^ 1, abort_flag)) break;
+        if (!mbar_wait(&s.v_empty[st], ph ^ 1, abort_flag, lim)) break;
         mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
         tma_load_3d(s.v[st], &tm_v, &s.v_full[st], 0, g, kt * BN);
         tma_load_3d(s.v[st] + kHalf, &tm_v, &s.v_full[st], 64, g, kt * BN);
         ++v_issued;
       }
-      if (*abort_flag) {  // let every copy in flight land before the CTA exits
+      if (*abort_flag, lim) {  // let every copy in flight land before the CTA exits
         int no_abort = 0;
         if (q_issued) mbar_wait(&s.q_full, 0, &no_abort, 200000000ull);
         for (int j = max(0, k_issued - NS); j < k_issued; ++j)
@@ -315,7 +316,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!opens_chunk(j)) umma8_ts_mnmajor<1>(d, pa, vb, idesc_pv);
         else umma8_ts_mnmajor<0>(d, pa, vb, idesc_pv);
       };
-      bool ok = n > 0 && mbar_wait(&s.q_full, 0, abort_flag) && mbar_wait(&s.k_full[0], 0, abort_flag);
+      bool ok = n > 0 && mbar_wait(&s.q_full, 0, abort_flag, lim) && mbar_wait(&s.k_full[0], 0, abort_flag, lim);
       if (ok) {
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
@@ -328,11 +329,11 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t q_lo_l = Lb ? q_lo1 : q_lo0;
       for (int jt = 0; jt < n && ok; ++jt) {
         const int st = jt & 1, st1 = (jt + 1) & 1;
-        if (!mbar_wait(&s.v_full[st], (jt >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&s.v_full[st], (jt >> 1) & 1, abort_flag, lim)) { ok = false; break; }
         if (tail2 && jt >= n_short) {
           // tail step: PV(jt) from the buffer holding P(jt), then S(jt+2) into it
           const int u = jt - n_short, xb = (u & 1) ? Sb : Lb;
-          if (!mbar_wait(&s.p_full[xb], (n_short + (u >> 1)) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.p_full[xb], (n_short + (u >> 1)) & 1, abort_flag, lim)) { ok = false; break; }
           tc_fence_after();
           if (CHUNKS && opens_chunk(jt))
             umma8_ts_mnmajor<0>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
@@ -344,7 +345,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           umma_commit(&s.pv_done);
           if (jt + 1 == n) umma_commit(&s.o_ready[Lb]);
           if (jt + 2 < n) {
-            if (!mbar_wait(&s.k_full[st], ((jt + 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&s.k_full[st], ((jt + 2) >> 1) & 1, abort_flag, lim)) { ok = false; break; }
             tc_fence_after();
             umma8_ss_kmajor(tmem + kColS + xb * BN, q_lo_l, st ? k_lo1 : k_lo0, idesc_qk);
             umma_commit(&s.s_full[xb]);
@@ -355,7 +356,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         bool k_ready = false;
         for (int x = 0; x < 2 && ok; ++x) {
           if (jt >= nx[x]) continue;
-          if (!mbar_wait(&s.p_full[x], jt & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.p_full[x], jt & 1, abort_flag, lim)) { ok = false; break; }
           tc_fence_after();
           issue_pv(jt, x);
           if (x == 1 || jt >= nx[1]) umma_commit(&s.v_empty[st]);
@@ -363,7 +364,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             umma_commit(&s.o_ready[x]);
           } else {
             if (!k_ready) {
-              if (!mbar_wait(&s.k_full[st1], ((jt + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+              if (!mbar_wait(&s.k_full[st1], ((jt + 1) >> 1) & 1, abort_flag, lim)) { ok = false; break; }
               tc_fence_after();
               k_ready = true;
             }
@@ -374,7 +375,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (ok && tail2 && jt + 1 == n_short && n_short + 1 < n) {
           // first tail tile's successor: S(n_short+1) into Sb's columns, which
           // PV_Sb(n_short-1), issued before it, has finished reading
-          if (!mbar_wait(&s.k_full[st], ((n_short + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.k_full[st], ((n_short + 1) >> 1) & 1, abort_flag, lim)) { ok = false; break; }
           tc_fence_after();
           umma8_ss_kmajor(tmem + kColS + Sb * BN, q_lo_l, st ? k_lo1 : k_lo0, idesc_qk);
           umma_commit(&s.s_full[Sb]);
@@ -418,7 +419,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ph = (n_short + (u >> 1)) & 1;
       }
       const uint32_t sb_col = s_col + (uint32_t)((xb - X) * BN);
-      ok = __all_sync(kFullMask, mbar_wait(&s.s_full[xb], ph, abort_flag));
+      ok = __all_sync(kFullMask, mbar_wait(&s.s_full[xb], ph, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();
       if constexpr (CHUNKS) {
@@ -427,7 +428,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (jt > 0) {
             // PV(jt-1) closed chunk cur_c; in the tail S(jt) follows only PV(jt-2)
             if (in_tail && i > n_short) {
-              ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (i - n_short - 1) & 1, abort_flag));
+              ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (i - n_short - 1) & 1, abort_flag, lim));
               if (!ok) break;
               tc_fence_after();
             }
@@ -501,7 +502,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // (jt - n_short)-th tail PV, unless jt is the first tail tile.
       if (__any_sync(kFullMask, rescale)) {
         if (in_tail && i > n_short) {
-          ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (i - n_short - 1) & 1, abort_flag));
+          ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (i - n_short - 1) & 1, abort_flag, lim));
           if (!ok) break;
           tc_fence_after();
         }
@@ -520,7 +521,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ++jt;
     }
     if (ok && jt > 0) {
-      ok = __all_sync(kFullMask, mbar_wait(&s.o_ready[X], 0, abort_flag));
+      ok = __all_sync(kFullMask, mbar_wait(&s.o_ready[X], 0, abort_flag, lim));
       if (ok) tc_fence_after();
     }
     const int64_t tok = tok_row;

@@ -445,6 +445,7 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int G = gridDim.x, g = blockIdx.x, nu = p.n_units;
   const int group = a.Hq / a.Hkv;
   volatile int* abort_flag = &s.abort;
+  const uint64_t lim = wait_limit(a);
 
   if (threadIdx.x == 0) {
     mbar_init(&s.q_full, 1);
@@ -537,7 +538,7 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const Block b1 = block_of(a.Hq, p.head_pairs, p.n_qtiles, pw.u, 1);
         const int kvh = b0.head / group;
         // Q of this unit once the previous piece's S MMAs are done with Q
-        if (!mbar_wait(&s.q_empty, (pc & 1) ^ 1, abort_flag)) break;
+        if (!mbar_wait(&s.q_empty, (pc & 1) ^ 1, abort_flag, lim)) break;
         mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
         tma_load_3d(s.q[0], &tm_q, &s.q_full, 0, b0.head, b0.q0);
         tma_load_3d(s.q[0] + kHalf, &tm_q, &s.q_full, 64, b0.head, b0.q0);
@@ -554,12 +555,12 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           lt.next(kt, kb);
           const int st = gj % NS;
           const uint32_t ph = (gj / NS) & 1;
-          if (!mbar_wait(&s.k_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.k_empty[st], ph ^ 1, abort_flag, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
           tma_load_3d(s.k[st], &tm_k, &s.k_full[st], 0, kvh, kt * BN);
           tma_load_3d(s.k[st] + kHalf, &tm_k, &s.k_full[st], 64, kvh, kt * BN);
           ++k_issued;
-          if (!mbar_wait(&s.v_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.v_empty[st], ph ^ 1, abort_flag, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
           tma_load_3d(s.v[st], &tm_v, &s.v_full[st], 0, kvh, kt * BN);
           tma_load_3d(s.v[st] + kHalf, &tm_v, &s.v_full[st], 64, kvh, kt * BN);
@@ -567,7 +568,7 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           ++gj;
         }
       }
-      if (*abort_flag) {  // let every copy in flight land before the CTA exits
+      if (*abort_flag, lim) {  // let every copy in flight land before the CTA exits
         int no_abort = 0;
         if (pc > 0) mbar_wait(&s.q_full, (pc - 1) & 1, &no_abort, 200000000ull);
         for (int j = max(0, k_issued - NS); j < k_issued; ++j)
@@ -602,8 +603,8 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       PieceWalk pw{s.pref, nu, S0, S1, 0, 0, 0};
       while (ok && pw.next()) {
         const int n = pw.t1 - pw.t0;
-        if (!mbar_wait(&s.q_full, pc & 1, abort_flag) ||
-            !mbar_wait(&s.k_full[gj % NS], (gj / NS) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&s.q_full, pc & 1, abort_flag, lim) ||
+            !mbar_wait(&s.k_full[gj % NS], (gj / NS) & 1, abort_flag, lim)) { ok = false; break; }
         tc_fence_after();
         issue_s(gj, 0);
         issue_s(gj, 1);
@@ -613,9 +614,9 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           const int j = gj + jt, st = j % NS, st1 = (j + 1) % NS;
           const bool more = jt + 1 < n;
           // block A: PV_A(j), then S_A(j+1)
-          if (!mbar_wait(&s.v_full[st], (j / NS) & 1, abort_flag) ||
-              !mbar_wait(&s.p_full[0], j & 1, abort_flag) ||
-              (jt == 0 && pc > 0 && !mbar_wait(&s.o_free[0], (pc - 1) & 1, abort_flag))) {
+          if (!mbar_wait(&s.v_full[st], (j / NS) & 1, abort_flag, lim) ||
+              !mbar_wait(&s.p_full[0], j & 1, abort_flag, lim) ||
+              (jt == 0 && pc > 0 && !mbar_wait(&s.o_free[0], (pc - 1) & 1, abort_flag, lim))) {
             ok = false;
             break;
           }
@@ -623,13 +624,13 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           issue_pv(j, 0, jt == 0);
           if (!more) umma_commit(&s.o_ready[0]);
           if (more) {
-            if (!mbar_wait(&s.k_full[st1], ((j + 1) / NS) & 1, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(&s.k_full[st1], ((j + 1) / NS) & 1, abort_flag, lim)) { ok = false; break; }
             tc_fence_after();
             issue_s(j + 1, 0);
           }
           // block B: PV_B(j), then S_B(j+1)
-          if (!mbar_wait(&s.p_full[1], j & 1, abort_flag) ||
-              (jt == 0 && pc > 0 && !mbar_wait(&s.o_free[1], (pc - 1) & 1, abort_flag))) {
+          if (!mbar_wait(&s.p_full[1], j & 1, abort_flag, lim) ||
+              (jt == 0 && pc > 0 && !mbar_wait(&s.o_free[1], (pc - 1) & 1, abort_flag, lim))) {
             ok = false;
             break;
           }
@@ -701,7 +702,7 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           lo_c = (int)max((int64_t)0, min((int64_t)BN, iv.lo - kbase));
           hi_c = (int)max((int64_t)-1, min((int64_t)kvalid - 1, iv.hi - kbase));
         }
-        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[X], jt & 1, abort_flag));
+        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[X], jt & 1, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
         float sv[BN];
@@ -776,7 +777,7 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_arrive(&s.p_full[X]);
         ++jt;
       }
-      ok = ok && __all_sync(kFullMask, mbar_wait(&s.o_ready[X], pc & 1, abort_flag));
+      ok = ok && __all_sync(kFullMask, mbar_wait(&s.o_ready[X], pc & 1, abort_flag, lim));
       if (ok) tc_fence_after();
       const int cnt_u = s.pref[u + 1] - s.pref[u];
       const bool whole = pw.t0 == 0 && pw.t1 == cnt_u;

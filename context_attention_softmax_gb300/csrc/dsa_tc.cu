@@ -105,6 +105,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
   const cpattn_attn_args& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &s.abort;
+  const uint64_t lim = wait_limit(a);
 
   if (threadIdx.x == 0) {
     mbar_init(&s.qs_full, 1);
@@ -145,7 +146,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
       bool ok = true;
       for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++ui) {
         const int i = it >> 1;
-        if (!mbar_wait(&s.qs_empty, (ui & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&s.qs_empty, (ui & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
         mbar_arrive_expect_tx(&s.qs_full, kQS * kQChunkBytes);
         for (int c = 0; c < kQS; ++c)
           tma_load_3d(s.qs[c], &tm_q, &s.qs_full, 64 * (kQT + c), 0, i);
@@ -179,7 +180,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         const int st = gj % NS;
         const uint32_t ph = ((gj / NS) & 1) ^ 1;
         const uint32_t stage = smem_u32(s.kv[st]);
-        ok = __all_sync(kFullMask, mbar_wait(&empty[st], ph, abort_flag));
+        ok = __all_sync(kFullMask, mbar_wait(&empty[st], ph, abort_flag, lim));
         if (!ok) break;
         // The tile's 64 indices, two per lane; masked slots fetch row 0.
         int64_t e2[2];
@@ -236,8 +237,8 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
       int prev = -1, prev_first = 0, prev_last = 0, prev_ui = 0, prev_c = 0;
       auto issue_pv = [&]() -> bool {
         const int g = prev;
-        if (!mbar_wait(&s.p_full[g & 1], (g >> 1) & 1, abort_flag)) return false;
-        if (prev_first && prev_ui > 0 && !mbar_wait(&s.o_free, (prev_ui - 1) & 1, abort_flag))
+        if (!mbar_wait(&s.p_full[g & 1], (g >> 1) & 1, abort_flag, lim)) return false;
+        if (prev_first && prev_ui > 0 && !mbar_wait(&s.o_free, (prev_ui - 1) & 1, abort_flag, lim))
           return false;
         tc_fence_after();
         // value channels [256c, 256c + 256) = chunks 4c..4c+3 of the key rows
@@ -258,12 +259,12 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
           if (!issue_pv()) { ok = false; break; }
           prev = -1;
         }
-        if (!mbar_wait(&s.qt_full, ui & 1, abort_flag) ||
-            !mbar_wait(&s.qs_full, ui & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&s.qt_full, ui & 1, abort_flag, lim) ||
+            !mbar_wait(&s.qs_full, ui & 1, abort_flag, lim)) { ok = false; break; }
         for (int j = 0; j < T; ++j, ++gj) {
           const int st = gj % NS;
           const uint32_t ph = (gj / NS) & 1;
-          if (!mbar_wait(&s.ka_full[st], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.ka_full[st], ph, abort_flag, lim)) { ok = false; break; }
           fence_proxy_async_smem();   // the gathered rows were written by cp.async
           tc_fence_after();
           const uint32_t d = tmem + kColS + (gj & 1) * BNK;
@@ -288,7 +289,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
           // its value chunks are released as early as possible.
           if (prev >= 0 && !issue_pv()) { ok = false; break; }
           prev = -1;
-          if (!mbar_wait(&s.kb_full[st], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.kb_full[st], ph, abort_flag, lim)) { ok = false; break; }
           fence_proxy_async_smem();
           tc_fence_after();
           if (hc == 0) {
@@ -357,7 +358,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
           m0 = __ballot_sync(kFullMask, e0 >= 0 && e0 < a.Tk && e0 >= iv.lo && e0 <= iv.hi);
           m1 = __ballot_sync(kFullMask, e1 >= 0 && e1 < a.Tk && e1 >= iv.lo && e1 <= iv.hi);
         }
-        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[gj & 1], (gj >> 1) & 1, abort_flag));
+        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[gj & 1], (gj >> 1) & 1, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
         const uint32_t s_col = tmem + lane_base + kColS + (gj & 1) * BNK;
@@ -409,7 +410,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         f2_unpack(f2_add(rs2[0], rs2[1]), a0, a1);
         l = l * alpha + (a0 + a1);
         if (__any_sync(kFullMask, rescale)) {
-          ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (gj - 1) & 1, abort_flag));
+          ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (gj - 1) & 1, abort_flag, lim));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
@@ -427,7 +428,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         mbar_arrive(&s.p_full[gj & 1]);
       }
       if (!ok) break;
-      ok = __all_sync(kFullMask, mbar_wait(&s.o_full, ui & 1, abort_flag));
+      ok = __all_sync(kFullMask, mbar_wait(&s.o_full, ui & 1, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();
       // epilogue: O[i, r, 256c ...] = z / l; LSE = m + ln l (half 0 writes it)

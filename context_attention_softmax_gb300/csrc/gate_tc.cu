@@ -157,6 +157,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int i0 = (int)((int64_t)blockIdx.x * p.n_items / gridDim.x);
   const int i1 = (int)((int64_t)(blockIdx.x + 1) * p.n_items / gridDim.x);
   volatile int* abort_flag = &s.abort;
+  const uint64_t lim = wait_limit(a);
 
   if (threadIdx.x == 0) {
     mbar_init(&s.mu_full, 1);
@@ -193,7 +194,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int h = it / p.n_qtiles, qt = it - h * p.n_qtiles, g = h / group;
         if (g != cur_g) {
           // the previous group's means stay until every MMA reading them is done
-          if (n_mu > 0 && !mbar_wait(&s.mu_empty, (n_mu - 1) & 1, abort_flag)) break;
+          if (n_mu > 0 && !mbar_wait(&s.mu_empty, (n_mu - 1) & 1, abort_flag, lim)) break;
           mbar_arrive_expect_tx(&s.mu_full, mu_bytes);
           for (int t = 0; t < 3; ++t)
             for (int kb = 0; kb < 2; ++kb)
@@ -202,12 +203,12 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           ++n_mu;
         }
         const int st = ti & 1;
-        if (!mbar_wait(&s.q_empty[st], ((ti >> 1) & 1) ^ 1, abort_flag)) break;
+        if (!mbar_wait(&s.q_empty[st], ((ti >> 1) & 1) ^ 1, abort_flag, lim)) break;
         mbar_arrive_expect_tx(&s.q_full[st], 2 * kQBox);
         tma_load_3d(s.q[st][0], &tm_q, &s.q_full[st], 0, h, qt * GM);
         tma_load_3d(s.q[st][1], &tm_q, &s.q_full[st], 64, h, qt * GM);
       }
-      if (*abort_flag) {   // let copies in flight land before the CTA exits
+      if (*abort_flag, lim) {   // let copies in flight land before the CTA exits
         int no_abort = 0;
         if (n_mu > 0) mbar_wait(&s.mu_full, (n_mu - 1) & 1, &no_abort, 200000000ull);
         for (int j = max(0, ti - 2); j < ti; ++j)
@@ -228,13 +229,13 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int it = i0; it < i1 && ok; ++it, ++ti) {
         const int h = it / p.n_qtiles, g = h / group;
         if (g != cur_g) {
-          if (!mbar_wait(&s.mu_full, n_mu & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.mu_full, n_mu & 1, abort_flag, lim)) { ok = false; break; }
           cur_g = g;
           ++n_mu;
         }
         const int st = ti & 1;
-        if (!mbar_wait(&s.q_full[st], (ti >> 1) & 1, abort_flag) ||
-            !mbar_wait(&s.acc_free[st], ((ti >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&s.q_full[st], (ti >> 1) & 1, abort_flag, lim) ||
+            !mbar_wait(&s.acc_free[st], ((ti >> 1) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(st * 128);
         // K = 3 x 128: the same query tile against each mean term
@@ -273,7 +274,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         cur_g = g;
       }
       const int st = ti & 1;
-      ok = ok && __all_sync(kFullMask, mbar_wait(&s.acc_full[st], (ti >> 1) & 1, abort_flag));
+      ok = ok && __all_sync(kFullMask, mbar_wait(&s.acc_full[st], (ti >> 1) & 1, abort_flag, lim));
       const int64_t qi = (int64_t)qt * GM + r;
       const bool valid = ok && qi < a.Tq;
       const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.q) +

@@ -92,6 +92,17 @@ cudaError_t launch_gate_tc(const cpattn_attn_args& a, int32_t block_size, int32_
                            const double* mu64, const float* mu32, void* parts, cudaStream_t stream,
                            bool* launched);
 size_t block_gate_smem(int n_blocks, int D);
+// MLA projections on the tensor cores (mla_gemm.cu); arguments validated by
+// the caller.
+cpattn_status mla_v_up_impl(const void* o_latent, int64_t o_st, int64_t o_sh,
+                            const void* up_v_weight, int32_t T, int32_t H, int32_t L, int32_t V,
+                            void* out, int64_t out_st, int64_t out_sh, int32_t* dev_status,
+                            int64_t wait_limit_ns, cudaStream_t stream);
+cpattn_status mla_kv_impl(const void* kv_c, int64_t c_st, const void* k_shared, int64_t ks_st,
+                          const void* wkv_b, int32_t T, int32_t L, int32_t H, int32_t N, int32_t R,
+                          int32_t V, void* k_out, int64_t k_st, int64_t k_sh, void* v_out,
+                          int64_t v_st, int64_t v_sh, int32_t* dev_status, int64_t wait_limit_ns,
+                          cudaStream_t stream);
 cudaError_t launch_block_gate(const cpattn_attn_args& a, int32_t block_size, int32_t topk,
                               int32_t* sel, void* workspace, size_t workspace_bytes,
                               cudaStream_t stream);

@@ -1,0 +1,348 @@
+// The MLA projections around the CP-chunk attention, as one persistent
+// tcgen05 GEMM kernel (bf16 x bf16 -> fp32 in tensor memory -> bf16):
+//
+//  * value up-projection after absorbed attention ("[1/2] Enable DSA CP, THD
+//    with absorbed MLA - #3674", sequence diagram and Background):
+//      out[t, h, :] = o_latent[t, h, :] @ up_v_weight[h]      (per head)
+//    a batch of H GEMMs, M = tokens, N = V, K = L; up_v_weight[h] is [L, V]
+//    with V contiguous, read as an MN-major B operand;
+//  * local K/V materialisation from gathered latents ("[BC][MLA][CP] Optimize
+//    MLA all-gather and Ulysses communication for Kimi K3 and dpskV3",
+//    "K/V all-gather CP"):
+//      kv = kv_c @ wkv_b^T, viewed [T, H, N + V];  k = [k_nope | k_shared],
+//    one GEMM, M = tokens, N = H * (N + V), K = L; wkv_b is a linear layer's
+//    weight [H * (N + V), L], read as a K-major B operand.  The epilogue sends
+//    each 128-column tile to the key or the value of its head and appends
+//    the head-shared key to every head's key row.
+//
+// Tiles of 128 x 128 outputs, K in steps of 64 (one 128-byte swizzled box of
+// bf16 per operand), six stages of 32 KiB.  Roles (256 threads): warp 0 TMA
+// producer, warp 1 MMA issuer and TMEM owner (two 128-column accumulators,
+// so the epilogue of one tile overlaps the main loop of the next), warps 4-7
+// epilogue (TMEM lane = output row).  Persistent CTAs take tiles in a fixed
+// stride; consecutive tiles share their A rows (materialisation) or their
+// head's weight (up-projection), so those reads come from L2.
+//
+// Every wait is bounded (wait_limit_ns, 2 s by default); on expiry the CTA
+// drains its copies and MMAs in flight, frees TMEM and reports
+// CPATTN_ERR_TIMEOUT in dev_status.
+#include "common.cuh"
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace cpattn {
+namespace {
+
+using namespace sm100;
+
+constexpr int GM = 128, GN = 128, GK = 64;
+constexpr int kStages = 6;
+constexpr int kGemmThreads = 256;
+constexpr uint32_t kABytes = GM * GK * 2;   // 16 KiB
+constexpr uint32_t kBBytes = GN * GK * 2;   // 16 KiB
+constexpr uint32_t kBHalf = GK * 64 * 2;    // MN-major B: 64 K-rows x 64 N-columns, 8 KiB
+
+enum { kModeVUp = 0, kModeKv = 1 };
+
+struct GemmParams {
+  int mode;
+  int M;              // output rows (tokens)
+  int m_tiles, n_tiles, batches, k_steps;
+  int n_total_tiles;  // m_tiles * n_tiles * batches
+  __nv_bfloat16* out; int64_t out_st, out_sh;       // up-projection [T, H, V]
+  __nv_bfloat16* k_out; int64_t k_st, k_sh;         // materialised key [T, H, N + R]
+  __nv_bfloat16* v_out; int64_t v_st, v_sh;         // materialised value [T, H, V]
+  const __nv_bfloat16* k_shared; int64_t ks_st;     // [T, R]
+  int N, V, R;
+  int32_t* dev_status;
+  uint64_t limit;
+};
+
+struct GemmSmem {
+  uint8_t a[kStages][kABytes];
+  uint8_t b[kStages][kBBytes];
+  uint64_t full[kStages], empty[kStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kGemmSmemBytes = sizeof(GemmSmem) + 1024;
+
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& b, int& mt, int& nt) {
+  const int per_b = p.m_tiles * p.n_tiles;
+  b = tile / per_b;
+  const int rem = tile - b * per_b;
+  mt = rem / p.n_tiles;
+  nt = rem - mt * p.n_tiles;
+}
+
+// One stage: four MMAs of K = 16.  A K-major (32 B per step); B K-major
+// (32 B per step) or MN-major (16 K-rows = 2 KiB per step).
+template <int B_MN>
+__device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                          bool acc_first) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    umma_ss_lo(d, a_lo + 2 * k, b_lo + (B_MN ? 128 * k : 2 * k), idesc, (k > 0 || acc_first) ? 1u : 0u);
+}
+
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  tmem_ld32(taddr, r);
+  tmem_wait_ld();
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+
+template <int B_MN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  GemmSmem& s = *reinterpret_cast<GemmSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &s.abort;
+  const uint64_t lim = p.limit;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.acc_full[i], 1);
+      mbar_init(&s.acc_empty[i], 128);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int it = 0;   // stage fills issued
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.n_total_tiles && ok; tile += gridDim.x) {
+        int b, mt, nt;
+        tile_coords(p, tile, b, mt, nt);
+        for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
+          const int st = it % kStages;
+          if (!mbar_wait(&s.empty[st], ((it / kStages) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.full[st], kABytes + kBBytes);
+          if (p.mode == kModeVUp) {
+            tma_load_3d(s.a[st], &tm_a, &s.full[st], ks * GK, b, mt * GM);
+            tma_load_3d(s.b[st], &tm_b, &s.full[st], nt * GN, ks * GK, b);
+            tma_load_3d(s.b[st] + kBHalf, &tm_b, &s.full[st], nt * GN + 64, ks * GK, b);
+          } else {
+            tma_load_3d(s.a[st], &tm_a, &s.full[st], ks * GK, 0, mt * GM);
+            tma_load_3d(s.b[st], &tm_b, &s.full[st], ks * GK, nt * GN, 0);
+          }
+        }
+      }
+      if (!ok || *abort_flag) {   // let the copies in flight land before the CTA exits
+        // fill j was issued only after fill j - kStages had been consumed, so
+        // at most the last kStages fills can still be in flight
+        int no_abort = 0;
+        for (int j = max(0, it - kStages); j < it; ++j)
+          mbar_wait(&s.full[j % kStages], (j / kStages) & 1, &no_abort, 200000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(GM, GN, 0, B_MN);
+      int it = 0, ti = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.n_total_tiles && ok; tile += gridDim.x, ++ti) {
+        const int buf = ti & 1;
+        if (!mbar_wait(&s.acc_empty[buf], ((ti >> 1) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * GN);
+        for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
+          const int st = it % kStages;
+          if (!mbar_wait(&s.full[st], (it / kStages) & 1, abort_flag, lim)) { ok = false; break; }
+          tc_fence_after();
+          mma_stage<B_MN>(d, desc_lo(smem_u32(s.a[st]), 16),
+                          desc_lo(smem_u32(s.b[st]), B_MN ? kBHalf : 16), idesc, ks > 0);
+          umma_commit(&s.empty[st]);
+        }
+        if (ok) umma_commit(&s.acc_full[buf]);
+      }
+      umma_commit(&s.drain);
+      int no_abort = 0;
+      mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int r = (warp - 4) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    int ti = 0;
+    for (int tile = blockIdx.x; tile < p.n_total_tiles; tile += gridDim.x, ++ti) {
+      const int buf = ti & 1;
+      const bool ok = __all_sync(kFullMask, mbar_wait(&s.acc_full[buf], (ti >> 1) & 1, abort_flag, lim));
+      if (!ok) break;
+      tc_fence_after();
+      int b, mt, nt;
+      tile_coords(p, tile, b, mt, nt);
+      const int64_t t = (int64_t)mt * GM + r;
+      __nv_bfloat16* dst;
+      bool rope = false;
+      int h = b;
+      if (p.mode == kModeVUp) {
+        dst = p.out + t * p.out_st + (int64_t)b * p.out_sh + nt * GN;
+      } else {
+        const int col = nt * GN, per_head = p.N + p.V;
+        h = col / per_head;
+        const int part = col - h * per_head;
+        if (part < p.N) {
+          dst = p.k_out + t * p.k_st + (int64_t)h * p.k_sh + part;
+          rope = part + GN == p.N;
+        } else {
+          dst = p.v_out + t * p.v_st + (int64_t)h * p.v_sh + (part - p.N);
+        }
+      }
+#pragma unroll
+      for (int c4 = 0; c4 < GN / 32; ++c4) {
+        uint32_t acc[32];
+        tmem_ld32_wait(tmem + lane_base + (uint32_t)(buf * GN + c4 * 32), acc);
+        if (t < p.M) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 val;
+            val.x = pack2_bf16(__uint_as_float(acc[i + 0]), __uint_as_float(acc[i + 1]));
+            val.y = pack2_bf16(__uint_as_float(acc[i + 2]), __uint_as_float(acc[i + 3]));
+            val.z = pack2_bf16(__uint_as_float(acc[i + 4]), __uint_as_float(acc[i + 5]));
+            val.w = pack2_bf16(__uint_as_float(acc[i + 6]), __uint_as_float(acc[i + 7]));
+            *reinterpret_cast<uint4*>(dst + c4 * 32 + i) = val;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty[buf]);
+      if (rope && t < p.M) {   // the head-shared key after this head's last key tile
+        const uint4* src = reinterpret_cast<const uint4*>(p.k_shared + t * p.ks_st);
+        uint4* kd = reinterpret_cast<uint4*>(p.k_out + t * p.k_st + (int64_t)h * p.k_sh + p.N);
+        for (int i = 0; i < p.R / 8; ++i) kd[i] = __ldg(src + i);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (threadIdx.x == 0 && s.abort) report_status(p.dev_status, CPATTN_ERR_TIMEOUT);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                        bool b_mn, cudaStream_t stream) {
+  const void* kern = b_mn ? reinterpret_cast<const void*>(mla_gemm_kernel<1>)
+                          : reinterpret_cast<const void*>(mla_gemm_kernel<0>);
+  cudaError_t e = ensure_smem_attr(kern, (int)kGemmSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_sm = device_sm_count();
+  const int grid = p.n_total_tiles < n_sm ? p.n_total_tiles : n_sm;
+  if (b_mn)
+    mla_gemm_kernel<1><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, p);
+  else
+    mla_gemm_kernel<0><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cpattn_status mla_v_up_impl(const void* o_latent, int64_t o_st, int64_t o_sh,
+                            const void* up_v_weight, int32_t T, int32_t H, int32_t L, int32_t V,
+                            void* out, int64_t out_st, int64_t out_sh, int32_t* dev_status,
+                            int64_t wait_limit_ns, cudaStream_t stream) {
+  if (T == 0) return CPATTN_OK;
+  CUtensorMap ta, tb;
+  const uint64_t ad[3] = {(uint64_t)L, (uint64_t)H, (uint64_t)T};
+  const uint64_t as[2] = {(uint64_t)o_sh * 2, (uint64_t)o_st * 2};
+  const uint32_t ab[3] = {GK, 1, GM};
+  const uint64_t bd[3] = {(uint64_t)V, (uint64_t)L, (uint64_t)H};
+  const uint64_t bs[2] = {(uint64_t)V * 2, (uint64_t)L * V * 2};
+  const uint32_t bb[3] = {64, GK, 1};
+  if (!encode_bf16_3d(&ta, o_latent, ad, as, ab) || !encode_bf16_3d(&tb, up_v_weight, bd, bs, bb))
+    return report_error(CPATTN_ERR_INVALID_ARG, "cpattn_mla_v_up: a TMA descriptor cannot describe the operands");
+  GemmParams p{};
+  p.mode = kModeVUp;
+  p.M = T;
+  p.m_tiles = (T + GM - 1) / GM;
+  p.n_tiles = V / GN;
+  p.batches = H;
+  p.k_steps = L / GK;
+  p.n_total_tiles = p.m_tiles * p.n_tiles * p.batches;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out_st = out_st;
+  p.out_sh = out_sh;
+  p.dev_status = dev_status;
+  p.limit = wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : 2000000000ull;
+  const cudaError_t e = launch_gemm(p, ta, tb, true, stream);
+  if (e != cudaSuccess) return report_error(CPATTN_ERR_CUDA, cudaGetErrorString(e));
+  return CPATTN_OK;
+}
+
+cpattn_status mla_kv_impl(const void* kv_c, int64_t c_st, const void* k_shared, int64_t ks_st,
+                          const void* wkv_b, int32_t T, int32_t L, int32_t H, int32_t N, int32_t R,
+                          int32_t V, void* k_out, int64_t k_st, int64_t k_sh, void* v_out,
+                          int64_t v_st, int64_t v_sh, int32_t* dev_status, int64_t wait_limit_ns,
+                          cudaStream_t stream) {
+  if (T == 0) return CPATTN_OK;
+  CUtensorMap ta, tb;
+  const int64_t n_rows = (int64_t)H * (N + V);
+  const uint64_t ad[3] = {(uint64_t)L, 1, (uint64_t)T};
+  const uint64_t as[2] = {(uint64_t)c_st * 2, (uint64_t)c_st * 2};
+  const uint32_t ab[3] = {GK, 1, GM};
+  const uint64_t bd[3] = {(uint64_t)L, (uint64_t)n_rows, 1};
+  const uint64_t bs[2] = {(uint64_t)L * 2, (uint64_t)n_rows * L * 2};
+  const uint32_t bb[3] = {GK, GN, 1};
+  if (!encode_bf16_3d(&ta, kv_c, ad, as, ab) || !encode_bf16_3d(&tb, wkv_b, bd, bs, bb))
+    return report_error(CPATTN_ERR_INVALID_ARG,
+                        "cpattn_mla_kv_materialise: a TMA descriptor cannot describe the operands");
+  GemmParams p{};
+  p.mode = kModeKv;
+  p.M = T;
+  p.m_tiles = (T + GM - 1) / GM;
+  p.n_tiles = (int)(n_rows / GN);
+  p.batches = 1;
+  p.k_steps = L / GK;
+  p.n_total_tiles = p.m_tiles * p.n_tiles;
+  p.k_out = static_cast<__nv_bfloat16*>(k_out);
+  p.k_st = k_st;
+  p.k_sh = k_sh;
+  p.v_out = static_cast<__nv_bfloat16*>(v_out);
+  p.v_st = v_st;
+  p.v_sh = v_sh;
+  p.k_shared = static_cast<const __nv_bfloat16*>(k_shared);
+  p.ks_st = ks_st;
+  p.N = N;
+  p.V = V;
+  p.R = R;
+  p.dev_status = dev_status;
+  p.limit = wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : 2000000000ull;
+  const cudaError_t e = launch_gemm(p, ta, tb, false, stream);
+  if (e != cudaSuccess) return report_error(CPATTN_ERR_CUDA, cudaGetErrorString(e));
+  return CPATTN_OK;
+}
+
+}  // namespace cpattn

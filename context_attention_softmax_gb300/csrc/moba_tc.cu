@@ -261,6 +261,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   const cpattn_attn_args& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &s.abort;
+  const uint64_t lim = wait_limit(a);
   const int n_units = *p.n_units;
   const int group = a.Hq / a.Hkv;
 
@@ -314,11 +315,11 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           const int st = jt % NS;
           const uint32_t ph = (jt / NS) & 1;
           const int row0 = un.y * p.B + t * BN;
-          if (!mbar_wait(&s.k_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.k_empty[st], ph ^ 1, abort_flag, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
           tma_load_3d(s.k[st], &tm_k, &s.k_full[st], 0, g, row0);
           tma_load_3d(s.k[st] + kHalf, &tm_k, &s.k_full[st], 64, g, row0);
-          if (!mbar_wait(&s.v_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.v_empty[st], ph ^ 1, abort_flag, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
           tma_load_3d(s.v[st], &tm_v, &s.v_full[st], 0, g, row0);
           tma_load_3d(s.v[st] + kHalf, &tm_v, &s.v_full[st], 64, g, row0);
@@ -344,7 +345,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
       const int4 un = p.units[u];
       const int qb = ui & 1;
-      ok = __all_sync(kFullMask, mbar_wait(&s.q_empty[qb], ((ui >> 1) & 1) ^ 1, abort_flag));
+      ok = __all_sync(kFullMask, mbar_wait(&s.q_empty[qb], ((ui >> 1) & 1) ^ 1, abort_flag, lim));
       if (!ok) break;
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -380,13 +381,13 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       int prev = -1, prev_first = 0, prev_last = 0, prev_ui = 0;
       auto issue_pv = [&]() -> bool {
         const int j = prev;
-        if (!mbar_wait(&s.p_full[j & 1], (j >> 1) & 1, abort_flag) ||
-            !mbar_wait(&s.v_full[j % NS], (j / NS) & 1, abort_flag)) return false;
+        if (!mbar_wait(&s.p_full[j & 1], (j >> 1) & 1, abort_flag, lim) ||
+            !mbar_wait(&s.v_full[j % NS], (j / NS) & 1, abort_flag, lim)) return false;
         // O of unit u lives in buffer u & 1; its first PV waits until the
         // epilogue has read unit u - 2 out of that buffer
         const int ob = prev_ui & 1;
         if (prev_first && prev_ui >= 2 &&
-            !mbar_wait(&s.o_free[ob], ((prev_ui - 2) >> 1) & 1, abort_flag)) return false;
+            !mbar_wait(&s.o_free[ob], ((prev_ui - 2) >> 1) & 1, abort_flag, lim)) return false;
         tc_fence_after();
         const uint32_t vb = (j % NS) ? v_lo1 : v_lo0;
         const uint32_t pa = tmem + kColS + (j & 1) * BN;
@@ -401,10 +402,10 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
         const int4 un = p.units[u];
         const int T = unit_tiles(p, un.y), qb = ui & 1;
-        if (!mbar_wait(&s.q_full[qb], (ui >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&s.q_full[qb], (ui >> 1) & 1, abort_flag, lim)) { ok = false; break; }
         for (int t = 0; t < T; ++t, ++jt) {
           const int st = jt % NS;
-          if (!mbar_wait(&s.k_full[st], (jt / NS) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&s.k_full[st], (jt / NS) & 1, abort_flag, lim)) { ok = false; break; }
           tc_fence_after();
           umma8_ss_kmajor(tmem + kColS + (jt & 1) * BN, qb ? q_lo1 : q_lo0, st ? k_lo1 : k_lo0,
                           idesc_qk);
@@ -452,7 +453,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           lo_c = (int)max((int64_t)0, min((int64_t)BN, iv.lo - kbase));
           hi_c = (int)max((int64_t)-1, min((int64_t)kvalid - 1, iv.hi - kbase));
         }
-        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[jt & 1], (jt >> 1) & 1, abort_flag));
+        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[jt & 1], (jt >> 1) & 1, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
         const uint32_t s_col = tmem + lane_base + kColS + (jt & 1) * BN;
@@ -511,7 +512,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         l = l * alpha + (a0 + a1);
         if (__any_sync(kFullMask, rescale)) {
           // O holds PV of this unit's earlier tiles: wait for the last one
-          ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (jt - 1) & 1, abort_flag));
+          ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (jt - 1) & 1, abort_flag, lim));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -546,8 +547,8 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
       const int4 un = p.units[u];
       const int ob = ui & 1;
-      ok = __all_sync(kFullMask, mbar_wait(&s.o_full[ob], (ui >> 1) & 1, abort_flag) &&
-                                     mbar_wait(&s.st_full[ob], (ui >> 1) & 1, abort_flag));
+      ok = __all_sync(kFullMask, mbar_wait(&s.o_full[ob], (ui >> 1) & 1, abort_flag, lim) &&
+                                     mbar_wait(&s.st_full[ob], (ui >> 1) & 1, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();
       const float4 st = s.stats[ob][r];

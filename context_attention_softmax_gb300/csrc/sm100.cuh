@@ -55,27 +55,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // As mbar_try_wait, but a thread whose phase is still open is suspended
-// until the phase completes or about a millisecond has passed, so a waiting
+// until the phase completes or about hint_ns have passed, so a waiting
 // warp takes no issue slots from the warps that share its sub-partition.
-__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
 
 // Wait until the phase with the given parity has completed.  Returns false
 // (and sets *abort) when the wait exceeds limit_ns or another role aborted.
+// A thread is suspended for at most min(limit_ns, 1 ms) at a time.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns = 2000000000ull) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait_suspend(bar, parity)) {
+  const uint32_t hint = limit_ns < 1000000ull ? (uint32_t)limit_ns : 1000000u;
+  while (!mbar_try_wait_suspend(bar, parity, hint)) {
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;

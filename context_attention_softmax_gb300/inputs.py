@@ -241,3 +241,41 @@ def moba(seed=0, Tq=8192, Tk=65536, offset=57344, H=32, D=128, block_size=512, t
     return Workload(f"moba_{Tq}x{Tk}_h{H}_b{block_size}_top{topk}", "bf16", q, k, v,
                     scale=1.0 / np.sqrt(D), causal=True, causal_offset=offset,
                     block_size=block_size, topk=topk)
+
+
+@dataclass
+class MlaVUpWorkload:
+    o_latent: torch.Tensor      # bf16 [T, H, L]
+    up_v_weight: torch.Tensor   # bf16 [H, L, V]
+
+
+def mla_v_up(seed=0, T=4096, H=128, L=512, V=128):
+    """Value up-projection after absorbed attention, bf16: the DSA workload's
+    latent output shape [4096, 128, 512] times up_v_weight [128, 512, 128].
+    o_latent ~ N(0, 1); up_v_weight ~ N(0, 1) / sqrt(L) (unit-variance output)."""
+    rng = np.random.default_rng(seed)
+    o = to_device_dtype(_draw(rng, (T, H, L)), "bf16")
+    w = to_device_dtype(_draw(rng, (H, L, V), 1.0 / np.sqrt(L)), "bf16")
+    return MlaVUpWorkload(o, w)
+
+
+@dataclass
+class MlaKvWorkload:
+    kv_c: torch.Tensor          # bf16 [T, L]   gathered compressed latents
+    k_shared: torch.Tensor      # bf16 [T, R]   gathered head-shared key
+    wkv_b: torch.Tensor         # bf16 [H * (N + V), L]
+    H: int
+    N: int
+    V: int
+
+
+def mla_kv(seed=0, T=32768, H=128, L=512, N=128, V=128, R=64):
+    """K/V materialisation from gathered latents, bf16, on the DSA workload's
+    absorbed-MLA dims (latent 512, shared rope key 64) over its 32768-token
+    gathered sequence, 128 heads with 128 key and 128 value channels each.
+    kv_c, k_shared ~ N(0, 1); wkv_b ~ N(0, 1) / sqrt(L)."""
+    rng = np.random.default_rng(seed)
+    c = to_device_dtype(_draw(rng, (T, L)), "bf16")
+    ks = to_device_dtype(_draw(rng, (T, R)), "bf16")
+    wb = to_device_dtype(_draw(rng, (H * (N + V), L), 1.0 / np.sqrt(L)), "bf16")
+    return MlaKvWorkload(c, ks, wb, H, N, V)

@@ -1,6 +1,6 @@
 /*
  * cpattn.h - C ABI of the GB300 context-parallel chunk attention library
- * (libcpattn.so).  One GPU, forward only.
+ * (libcpattn.so).  One GPU, forward (plus the MLA projections around it).
  *
  * What it computes.  A local query chunk placed at a global token offset
  * attends to a gathered global KV sequence:
@@ -45,7 +45,11 @@
  *     Data errors found on the device (an index out of range) are written to
  *     the optional `dev_status` word (set to CPATTN_ERR_BAD_INDEX, first
  *     error wins; the caller zeroes it and reads it after synchronising).
- *     No call traps, asserts or aborts.
+ *     No call traps, asserts or aborts.  The tensor-core kernels wait on
+ *     their own pipeline barriers with a bounded wait (wait_limit_ns, 2 s by
+ *     default); a wait that runs out makes the kernel drain its copies and
+ *     MMAs in flight, release its tensor memory, write CPATTN_ERR_TIMEOUT to
+ *     dev_status and return; later calls on the stream are unaffected.
  *   Dtypes: q, k, v and o are all CPATTN_BF16 (fp32 accumulation) or all
  *     CPATTN_FP32.  LSE, partials and scratch are fp32.
  */
@@ -59,7 +63,7 @@
 extern "C" {
 #endif
 
-#define CPATTN_VERSION 100  /* 1.0.0 */
+#define CPATTN_VERSION 110  /* 1.1.0 */
 
 typedef enum {
   CPATTN_OK = 0,
@@ -130,6 +134,7 @@ typedef struct cpattn_attn_args {
   float* partial_o;                      /* see above, or NULL */
   float* partial_lse;
   int32_t* dev_status;                   /* optional device int32 */
+  int64_t wait_limit_ns;                 /* limit of each bounded device wait; 0 = 2 s */
 } cpattn_attn_args;
 
 /*
@@ -274,6 +279,44 @@ cpattn_status cpattn_block_gate_static(const cpattn_attn_args* args, int32_t blo
 cpattn_status cpattn_dsa_indexer(const cpattn_attn_args* args, const float* w, int32_t topk,
                                  int32_t* indices, void* workspace, size_t workspace_bytes,
                                  void* stream);
+
+/*
+ * cpattn_mla_v_up - value up-projection after absorbed attention.
+ * Source: "[1/2] Enable DSA CP, THD with absorbed MLA - #3674", sequence
+ * diagram (after the sparse gather, an einsum with up_v_weight gives each
+ * head's v_channels) and Background (the value up-projection is applied
+ * after attention on the latent).
+ *   out[t, h, :] = o_latent[t, h, :] @ up_v_weight[h]
+ * o_latent: bf16 [T, H, L] (strides in elements, last dim contiguous), e.g.
+ * the output of cpattn_topk_sparse_fwd on absorbed-MLA shapes; up_v_weight:
+ * bf16 [H, L, V] contiguous; out: bf16 [T, H, V].  fp32 accumulation.
+ * Limits: L a multiple of 64, V a multiple of 128.  No workspace.
+ * wait_limit_ns: limit of each bounded device wait (0 = 2 s).
+ */
+cpattn_status cpattn_mla_v_up(const void* o_latent, int64_t o_stride_t, int64_t o_stride_h,
+                              const void* up_v_weight, int32_t T, int32_t H, int32_t L, int32_t V,
+                              void* out, int64_t out_stride_t, int64_t out_stride_h,
+                              int32_t* dev_status, int64_t wait_limit_ns, void* stream);
+
+/*
+ * cpattn_mla_kv_materialise - per-head K and V from gathered MLA latents.
+ * Source: "[BC][MLA][CP] Optimize MLA all-gather and Ulysses communication
+ * for Kimi K3 and dpskV3", "K/V all-gather CP" (gather the compressed
+ * latents and the head-shared key, then apply wkv_b and build K/V locally).
+ *   kv = kv_c @ wkv_b^T viewed [T, H, N + V];
+ *   k_out[t, h] = [kv[t, h, :N] | k_shared[t]],  v_out[t, h] = kv[t, h, N:]
+ * kv_c: bf16 [T, L] (row stride c_stride_t); k_shared: bf16 [T, R] (row
+ * stride ks_stride_t; unused when R = 0); wkv_b: bf16 [H * (N + V), L]
+ * contiguous (a linear layer's weight); k_out: bf16 [T, H, N + R]; v_out:
+ * bf16 [T, H, V].  fp32 accumulation.  Limits: L a multiple of 64, N and V
+ * multiples of 128, R a multiple of 8.  No workspace.
+ */
+cpattn_status cpattn_mla_kv_materialise(const void* kv_c, int64_t c_stride_t, const void* k_shared,
+                                        int64_t ks_stride_t, const void* wkv_b, int32_t T, int32_t L,
+                                        int32_t H, int32_t N, int32_t R, int32_t V, void* k_out,
+                                        int64_t k_stride_t, int64_t k_stride_h, void* v_out,
+                                        int64_t v_stride_t, int64_t v_stride_h, int32_t* dev_status,
+                                        int64_t wait_limit_ns, void* stream);
 
 /* Bytes of device workspace the call needs (0 if none; for
  * CPATTN_OP_CHUNK_FWD the bytes that enable the SM-balanced schedule).

@@ -53,3 +53,18 @@ def to_gpu(w: inputs.Workload):
     else:
         v = w.v.to(d)
     return q, k, v
+
+
+# Outputs of a bf16 GEMM (fp32 accumulation, one bf16 rounding of the result):
+# the rounding is at most 2^-9 relative; the fp32 sums of K <= 1024 exact bf16
+# products add at most K 2^-24 sum|a b|, far below that.  The bound used:
+# |got - ref| <= 2^-8 |ref| + 1e-3 (twice the rounding, plus an absolute floor
+# for results near zero).
+def assert_gemm_close(got, ref, what=""):
+    g = got.detach().float().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    assert g.shape == ref.shape, (what, g.shape, ref.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-3
+    bad = np.abs(g - ref) > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} elements beyond 2^-8|ref| + 1e-3, worst "
+                           f"{np.abs(g - ref)[bad].max():.3e}")

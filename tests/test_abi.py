@@ -57,7 +57,7 @@ def test_struct_layout_matches_c():
 
 
 def test_version_and_empty_error(lib):
-    assert lib.cpattn_version() == 100
+    assert lib.cpattn_version() == 110
 
 
 def _valid_args():

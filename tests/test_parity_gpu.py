@@ -556,3 +556,37 @@ def test_dsa_indexer_full_size_every_row():
     lay = orc.make_layout(qI.shape[0], kI.shape[0], True, w.causal_offset)
     ref = orc.dsa_indexer_topk(qI.numpy(), kI.numpy(), wt.numpy(), lay, w.topk)[:, 0, :]
     np.testing.assert_array_equal(got.cpu().numpy(), ref)
+
+
+# ---------------------------------------------------------------- bounded waits
+def test_bounded_wait_runs_out_reports_timeout_and_the_stream_stays_usable():
+    """A wait limit of 1 ns on the dense tensor-core kernel (one unit per CTA,
+    64 KV tiles per CTA, so hundreds of waits): some barrier wait runs out,
+    the kernel drains its copies and MMAs, frees tensor memory, writes
+    CPATTN_ERR_TIMEOUT to dev_status and returns.  The next call on the same
+    stream, with the default limit, is correct."""
+    import ctypes
+    from context_attention_softmax_gb300 import _lib
+    w = inputs.dense_gqa(seed=12, global_seq=256, cp_size=1, rank=0, Hq=2, Hkv=1, Tk=8192,
+                         kv_chunks=0)
+    w.causal_offset = 8192 - 256
+    qd, kd, vd = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    o = torch.empty((qd.shape[0], qd.shape[1], 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((qd.shape[0], qd.shape[1]), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lib = _lib.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    a = pkg._args(qd, kd, vd, w.scale, True, w.causal_offset, None, None, None, 0, o, lse,
+                  dev_status=status)
+    a.wait_limit_ns = 1
+    _lib.check(lib.cpattn_chunk_fwd(ctypes.byref(a), None, 0, stream))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 5               # CPATTN_ERR_TIMEOUT
+    status.zero_()
+    a.wait_limit_ns = 0                          # default limit
+    _lib.check(lib.cpattn_chunk_fwd(ctypes.byref(a), None, 0, stream))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    q, k, v = f64(w)
+    O, L = orc.dense_attention(q, k, v, w.scale, layout_of(w))
+    assert_matches(o, lse, O, L, "bf16", "after a timed-out call")

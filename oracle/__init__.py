@@ -15,6 +15,7 @@ from .attention import (  # noqa: F401
     block_means,
     chunk_summary,
     dense_attention,
+    dense_attention_backward,
     dsa_indexer_topk,
     finalise,
     logical_positions,

@@ -187,6 +187,52 @@ def dense_attention(q, k, v, scale, layout, rows=None, row_block=256):
     return O, LSE
 
 
+def dense_attention_backward(q, k, v, scale, layout, d_out):
+    """Gradients of ``dense_attention`` with respect to q, k and v.
+
+    [CP] ¶2: backward must return the contributions of a chunk's queries to
+    the owners of K and V, so dk and dv cover every gathered KV row (what
+    this chunk's queries add; summing over chunks is outside this function).
+    [CP] ¶4: the backward rebuilds the probabilities from the forward's
+    saved statistics; here they are the exact global-softmax weights.  With
+    P[i, j] = softmax over the permitted keys of row i (0 elsewhere) and
+    g = dO:
+        dv[j]  = sum_i P[i, j] g[i]                      (per KV head, summed
+        dP[i, j] = <g[i], v[j]>                           over its query heads)
+        dS[i, j] = P[i, j] (dP[i, j] - sum_j' P[i, j'] dP[i, j'])
+        dq[i]  = scale sum_j dS[i, j] k[j]
+        dk[j]  = scale sum_i dS[i, j] q[i]
+    A row with no permitted key contributes nothing.
+
+    q: [Tq, Hq, Dqk], k: [Tk, Hkv, Dqk], v: [Tk, Hkv, Dv], d_out: [Tq, Hq, Dv].
+    Returns dq [Tq, Hq, Dqk], dk [Tk, Hkv, Dqk], dv [Tk, Hkv, Dv] float64.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    g = np.asarray(d_out, np.float64)
+    Tq, Hq, _ = q.shape
+    Hkv = k.shape[1]
+    A = layout.allowed()
+    nonempty = A.any(axis=1)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for h in range(Hq):
+        gh = _kv_head(h, Hq, Hkv)
+        S = np.where(A, scale * (q[:, h, :] @ k[:, gh, :].T), NEG_INF)
+        m = np.where(nonempty, S.max(axis=1) if S.shape[1] else 0.0, 0.0)
+        E = np.where(A, np.exp(S - m[:, None]), 0.0)
+        ell = np.where(nonempty, E.sum(axis=1), 1.0)
+        P = E / ell[:, None]
+        dv[:, gh, :] += P.T @ g[:, h, :]
+        dP = g[:, h, :] @ v[:, gh, :].T
+        dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+        dq[:, h, :] = scale * (dS @ k[:, gh, :])
+        dk[:, gh, :] += scale * (dS.T @ q[:, h, :])
+    return dq, dk, dv
+
+
 # ---------------------------------------------------------------------------
 # Chunk summaries and their merge  ([CP] ¶3, ¶4)
 # ---------------------------------------------------------------------------

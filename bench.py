@@ -145,8 +145,8 @@ class DenseRunner(Runner):
         if kv_chunks:
             self.name = "dense_gqa_4chunks"
             self.launches_per_step = 2                        # chunk summaries, LSE merge
-            how = ("KV as 4 chunks of 2048: per-chunk finalised summaries (O_c, LSE_c), then "
-                   "cpattn_lse_merge (chunk 3 fully masked, neutral)")
+            how = ("KV as 4 chunks of 2048: per-chunk finalised summaries (O_c, LSE_c) only, "
+                   "then cpattn_lse_merge (chunk 3 fully masked, neutral)")
         else:
             how = "KV folded in-kernel (4 chunks of 2048, chunk 3 fully masked)"
         self.config = {
@@ -174,8 +174,8 @@ class DenseRunner(Runner):
         w = self.w
         if self.kv_chunks:
             cpattn_chunk_fwd(q, k, v, scale=w.scale, causal=True, causal_offset=w.causal_offset,
-                             kv_chunk_len=w.kv_chunk_len, out=self.o, lse=self.lse,
-                             partial_o=self.po, partial_lse=self.pl, workspace=self.ws)
+                             kv_chunk_len=w.kv_chunk_len, partial_o=self.po, partial_lse=self.pl,
+                             workspace=self.ws, merged=False)
             cpattn_lse_merge(self.po, self.pl, out=self.o, lse=self.lse)
         else:
             cpattn_chunk_fwd(q, k, v, scale=w.scale, causal=True, causal_offset=w.causal_offset,

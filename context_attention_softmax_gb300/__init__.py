@@ -17,7 +17,7 @@ from . import _lib
 from ._lib import CPATTN_BF16, CPATTN_FP32, CpattnError  # noqa: F401
 
 __all__ = [
-    "cpattn_chunk_fwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd", "cpattn_block_gate",
+    "cpattn_chunk_fwd", "cpattn_chunk_bwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd", "cpattn_block_gate",
     "cpattn_dsa_indexer", "cpattn_mla_v_up", "cpattn_mla_kv_materialise",
     "cpattn_workspace_size", "cpattn_version", "CpattnError",
 ]
@@ -93,17 +93,21 @@ def _args(q, k, v, scale, causal, causal_offset, cu_seqlens, q_chunk_map, kv_chu
 def cpattn_chunk_fwd(q, k, v, scale=None, causal=True, causal_offset=0, cu_seqlens=None,
                      q_chunk_map=None, kv_chunk_map=None, chunk_len=0, kv_chunk_len=0,
                      out=None, lse=None, partial_o=None, partial_lse=None, dev_status=None,
-                     workspace=None, stream=None):
+                     workspace=None, stream=None, merged=True):
     """Dense CP-chunk attention; returns (out, lse) or, with kv_chunk_len > 0,
-    (out, lse, partial_o, partial_lse).  `workspace` (uint8, device) enables
-    the SM-balanced schedule; one is allocated when it is missing or short."""
+    (out, lse, partial_o, partial_lse) - out and lse None when merged=False
+    (partial summaries only).  `workspace` (uint8, device) enables the
+    SM-balanced schedule; one is allocated when it is missing or short."""
     dev = q.device
     cu, qm, km = (_device_i32(x, dev) for x in (cu_seqlens, q_chunk_map, kv_chunk_map))
     Tq, Hq = q.shape[0], q.shape[1]
-    if out is None:
-        out = torch.empty((Tq, Hq, v.shape[2]), dtype=q.dtype, device=dev)
-    if lse is None:
-        lse = torch.empty((Tq, Hq), dtype=torch.float32, device=dev)
+    if not merged and kv_chunk_len > 0:
+        out, lse = None, None
+    else:
+        if out is None:
+            out = torch.empty((Tq, Hq, v.shape[2]), dtype=q.dtype, device=dev)
+        if lse is None:
+            lse = torch.empty((Tq, Hq), dtype=torch.float32, device=dev)
     if kv_chunk_len > 0:
         n = -(-k.shape[0] // kv_chunk_len)
         if partial_o is None:
@@ -121,6 +125,38 @@ def cpattn_chunk_fwd(q, k, v, scale=None, causal=True, causal_offset=0, cu_seqle
     if kv_chunk_len > 0:
         return out, lse, partial_o, partial_lse
     return out, lse
+
+
+def cpattn_chunk_bwd(q, k, v, out, lse, d_out, scale=None, causal=True, causal_offset=0,
+                     cu_seqlens=None, q_chunk_map=None, kv_chunk_map=None, chunk_len=0,
+                     dq=None, dk=None, dv=None, dev_status=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv), fp32, of cpattn_chunk_fwd given its outputs
+    (out, lse) and d_out; dk, dv hold this chunk's contribution to every
+    gathered KV row."""
+    dev = q.device
+    cu, qm, km = (_device_i32(x, dev) for x in (cu_seqlens, q_chunk_map, kv_chunk_map))
+    _thd("d_out", d_out)
+    if dq is None:
+        dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    if dk is None:
+        dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    if dv is None:
+        dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _thd(n, t)
+    a = _args(q, k, v, scale, causal, causal_offset, cu, qm, km, chunk_len, out, lse,
+              dev_status=dev_status)
+    lib = _lib.load()
+    ws_bytes = lib.cpattn_workspace_size(_lib.OP_CHUNK_BWD, ctypes.byref(a), 0, 1)
+    if ws_bytes and (workspace is None or workspace.numel() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _lib.check(lib.cpattn_chunk_bwd(ctypes.byref(a), d_out.data_ptr(), d_out.stride(0),
+                                    d_out.stride(1), dq.data_ptr(), dq.stride(0), dq.stride(1),
+                                    dk.data_ptr(), dk.stride(0), dk.stride(1), dv.data_ptr(),
+                                    dv.stride(0), dv.stride(1),
+                                    _ptr(workspace) if ws_bytes else None, ws_bytes,
+                                    _stream(stream)))
+    return dq, dk, dv
 
 
 def cpattn_lse_merge(part_o, part_lse, out=None, lse=None, out_dtype=torch.bfloat16, stream=None):

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(HERE, "libcpattn.so")
 
 CPATTN_FP32 = 0
 CPATTN_BF16 = 1
-OP_CHUNK_FWD, OP_TOPK_SPARSE_FWD, OP_BLOCK_GATE, OP_DSA_INDEXER = 0, 1, 2, 3
+OP_CHUNK_FWD, OP_TOPK_SPARSE_FWD, OP_BLOCK_GATE, OP_DSA_INDEXER, OP_CHUNK_BWD = 0, 1, 2, 3, 4
 
 STATUS = {
     0: "CPATTN_OK",
@@ -29,6 +29,7 @@ STATUS = {
 # every symbol include/cpattn.h declares
 EXPORTS = (
     "cpattn_chunk_fwd",
+    "cpattn_chunk_bwd",
     "cpattn_lse_merge",
     "cpattn_topk_sparse_fwd",
     "cpattn_block_gate",
@@ -85,6 +86,8 @@ def load(path: str = LIB_PATH):
     lib = ctypes.CDLL(path)
     P = ctypes.POINTER(AttnArgs)
     lib.cpattn_chunk_fwd.argtypes = [P, c_p, ctypes.c_size_t, c_p]
+    lib.cpattn_chunk_bwd.argtypes = [P, c_p, c_i64, c_i64, c_p, c_i64, c_i64, c_p, c_i64, c_i64,
+                                     c_p, c_i64, c_i64, c_p, ctypes.c_size_t, c_p]
     lib.cpattn_lse_merge.argtypes = [c_i32, c_p, c_p, c_i32, c_i32, c_i32, c_p, c_i32, c_i64,
                                      c_i64, c_p, c_p]
     lib.cpattn_topk_sparse_fwd.argtypes = [P, c_p, c_i32, c_i32, c_i32, c_p, ctypes.c_size_t, c_p]
@@ -98,7 +101,7 @@ def load(path: str = LIB_PATH):
                                               c_i64, c_p, c_i64, c_p]
     lib.cpattn_workspace_size.argtypes = [c_i32, P, c_i32, c_i32]
     lib.cpattn_workspace_size.restype = ctypes.c_size_t
-    for name in ("cpattn_chunk_fwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd",
+    for name in ("cpattn_chunk_fwd", "cpattn_chunk_bwd", "cpattn_lse_merge", "cpattn_topk_sparse_fwd",
                  "cpattn_block_gate", "cpattn_block_gate_static", "cpattn_dsa_indexer",
                  "cpattn_mla_v_up", "cpattn_mla_kv_materialise"):
         getattr(lib, name).restype = c_i32

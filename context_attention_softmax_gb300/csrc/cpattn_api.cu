@@ -117,8 +117,13 @@ extern "C" {
 
 cpattn_status cpattn_chunk_fwd(const cpattn_attn_args* a, void* workspace, size_t workspace_bytes,
                                void* stream) {
-  TRY(check_attn(a, true, true));
+  CHECK(a != nullptr, CPATTN_ERR_INVALID_ARG, "args is NULL");
+  const bool partials_only = a->kv_chunk_len > 0 && a->o == nullptr;
+  TRY(check_attn(a, true, !partials_only));
   CHECK(a->kv_chunk_len >= 0, CPATTN_ERR_INVALID_ARG, "kv_chunk_len=%d must be >= 0", a->kv_chunk_len);
+  if (partials_only)
+    CHECK(a->lse == nullptr, CPATTN_ERR_INVALID_ARG,
+          "with o = NULL (partial summaries only) lse must be NULL too");
   if (a->kv_chunk_len > 0 && a->Tk > 0 && (int64_t)a->Tq * a->Hq > 0)
     CHECK(a->partial_o != nullptr && a->partial_lse != nullptr, CPATTN_ERR_INVALID_ARG,
           "kv_chunk_len > 0 needs partial_o and partial_lse");
@@ -227,6 +232,50 @@ cpattn_status cpattn_dsa_indexer(const cpattn_attn_args* a, const float* w, int3
                      "cpattn_dsa_indexer launch");
 }
 
+cpattn_status cpattn_chunk_bwd(const cpattn_attn_args* a, const void* d_out, int64_t do_stride_t,
+                               int64_t do_stride_h, float* dq, int64_t dq_stride_t,
+                               int64_t dq_stride_h, float* dk, int64_t dk_stride_t,
+                               int64_t dk_stride_h, float* dv, int64_t dv_stride_t,
+                               int64_t dv_stride_h, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  TRY(check_attn(a, true, true));
+  CHECK(a->dtype == CPATTN_BF16 && a->Dqk == 128 && a->Dv == 128, CPATTN_ERR_UNSUPPORTED,
+        "the backward takes bf16 q, k, v with head dims 128 (Dqk=%d, Dv=%d)", a->Dqk, a->Dv);
+  CHECK(a->kv_chunk_len == 0, CPATTN_ERR_INVALID_ARG, "the backward takes kv_chunk_len = 0");
+  CHECK(dense_bwd_supported(*a), CPATTN_ERR_UNSUPPORTED,
+        "layout not supported by the backward (chunk_len a multiple of 128, positions < 2^31)");
+  if (a->Tq > 0) {
+    CHECK(a->lse != nullptr, CPATTN_ERR_INVALID_ARG, "lse (the forward's) is NULL");
+    TRY(check_tensor("d_out", d_out, do_stride_t, do_stride_h, a->Tq, 2));
+    TRY(check_tensor("dq", dq, dq_stride_t, dq_stride_h, a->Tq, 4));
+  }
+  if (a->Tk > 0) {
+    TRY(check_tensor("dk", dk, dk_stride_t, dk_stride_h, a->Tk, 4));
+    TRY(check_tensor("dv", dv, dv_stride_t, dv_stride_h, a->Tk, 4));
+  }
+  if (a->Tq == 0 && a->Tk == 0) return ok();
+  const size_t need = a->Tq > 0 ? dense_bwd_workspace(*a) : 0;
+  CHECK(workspace_bytes >= need && (need == 0 || workspace != nullptr), CPATTN_ERR_WORKSPACE,
+        "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  if (need > 0) CHECK(aligned16(workspace), CPATTN_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (a->Tq == 0 || a->Tk == 0) {   // no pair: every gradient is zero
+    for (int64_t t = 0; t < a->Tq; ++t)   // rows may be strided: clear row by row
+      if (cudaMemsetAsync(dq + t * dq_stride_t, 0, (size_t)((a->Hq - 1) * dq_stride_h + 128) * 4, st) != cudaSuccess)
+        return fail(CPATTN_ERR_CUDA, "cudaMemsetAsync failed");
+    for (int64_t t = 0; t < a->Tk; ++t) {
+      if (cudaMemsetAsync(dk + t * dk_stride_t, 0, (size_t)((a->Hkv - 1) * dk_stride_h + 128) * 4, st) != cudaSuccess ||
+          cudaMemsetAsync(dv + t * dv_stride_t, 0, (size_t)((a->Hkv - 1) * dv_stride_h + 128) * 4, st) != cudaSuccess)
+        return fail(CPATTN_ERR_CUDA, "cudaMemsetAsync failed");
+    }
+    return ok();
+  }
+  return cuda_status(launch_dense_bwd(*a, d_out, do_stride_t, do_stride_h, dq, dq_stride_t,
+                                      dq_stride_h, dk, dk_stride_t, dk_stride_h, dv, dv_stride_t,
+                                      dv_stride_h, workspace, st),
+                     "cpattn_chunk_bwd launch");
+}
+
 cpattn_status cpattn_mla_v_up(const void* o_latent, int64_t o_stride_t, int64_t o_stride_h,
                               const void* up_v_weight, int32_t T, int32_t H, int32_t L, int32_t V,
                               void* out, int64_t out_stride_t, int64_t out_stride_h,
@@ -280,6 +329,7 @@ size_t cpattn_workspace_size(int32_t op, const cpattn_attn_args* a, int32_t topk
   if (op == CPATTN_OP_BLOCK_GATE) return block_size > 0 ? block_gate_workspace(*a, block_size) : 0;
   if (op == CPATTN_OP_DSA_INDEXER) return a->Tq > 0 ? dsa_indexer_workspace(*a, dsa_indexer_grid(*a)) : 0;
   if (op == CPATTN_OP_CHUNK_FWD) return a->kv_chunk_len == 0 ? dense_tc_bal_workspace(*a) : 0;
+  if (op == CPATTN_OP_CHUNK_BWD) return a->Tq > 0 ? dense_bwd_workspace(*a) : 0;
   if (op == CPATTN_OP_TOPK_SPARSE_FWD && block_size > 1 && topk > 0 &&
       moba_tc_supported(*a, 1, block_size, topk))
     return moba_tc_workspace(*a, topk, block_size);

@@ -129,10 +129,13 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const cpattn_attn_args& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
-  const Block blk[2] = {
-      p.fold ? folded_block_of(a.Hq, p.n_qtiles, u, 0) : block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 0),
-      p.fold ? folded_block_of(a.Hq, p.n_qtiles, u, 1) : block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 1)};
-  const int g = blk[0].head / (a.Hq / a.Hkv);
+  // The two blocks as separate values (a runtime-indexed array would live in
+  // local memory); the softmax warps select theirs once.
+  const Block blk0 = p.fold ? folded_block_of(a.Hq, p.n_qtiles, u, 0)
+                            : block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 0);
+  const Block blk1 = p.fold ? folded_block_of(a.Hq, p.n_qtiles, u, 1)
+                            : block_of(a.Hq, p.head_pairs, p.n_qtiles, u, 1);
+  const int g = blk0.head / (a.Hq / a.Hkv);
   volatile int* abort_flag = &s.abort;
   const uint64_t lim = wait_limit(a);
 
@@ -174,9 +177,10 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const bool softmax_role = warp >= 4;
   const int X = softmax_role ? (warp - 4) >> 2 : 0;
   const int r = (warp & 3) * 32 + lane;
+  const int my_head = X ? blk1.head : blk0.head, my_q0 = X ? blk1.q0 : blk0.q0;
   KeyInterval iv{1, 0};
   if (softmax_role) {
-    const int64_t tok = (int64_t)blk[X].q0 + r;
+    const int64_t tok = (int64_t)my_q0 + r;
     if (tok < a.Tq) iv = allowed_interval(a, query_pos(a, tok));
     long long lo = iv.lo <= iv.hi ? (long long)iv.lo : LLONG_MAX;
     long long hi = iv.lo <= iv.hi ? (long long)iv.hi : LLONG_MIN;
@@ -234,16 +238,16 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   }
   __syncthreads();
-  const int nx[2] = {s.n_blk[0], s.n_blk[1]};
-  const int n_run = max(nx[0], nx[1]);   // list entries loaded and multiplied
+  const int nx0 = s.n_blk[0], nx1 = s.n_blk[1];
+  const int n_run = max(nx0, nx1);   // list entries loaded and multiplied
   // Tail: once the short block Sb has run its n_short tiles, the long block
   // Lb alternates its S between its own S columns and Sb's, so S(j+1) runs on
   // the tensor core while softmax(j) runs.  Tail tile n_short + u uses Lb's
   // columns for even u, Sb's for odd u; both barriers have then completed
   // n_short + u/2 phases before it.
-  const int Sb = nx[0] < nx[1] ? 0 : 1, Lb = 1 - Sb;
-  const int n_short = nx[Sb];
-  const bool tail2 = n_short >= 1 && nx[Lb] > n_short;
+  const int Sb = nx0 < nx1 ? 0 : 1, Lb = 1 - Sb;
+  const int n_short = min(nx0, nx1);
+  const bool tail2 = n_short >= 1 && n_run > n_short;
 
   if (warp < 4) {
   regs_dec<kRegsControl>();
@@ -256,10 +260,10 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int kt = s.live_kt[i];
         if (!q_issued) {
           mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
-          for (int x = 0; x < 2; ++x) {
-            tma_load_3d(s.q[x], &tm_q, &s.q_full, 0, blk[x].head, blk[x].q0);
-            tma_load_3d(s.q[x] + kHalf, &tm_q, &s.q_full, 64, blk[x].head, blk[x].q0);
-          }
+          tma_load_3d(s.q[0], &tm_q, &s.q_full, 0, blk0.head, blk0.q0);
+          tma_load_3d(s.q[0] + kHalf, &tm_q, &s.q_full, 64, blk0.head, blk0.q0);
+          tma_load_3d(s.q[1], &tm_q, &s.q_full, 0, blk1.head, blk1.q0);
+          tma_load_3d(s.q[1] + kHalf, &tm_q, &s.q_full, 64, blk1.head, blk1.q0);
           q_issued = true;
         }
         const int jt = k_issued, st = jt % NS;
@@ -320,7 +324,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (ok) {
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
-          if (nx[x] > 0) issue_s(0, x);
+          if ((x ? nx1 : nx0) > 0) issue_s(0, x);
         umma_commit(&s.k_empty[0]);
       }
       // Step jt: for each block still running, PV_X(jt) then S_X(jt+1).  A
@@ -355,12 +359,13 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         bool k_ready = false;
         for (int x = 0; x < 2 && ok; ++x) {
-          if (jt >= nx[x]) continue;
+          const int nxx = x ? nx1 : nx0;
+          if (jt >= nxx) continue;
           if (!mbar_wait(&s.p_full[x], jt & 1, abort_flag, lim)) { ok = false; break; }
           tc_fence_after();
           issue_pv(jt, x);
-          if (x == 1 || jt >= nx[1]) umma_commit(&s.v_empty[st]);
-          if (jt + 1 == nx[x]) {
+          if (x == 1 || jt >= nx1) umma_commit(&s.v_empty[st]);
+          if (jt + 1 == nxx) {
             umma_commit(&s.o_ready[x]);
           } else {
             if (!k_ready) {
@@ -398,9 +403,10 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float m2 = -CUDART_INF_F, l = 0.f;
     int jt = 0;
     bool ok = true;
-    const int64_t tok_row = (int64_t)blk[X].q0 + r;
+    const int64_t tok_row = (int64_t)my_q0 + r;
     int cur_c = 0;                       // CHUNKS: the chunk being summarised
-    for (int i = 0; i < nx[X]; ++i) {
+    const int my_n = X ? nx1 : nx0;
+    for (int i = 0; i < my_n; ++i) {
       const int kt = s.live_kt[i];
       const int64_t kbase = logical_pos(a.kv_chunk_map, a.chunk_len, (int64_t)kt * BN);
       const int kvalid = min(BN, a.Tk - kt * BN);
@@ -432,11 +438,11 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               if (!ok) break;
               tc_fence_after();
             }
-            write_partial(a, cur_c, tok_row, blk[X].head, o_col, l, m2, true);
+            write_partial(a, cur_c, tok_row, my_head, o_col, l, m2, true);
             ++cur_c;
           }
           for (; cur_c < c_tile; ++cur_c)
-            write_partial(a, cur_c, tok_row, blk[X].head, o_col, 0.f, 0.f, false);
+            write_partial(a, cur_c, tok_row, my_head, o_col, 0.f, 0.f, false);
           m2 = -CUDART_INF_F;
           l = 0.f;
         }
@@ -525,7 +531,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       if (ok) tc_fence_after();
     }
     const int64_t tok = tok_row;
-    const int h = blk[X].head;
+    const int h = my_head;
     if constexpr (CHUNKS) {
       // close the last chunk, write the unreached ones neutral, then merge
       // this row's partials: L = max_c LSE_c, w_c = exp(LSE_c - L),
@@ -535,7 +541,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++cur_c;
       }
       for (; cur_c < p.n_parts; ++cur_c) write_partial(a, cur_c, tok, h, o_col, 0.f, 0.f, false);
-      if (tok < a.Tq) {
+      if (tok < a.Tq && a.o != nullptr) {   // o == NULL: the partial summaries only
         const int64_t stride = (int64_t)a.Tq * a.Hq;
         const int64_t row0 = tok * a.Hq + h;
         float L = -CUDART_INF_F;

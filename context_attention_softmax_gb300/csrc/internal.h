@@ -92,6 +92,14 @@ cudaError_t launch_gate_tc(const cpattn_attn_args& a, int32_t block_size, int32_
                            const double* mu64, const float* mu32, void* parts, cudaStream_t stream,
                            bool* launched);
 size_t block_gate_smem(int n_blocks, int D);
+// Backward of the dense chunk attention on the tensor cores (dense_bwd.cu):
+// bf16, d = 128; fp32 gradients; workspace for D, LSE2 and tile intervals.
+bool dense_bwd_supported(const cpattn_attn_args& a);
+size_t dense_bwd_workspace(const cpattn_attn_args& a);
+cudaError_t launch_dense_bwd(const cpattn_attn_args& a, const void* g, int64_t g_st, int64_t g_sh,
+                             float* dq, int64_t dq_st, int64_t dq_sh, float* dk, int64_t dk_st,
+                             int64_t dk_sh, float* dv, int64_t dv_st, int64_t dv_sh, void* ws,
+                             cudaStream_t stream);
 // MLA projections on the tensor cores (mla_gemm.cu); arguments validated by
 // the caller.
 cpattn_status mla_v_up_impl(const void* o_latent, int64_t o_st, int64_t o_sh,

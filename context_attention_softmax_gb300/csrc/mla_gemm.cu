@@ -218,6 +218,16 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
           dst = p.v_out + t * p.v_st + (int64_t)h * p.v_sh + (part - p.N);
         }
       }
+      // the head-shared key after this head's last key tile: every load is
+      // issued before the accumulator is read, so their latency overlaps it
+      constexpr int kRopeRegs = 8;   // up to 64 channels in registers per pass
+      uint4 rope_v[kRopeRegs];
+      const bool do_rope = rope && t < p.M;
+      const uint4* rsrc = reinterpret_cast<const uint4*>(p.k_shared + (do_rope ? t : 0) * p.ks_st);
+      const int n_rope = do_rope ? p.R / 8 : 0;
+#pragma unroll
+      for (int i = 0; i < kRopeRegs; ++i)
+        if (i < n_rope) rope_v[i] = __ldg(rsrc + i);
 #pragma unroll
       for (int c4 = 0; c4 < GN / 32; ++c4) {
         uint32_t acc[32];
@@ -236,10 +246,19 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty[buf]);
-      if (rope && t < p.M) {   // the head-shared key after this head's last key tile
-        const uint4* src = reinterpret_cast<const uint4*>(p.k_shared + t * p.ks_st);
+      if (do_rope) {
         uint4* kd = reinterpret_cast<uint4*>(p.k_out + t * p.k_st + (int64_t)h * p.k_sh + p.N);
-        for (int i = 0; i < p.R / 8; ++i) kd[i] = __ldg(src + i);
+#pragma unroll
+        for (int i = 0; i < kRopeRegs; ++i)
+          if (i < n_rope) kd[i] = rope_v[i];
+        for (int i0 = kRopeRegs; i0 < n_rope; i0 += kRopeRegs) {   // R > 64: further passes
+#pragma unroll
+          for (int i = 0; i < kRopeRegs; ++i)
+            if (i0 + i < n_rope) rope_v[i] = __ldg(rsrc + i0 + i);
+#pragma unroll
+          for (int i = 0; i < kRopeRegs; ++i)
+            if (i0 + i < n_rope) kd[i0 + i] = rope_v[i];
+        }
       }
     }
   }

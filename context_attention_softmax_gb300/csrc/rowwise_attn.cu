@@ -227,6 +227,7 @@ rowwise_attn_kernel(const RowParams p) {
     }
   }
 
+  if (a.o == nullptr) return;   // partial summaries only (kv_chunk_len > 0)
   T* orow = reinterpret_cast<T*>(a.o) + i * a.o_stride_t + h * a.o_stride_h;
   write_final<T, VPL>(tot, orow, a.lse ? a.lse + row : nullptr, Dv, lane);
 }

@@ -1,6 +1,7 @@
 /*
  * cpattn.h - C ABI of the GB300 context-parallel chunk attention library
- * (libcpattn.so).  One GPU, forward (plus the MLA projections around it).
+ * (libcpattn.so).  One GPU: forward, backward, and the MLA projections
+ * around them.
  *
  * What it computes.  A local query chunk placed at a global token offset
  * attends to a gathered global KV sequence:
@@ -78,7 +79,7 @@ typedef enum {
 enum { CPATTN_FP32 = 0, CPATTN_BF16 = 1 };
 
 enum { CPATTN_OP_CHUNK_FWD = 0, CPATTN_OP_TOPK_SPARSE_FWD = 1, CPATTN_OP_BLOCK_GATE = 2,
-       CPATTN_OP_DSA_INDEXER = 3 };
+       CPATTN_OP_DSA_INDEXER = 3, CPATTN_OP_CHUNK_BWD = 4 };
 
 /*
  * Arguments of one attention call (shared by chunk_fwd, topk_sparse_fwd and
@@ -107,6 +108,9 @@ enum { CPATTN_OP_CHUNK_FWD = 0, CPATTN_OP_TOPK_SPARSE_FWD = 1, CPATTN_OP_BLOCK_G
  *   partial_o   fp32 [n_parts, Tq, Hq, Dv] contiguous: z_c / l_c (0 if neutral)
  *   partial_lse fp32 [n_parts, Tq, Hq] contiguous:  m_c + ln l_c (-inf if neutral)
  * and o / lse hold the merge of all chunks (cpattn_lse_merge semantics).
+ * With kv_chunk_len > 0, o and lse may both be NULL: only the partial
+ * summaries are written (a caller that merges them itself, e.g. after
+ * exchanging them, skips the in-kernel merge).
  */
 typedef struct cpattn_attn_args {
   int32_t dtype;                         /* CPATTN_BF16 or CPATTN_FP32 */
@@ -156,6 +160,35 @@ typedef struct cpattn_attn_args {
  */
 cpattn_status cpattn_chunk_fwd(const cpattn_attn_args* args, void* workspace,
                                size_t workspace_bytes, void* stream);
+
+/*
+ * cpattn_chunk_bwd - gradients of cpattn_chunk_fwd for one query chunk.
+ * Source: "Context parallel attention: exchange keys and merge softmax
+ * globally" para 2 (backward returns and combines contributions to the
+ * owners of K and V) and para 4 (backward intermediates are rebuilt with
+ * matching reconstruction rules: here the probabilities come from the
+ * forward's LSE).  With P[i, j] = exp(s_ij - LSE_i) on permitted pairs,
+ * g = d_out and D_i = <g_i, o_i>:
+ *   dv_j = sum_i P_ij g_i,  dS_ij = P_ij (<g_i, v_j> - D_i),
+ *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,
+ * dk, dv of a KV head summed over its query heads.  dk and dv cover every
+ * gathered KV row and hold this chunk's contribution only; adding the
+ * contributions of all chunks (a reduce-scatter to the owners) is the
+ * caller's.
+ * Inputs: args as given to the forward (q, k, v, positions, cu_seqlens,
+ * chunk maps, scale, causal) plus its outputs o (bf16) and lse (fp32);
+ * d_out bf16 [Tq, Hq, 128].  Outputs (overwritten, not accumulated): dq fp32
+ * [Tq, Hq, 128], dk, dv fp32 [Tk, Hkv, 128], strides in elements.
+ * Workspace: cpattn_workspace_size(CPATTN_OP_CHUNK_BWD, ...) bytes.
+ * Limits: bf16, Dqk = Dv = 128, kv_chunk_len = 0, chunk maps with chunk_len
+ * a multiple of 128, logical positions below 2^31.
+ */
+cpattn_status cpattn_chunk_bwd(const cpattn_attn_args* args, const void* d_out, int64_t do_stride_t,
+                               int64_t do_stride_h, float* dq, int64_t dq_stride_t,
+                               int64_t dq_stride_h, float* dk, int64_t dk_stride_t,
+                               int64_t dk_stride_h, float* dv, int64_t dv_stride_t,
+                               int64_t dv_stride_h, void* workspace, size_t workspace_bytes,
+                               void* stream);
 
 /*
  * cpattn_lse_merge - merge finalised per-chunk results into the global one.

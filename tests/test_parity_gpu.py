@@ -98,6 +98,10 @@ def test_dense_gqa_full_size_every_row():
     assert_matches(o4, l4, O, L, "bf16", "cfg 4 chunks")
     om, lm = cpattn_lse_merge(po, pl, out_dtype=torch.bfloat16)
     assert_matches(om, lm, O, L, "bf16", "cfg 4 chunks merged")
+    # partial summaries only (o = lse = NULL), then the merge: the bench's step
+    none_o, none_l, po2, pl2 = _chunk(w, kv_chunk_len=w.kv_chunk_len, merged=False)
+    assert none_o is None and none_l is None
+    assert torch.equal(po2, po) and torch.equal(pl2, pl)
     rows = sample_rows(w.Tq, 64, edges=(1, 127, 128, 1023, 2047))
     _, _, PO, PL = orc.summarised_attention(q, k, v, w.scale, layout_of(w), w.kv_chunk_len,
                                             rows=rows)

@@ -13,6 +13,7 @@ The same JSON line carries one record per other workload under "workloads",
 each timed the same way with its own roofline, oracle baseline and
 end-to-end figure:
   dense_gqa_4chunks  the headline problem as 4 KV-chunk summaries + merge
+  dense_gqa_bwd      its backward (dq, dk, dv; TFLOP/s at 10 d per pair)
   zigzag             packed THD varlen, zigzag cp=8, all 8 rank calls (TFLOP/s)
   dsa                DSA top-2048 sparse attention, absorbed MLA (TFLOP/s and
                      gathered GB/s)
@@ -197,6 +198,72 @@ class DenseRunner(Runner):
             orc.dense_attention(q, k, v, w.scale, self._lay, rows=rows)
         qpos = w.causal_offset + rows
         return 4.0 * w.q.shape[2] * float(np.minimum(qpos + 1, w.Tk).sum()) * w.q.shape[1]
+
+
+class DenseBwdRunner(Runner):
+    """Backward of the headline workload: dq, dk, dv from the forward's O and
+    LSE and a seeded d_out (prep, dk/dv kernel, dq kernel)."""
+
+    name = "dense_gqa_bwd"
+    kernel = "cpattn_chunk_bwd (bwd_dkdv_kernel + bwd_dq_kernel)"
+    launches_per_step = 4   # interval init, prep, dk/dv, dq
+
+    def __init__(self, device):
+        from context_attention_softmax_gb300 import cpattn_chunk_fwd
+        self.w = w = inputs.dense_gqa()
+        Tq, Hq, D = w.q.shape
+        qpos = w.causal_offset + np.arange(Tq)
+        pairs = int(np.minimum(qpos + 1, w.Tk).sum())
+        # the usual count: five 2*d products per permitted pair and head
+        # (S recomputed, dP, dV, dQ, dK)
+        self.work = 10.0 * D * pairs * Hq
+        self.n_rows = Tq
+        self.q, self.k, self.v = (t.to(device) for t in (w.q, w.k, w.v))
+        self.o, self.lse = cpattn_chunk_fwd(self.q, self.k, self.v, scale=w.scale, causal=True,
+                                            causal_offset=w.causal_offset)
+        rng = np.random.default_rng(7)
+        self.g_host = inputs.to_device_dtype(
+            (rng.standard_normal(tuple(self.o.shape)) * 0.5).astype(np.float32), "bf16")
+        self.g = self.g_host.to(device)
+        self.dq = torch.empty(self.q.shape, dtype=torch.float32, device=device)
+        self.dk = torch.empty(self.k.shape, dtype=torch.float32, device=device)
+        self.dv = torch.empty(self.v.shape, dtype=torch.float32, device=device)
+        self.ws = torch.empty(16 << 20, dtype=torch.uint8, device=device)
+        self.config = {"workload": "backward of the dense causal CP chunk: 2048 queries (causal_offset "
+                                   "4096) x 8192 keys, 16 q heads / 4 kv heads, d=128; bf16 q, k, v, "
+                                   "o, d_out, fp32 dq, dk, dv",
+                       "permitted_pairs_per_head": pairs,
+                       "flops_note": "10 d per permitted pair and head (5 products of 2 d)",
+                       "l2": L2_NOTE}
+
+    def device_inputs(self):
+        return [self.q, self.k, self.v, self.o, self.lse, self.g]
+
+    def step(self, q, k, v, o, lse, g):
+        from context_attention_softmax_gb300 import cpattn_chunk_bwd
+        w = self.w
+        cpattn_chunk_bwd(q, k, v, o, lse, g, scale=w.scale, causal=True,
+                         causal_offset=w.causal_offset, dq=self.dq, dk=self.dk, dv=self.dv,
+                         workspace=self.ws)
+
+    def outputs(self):
+        return [self.dq, self.dk, self.dv]
+
+    def oracle_sample(self, rows):
+        """The oracle backward of the query rows `rows` (their dq, and their
+        contribution to dk, dv)."""
+        import oracle as orc
+        w = self.w
+        if not hasattr(self, "_f64"):
+            self._f64 = (inputs.as_f64(w.q), inputs.as_f64(w.k), inputs.as_f64(w.v),
+                         inputs.as_f64(self.g_host))
+        q, k, v, g = self._f64
+        lay = orc.make_layout(len(rows), w.Tk, True, 0)
+        lay.qpos = w.causal_offset + np.asarray(rows)
+        lay.qseq = np.zeros(len(rows), dtype=np.int64)
+        orc.dense_attention_backward(q[rows], k, v, w.scale, lay, g[rows])
+        qpos = w.causal_offset + rows
+        return 10.0 * w.q.shape[2] * float(np.minimum(qpos + 1, w.Tk).sum()) * w.q.shape[1]
 
 
 class ZigzagRunner(Runner):
@@ -543,9 +610,10 @@ class MlaKvRunner(Runner):
 RUNNERS = {"dense_gqa": DenseRunner,
            "dense_gqa_4chunks": lambda dev: DenseRunner(dev, kv_chunks=True),
            "zigzag": ZigzagRunner, "dsa": DsaRunner, "moba": MobaRunner,
-           "dsa_indexer": IndexerRunner, "mla_v_up": MlaVUpRunner, "mla_kv": MlaKvRunner}
-ALL_ORDER = ["dense_gqa", "dense_gqa_4chunks", "zigzag", "dsa", "moba", "dsa_indexer", "mla_v_up",
-             "mla_kv"]
+           "dsa_indexer": IndexerRunner, "mla_v_up": MlaVUpRunner, "mla_kv": MlaKvRunner,
+           "dense_gqa_bwd": DenseBwdRunner}
+ALL_ORDER = ["dense_gqa", "dense_gqa_4chunks", "dense_gqa_bwd", "zigzag", "dsa", "moba",
+             "dsa_indexer", "mla_v_up", "mla_kv"]
 
 
 # ---------------------------------------------------------------------------

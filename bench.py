@@ -67,11 +67,16 @@ L2_NOTE = "flushed by a 256 MiB write before every timed step"
 # dominant kernel from one ncu capture (summarised under profiles/), valid
 # only while the kernel's sources hash to the value they had then.
 TRAFFIC = {
-    "dense_gqa": {"bytes": 21_066_496 + 0, "kernel": "dense_tc_kernel",
+    "dense_gqa": {"bytes": 21_195_008 + 0, "kernel": "dense_tc_kernel",
                   "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                  "sha": "710df07de8adbb71"},
+                  "sha": "e207fd27a5d08658"},
     "dsa": {"bytes": 662_182_656 + 505_942_016, "kernel": "dsa_attn_kernel",
             "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "1a2d63f8b3cc8586"},
+    "mla_kv": {"bytes": 250_570_240 + 2_629_161_472, "kernel": "mla_gemm_kernel",
+               "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "8dfc188bab9ff2ce"},
+    "dense_gqa_bwd": {"bytes": 29_677_568 + 153_600, "kernel": "bwd_dkdv_kernel",
+                      "sources": ["dense_bwd.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
+                      "sha": "4af28464f5940964"},
 }
 
 

@@ -123,7 +123,7 @@ __device__ __forceinline__ float kth_lower(uint32_t acc, int k, int n_cand) {
   float tv[KMAX];
 #pragma unroll
   for (int t = 0; t < KMAX; ++t) tv[t] = -CUDART_INF_F;
-#pragma unroll
+#pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t rr[32];
     tmem_ld32(acc + 32 * c, rr);
@@ -164,7 +164,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_init(&s.mu_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.q_full[i], 1);
-      mbar_init(&s.q_empty[i], 1);
+      mbar_init(&s.q_empty[i], 128);   // the selection group reads ||q|| from the tile
       mbar_init(&s.acc_full[i], 1);
       mbar_init(&s.acc_free[i], 128);
     }
@@ -245,7 +245,6 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           for (int kk = 0; kk < 8; ++kk)
             umma_ss_lo(d, qlo[st][kk >> 2] + (kk & 3) * 2, mlo[t][kk >> 2] + (kk & 3) * 2, idesc,
                        (t | kk) != 0);
-        umma_commit(&s.q_empty[st]);
         umma_commit(&s.acc_full[st]);
         const bool last_of_group = it + 1 >= i1 || (it + 1) / p.n_qtiles / group != g;
         if (last_of_group) umma_commit(&s.mu_empty);
@@ -277,21 +276,30 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       ok = ok && __all_sync(kFullMask, mbar_wait(&s.acc_full[st], (ti >> 1) & 1, abort_flag, lim));
       const int64_t qi = (int64_t)qt * GM + r;
       const bool valid = ok && qi < a.Tq;
-      const __nv_bfloat16* qrow = reinterpret_cast<const __nv_bfloat16*>(a.q) +
-                                  (valid ? qi : 0) * a.q_stride_t + (int64_t)h * a.q_stride_h;
+      // ||q||^2 of this row from the staged query tile (the MMA that read it
+      // is complete: acc_full); the tile is released for the tile after next
+      // once the whole group has read it.  Row r of a 64-channel box sits at
+      // r * 128 bytes, its 16-byte piece c at ((c ^ (r % 8)) * 16).
       float qss = 0.f;
-      if (valid) {
-#pragma unroll 8
-        for (int d8 = 0; d8 < GD / 8; ++d8) {
-          const uint4 w = *reinterpret_cast<const uint4*>(qrow + 8 * d8);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      if (ok) {
+        tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = __uint_as_float(ws[j] << 16), hi = __uint_as_float(ws[j] & 0xffff0000u);
-            qss = fmaf(lo, lo, fmaf(hi, hi, qss));
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint8_t* rowp = s.q[st][kb] + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 w = *reinterpret_cast<const uint4*>(rowp + ((c ^ (r & 7)) << 4));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = __uint_as_float(ws[j] << 16), hi = __uint_as_float(ws[j] & 0xffff0000u);
+              qss = fmaf(lo, lo, fmaf(hi, hi, qss));
+            }
           }
         }
+        mbar_arrive(&s.q_empty[st]);
       }
+      if (!valid) qss = 0.f;
       const float ge = gamma * sqrtf(qss);
       const int64_t own = valid ? query_pos(a, qi) / p.B : 0;
       const int n_cand = (int)max((int64_t)0, min((int64_t)p.n_blocks, own));
@@ -307,7 +315,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // lower bounds g_b - e_b written back in place; upper bounds are taken
         // as lower + 2 e_b, which rounding leaves above g_b + e_b by far less
         // than the bound's padding
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t rr[32];
           tmem_ld32(acc + 32 * c, rr);

@@ -458,12 +458,14 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         tc_fence_after();
         const uint32_t s_col = tmem + lane_base + kColS + (jt & 1) * BN;
         float sv[BN];
+        {   // the row's 128 scores in four loads and one wait
+          uint32_t rr[BN];
 #pragma unroll
-        for (int c4 = 0; c4 < BN / 32; ++c4) {
-          uint32_t rr[32];
-          tmem_ld32_sync(s_col + c4 * 32, rr);
+          for (int c4 = 0; c4 < BN / 32; ++c4)
+            tmem_ld32(s_col + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(rr + 32 * c4));
+          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sv[c4 * 32 + i] = __uint_as_float(rr[i]);
+          for (int i = 0; i < BN; ++i) sv[i] = __uint_as_float(rr[i]);
         }
         if (!(lo_c == 0 && hi_c == BN - 1)) {
 #pragma unroll

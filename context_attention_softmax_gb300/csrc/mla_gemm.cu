@@ -53,7 +53,7 @@ struct GemmParams {
   __nv_bfloat16* k_out; int64_t k_st, k_sh;         // materialised key [T, H, N + R]
   __nv_bfloat16* v_out; int64_t v_st, v_sh;         // materialised value [T, H, V]
   const __nv_bfloat16* k_shared; int64_t ks_st;     // [T, R]
-  int N, V, R;
+  int N, V, R, H;
   int32_t* dev_status;
   uint64_t limit;
 };
@@ -270,6 +270,212 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
   if (threadIdx.x == 0 && s.abort) report_status(p.dev_status, CPATTN_ERR_TIMEOUT);
 }
 
+// ---------------------------------------------------------------- K/V materialisation
+// The materialisation's A block (128 tokens x L <= 512 latent channels) is
+// reused by every 256-wide N tile of its row block, so a CTA keeps it in
+// shared memory (eight 16 KiB boxes) and streams only wkv_b through a
+// three-stage ring of 256 x 64 boxes.  Per tile that is 256 KiB of operands
+// for 33.5 MFLOP, against 256 KiB for 16.8 MFLOP with 128 x 128 tiles, so
+// the kernel is no longer bound by the L2-to-SM bandwidth.  CTAs take
+// contiguous runs of tiles in (row block, N tile) order, so a CTA loads a
+// new A block only when its run crosses a row block.
+constexpr int KN = 256;                       // N tile
+constexpr int kKvStages = 3;
+constexpr int kMaxKSteps = 8;                 // L <= 512
+constexpr uint32_t kKvABox = GM * GK * 2;     // 16 KiB
+constexpr uint32_t kKvBBox = KN * GK * 2;     // 32 KiB
+
+struct KvSmem {
+  uint8_t a[kMaxKSteps][kKvABox];
+  uint8_t b[kKvStages][kKvBBox];
+  uint64_t a_full, a_empty, b_full[kKvStages], b_empty[kKvStages];
+  uint64_t acc_full[2], acc_empty[2], drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kKvSmemBytes = sizeof(KvSmem) + 1024;
+static_assert(kKvSmemBytes <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  KvSmem& s = *reinterpret_cast<KvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                         ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &s.abort;
+  const uint64_t lim = p.limit;
+  // this CTA's run of tiles (row block major, N tile minor)
+  const int t0 = (int)((int64_t)blockIdx.x * p.n_total_tiles / gridDim.x);
+  const int t1 = (int)((int64_t)(blockIdx.x + 1) * p.n_total_tiles / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&s.a_full, 1);
+    mbar_init(&s.a_empty, 1);
+    for (int i = 0; i < kKvStages; ++i) {
+      mbar_init(&s.b_full[i], 1);
+      mbar_init(&s.b_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.acc_full[i], 1);
+      mbar_init(&s.acc_empty[i], 128);
+    }
+    mbar_init(&s.drain, 1);
+    s.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  int a_loads = 0, b_fills = 0;   // producer's counts, for the drain on abort
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int cur_mt = -1;
+      bool ok = true;
+      for (int tile = t0; tile < t1 && ok; ++tile) {
+        const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+        if (mt != cur_mt) {
+          // the previous row block's MMAs are done with the resident A
+          if (a_loads > 0 && !mbar_wait(&s.a_empty, (a_loads - 1) & 1, abort_flag, lim)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.a_full, (uint32_t)p.k_steps * kKvABox);
+          for (int ks = 0; ks < p.k_steps; ++ks)
+            tma_load_3d(s.a[ks], &tm_a, &s.a_full, ks * GK, 0, mt * GM);
+          ++a_loads;
+          cur_mt = mt;
+        }
+        for (int ks = 0; ks < p.k_steps; ++ks, ++b_fills) {
+          const int st = b_fills % kKvStages;
+          if (!mbar_wait(&s.b_empty[st], ((b_fills / kKvStages) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.b_full[st], kKvBBox);
+          tma_load_3d(s.b[st], &tm_b, &s.b_full[st], ks * GK, nt * KN, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(GM, KN, 0, 0);
+      int cur_mt = -1, n_a = 0, it = 0, ti = 0;
+      bool ok = true;
+      for (int tile = t0; tile < t1 && ok; ++tile, ++ti) {
+        const int mt = tile / p.n_tiles;
+        const int buf = ti & 1;
+        if (mt != cur_mt) {
+          if (!mbar_wait(&s.a_full, n_a & 1, abort_flag, lim)) { ok = false; break; }
+          ++n_a;
+          cur_mt = mt;
+        }
+        if (!mbar_wait(&s.acc_empty[buf], ((ti >> 1) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * KN);
+        for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
+          const int st = it % kKvStages;
+          if (!mbar_wait(&s.b_full[st], (it / kKvStages) & 1, abort_flag, lim)) { ok = false; break; }
+          tc_fence_after();
+          mma_stage<0>(d, desc_lo(smem_u32(s.a[ks]), 16), desc_lo(smem_u32(s.b[st]), 16), idesc, ks > 0);
+          umma_commit(&s.b_empty[st]);
+        }
+        if (!ok) break;
+        umma_commit(&s.acc_full[buf]);
+        // the last tile of this row block in the run: A may be replaced
+        if (tile + 1 >= t1 || (tile + 1) / p.n_tiles != mt) umma_commit(&s.a_empty);
+      }
+      umma_commit(&s.drain);
+      int no_abort = 0;
+      mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int r = (warp - 4) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const int per_head = p.N + p.V;
+    const int64_t n_rows = (int64_t)p.n_tiles * KN;   // padded N
+    int ti = 0;
+    for (int tile = t0; tile < t1; ++tile, ++ti) {
+      const int buf = ti & 1;
+      const bool ok = __all_sync(kFullMask, mbar_wait(&s.acc_full[buf], (ti >> 1) & 1, abort_flag, lim));
+      if (!ok) break;
+      tc_fence_after();
+      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      const int64_t t = (int64_t)mt * GM + r;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const int col = nt * KN + half * GN;
+        const int h = col / per_head;
+        const bool valid = h < p.H && t < p.M;
+        (void)n_rows;
+        const int part = col - h * per_head;
+        __nv_bfloat16* dst = part < p.N ? p.k_out + t * p.k_st + (int64_t)h * p.k_sh + part
+                                        : p.v_out + t * p.v_st + (int64_t)h * p.v_sh + (part - p.N);
+        const bool rope = valid && part < p.N && part + GN == p.N;
+        uint4 rope_v[8];
+        const uint4* rsrc = reinterpret_cast<const uint4*>(p.k_shared + (rope ? t : 0) * p.ks_st);
+        const int n_rope = rope ? p.R / 8 : 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < n_rope) rope_v[i] = __ldg(rsrc + i);
+#pragma unroll
+        for (int c4 = 0; c4 < GN / 32; ++c4) {
+          uint32_t acc[32];
+          tmem_ld32_wait(tmem + lane_base + (uint32_t)(buf * KN + half * GN + c4 * 32), acc);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 val;
+              val.x = pack2_bf16(__uint_as_float(acc[i + 0]), __uint_as_float(acc[i + 1]));
+              val.y = pack2_bf16(__uint_as_float(acc[i + 2]), __uint_as_float(acc[i + 3]));
+              val.z = pack2_bf16(__uint_as_float(acc[i + 4]), __uint_as_float(acc[i + 5]));
+              val.w = pack2_bf16(__uint_as_float(acc[i + 6]), __uint_as_float(acc[i + 7]));
+              *reinterpret_cast<uint4*>(dst + c4 * 32 + i) = val;
+            }
+          }
+        }
+        if (rope) {
+          uint4* kd = reinterpret_cast<uint4*>(p.k_out + t * p.k_st + (int64_t)h * p.k_sh + p.N);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < n_rope) kd[i] = rope_v[i];
+          for (int i0 = 8; i0 < n_rope; i0 += 8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i0 + i < n_rope) rope_v[i] = __ldg(rsrc + i0 + i);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (i0 + i < n_rope) kd[i0 + i] = rope_v[i];
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s.acc_empty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (s.abort && warp == 0 && lane == 0) {
+    // every role has stopped: let the copies in flight land (the last A load
+    // and at most the last kKvStages B fills; earlier ones were consumed)
+    int no_abort = 0;
+    if (a_loads > 0) mbar_wait(&s.a_full, (a_loads - 1) & 1, &no_abort, 200000000ull);
+    for (int j = max(0, b_fills - kKvStages); j < b_fills; ++j)
+      mbar_wait(&s.b_full[j % kKvStages], (j / kKvStages) & 1, &no_abort, 200000000ull);
+  }
+  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (threadIdx.x == 0 && s.abort) report_status(p.dev_status, CPATTN_ERR_TIMEOUT);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
@@ -329,20 +535,22 @@ cpattn_status mla_kv_impl(const void* kv_c, int64_t c_st, const void* k_shared, 
   if (T == 0) return CPATTN_OK;
   CUtensorMap ta, tb;
   const int64_t n_rows = (int64_t)H * (N + V);
+  const bool resident_a = L <= kMaxKSteps * GK;   // the A block fits shared memory
   const uint64_t ad[3] = {(uint64_t)L, 1, (uint64_t)T};
   const uint64_t as[2] = {(uint64_t)c_st * 2, (uint64_t)c_st * 2};
   const uint32_t ab[3] = {GK, 1, GM};
   const uint64_t bd[3] = {(uint64_t)L, (uint64_t)n_rows, 1};
   const uint64_t bs[2] = {(uint64_t)L * 2, (uint64_t)n_rows * L * 2};
-  const uint32_t bb[3] = {GK, GN, 1};
+  const uint32_t bb[3] = {GK, (uint32_t)(resident_a ? KN : GN), 1};
   if (!encode_bf16_3d(&ta, kv_c, ad, as, ab) || !encode_bf16_3d(&tb, wkv_b, bd, bs, bb))
     return report_error(CPATTN_ERR_INVALID_ARG,
                         "cpattn_mla_kv_materialise: a TMA descriptor cannot describe the operands");
   GemmParams p{};
   p.mode = kModeKv;
   p.M = T;
+  p.H = H;
   p.m_tiles = (T + GM - 1) / GM;
-  p.n_tiles = (int)(n_rows / GN);
+  p.n_tiles = resident_a ? (int)((n_rows + KN - 1) / KN) : (int)(n_rows / GN);
   p.batches = 1;
   p.k_steps = L / GK;
   p.n_total_tiles = p.m_tiles * p.n_tiles;
@@ -359,7 +567,18 @@ cpattn_status mla_kv_impl(const void* kv_c, int64_t c_st, const void* k_shared, 
   p.R = R;
   p.dev_status = dev_status;
   p.limit = wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : 2000000000ull;
-  const cudaError_t e = launch_gemm(p, ta, tb, false, stream);
+  cudaError_t e;
+  if (resident_a) {
+    e = ensure_smem_attr(reinterpret_cast<const void*>(mla_kv_kernel), (int)kKvSmemBytes);
+    if (e == cudaSuccess) {
+      const int n_sm = device_sm_count();
+      const int grid = p.n_total_tiles < n_sm ? p.n_total_tiles : n_sm;
+      mla_kv_kernel<<<grid, kGemmThreads, kKvSmemBytes, stream>>>(ta, tb, p);
+      e = cudaGetLastError();
+    }
+  } else {
+    e = launch_gemm(p, ta, tb, false, stream);
+  }
   if (e != cudaSuccess) return report_error(CPATTN_ERR_CUDA, cudaGetErrorString(e));
   return CPATTN_OK;
 }

@@ -71,6 +71,8 @@ def test_v_up_full_size_sampled():
     (300, 3, 128, 128, 128, 64),    # ragged rows, shared key appended to every head
     (200, 2, 512, 256, 128, 8),     # two key tiles per head, a narrow shared key
     (130, 2, 64, 128, 256, 0),      # no shared key, two value tiles per head
+    (100, 1, 128, 128, 256, 16),    # three 128-column halves: the last 256-wide tile half empty
+    (150, 2, 576, 128, 128, 64),    # latent wider than 512: the kernel without a resident A block
 ])
 def test_kv_materialise_small(T, H, L, N, V, R):
     w = inputs.mla_kv(seed=T + L, T=T, H=H, L=L, N=N, V=V, R=R)

@@ -35,7 +35,11 @@
 namespace cpattn {
 namespace {
 
-constexpr int kBwdThreads = 256;    // warp 0 TMA, 1 MMA, 3 tile list, 4-7 element work
+constexpr int kBwdThreads = 384;    // warp 0 TMA, 1 MMA, 3 tile list, 4-11 element work
+// Element warps 4..11: warp w works on TMEM lanes 32 (w % 4) .. + 31 (its rows)
+// and on columns [64 hc, 64 hc + 64) of them, hc = (w - 4) / 4, so each
+// sub-partition runs two element warps.
+constexpr int kElemThreads = 256;
 constexpr int kMaxQTiles = 8192;    // Tq <= 1 Mi tokens on this path
 
 struct BwdParams {
@@ -126,7 +130,7 @@ struct DkdvSmem {
   int abort;
   int n_live;
   int issued;                       // query-tile loads issued (for the drain on abort)
-  int4 qinfo[4][BM];                // per element warp: (lo, hi, lse2, D) of each query of the step
+  int4 qinfo[8][BM / 2];            // per element warp: (lo, hi, lse2, D) of its 64 queries
   uint16_t live_qt[kMaxQTiles];
 };
 constexpr size_t kDkdvSmem = sizeof(DkdvSmem) + 1024;
@@ -142,7 +146,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
                                              ~uintptr_t(1023));
   const cpattn_attn_args& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = blockIdx.x % p.n_ktiles, gkv = blockIdx.x / p.n_ktiles;
+  // Key tiles in ascending order, KV heads minor: under a causal mask the
+  // early key tiles meet the most query tiles, so the heaviest CTAs are
+  // launched first and the light ones fill in behind them.
+  const int kt = blockIdx.x / a.Hkv, gkv = blockIdx.x % a.Hkv;
   const int group = a.Hq / a.Hkv;
   volatile int* abort_flag = &s.abort;
   const uint64_t lim = wait_limit(a);
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
       mbar_init(&s.qg_empty[i], 1);
     }
     mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_full, 128);
+    mbar_init(&s.p_full, kElemThreads);
     mbar_init(&s.acc_done, 1);
     mbar_init(&s.drain, 1);
     s.abort = 0;
@@ -234,13 +241,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
         if (!mbar_wait(&s.p_full, it & 1, abort_flag, lim)) { ok = false; break; }
         tc_fence_after();
         const uint32_t q_mn = desc_lo(smem_u32(s.q[b]), kHalf), g_mn = desc_lo(smem_u32(s.g[b]), kHalf);
+        // P^T and dS^T of queries 0..63 sit at columns 0..31 of their
+        // regions, those of queries 64..127 at columns 64..95 (one half per
+        // element warpgroup); B rows 64.. start 4 K-steps (8 KiB) further on.
         if (it == 0) {
-          umma8_ts_mnmajor<0>(tmem + kColDV, tmem + kColS, g_mn, idesc_mn);    // dv  = P^T g
-          umma8_ts_mnmajor<0>(tmem + kColDK, tmem + kColDP, q_mn, idesc_mn);   // dk  = dS^T q
+          umma4_ts_mn<0>(tmem + kColDV, tmem + kColS, g_mn, idesc_mn);          // dv  = P^T g
+          umma4_ts_mn<0>(tmem + kColDK, tmem + kColDP, q_mn, idesc_mn);         // dk  = dS^T q
         } else {
-          umma8_ts_mnmajor<1>(tmem + kColDV, tmem + kColS, g_mn, idesc_mn);    // dv += P^T g
-          umma8_ts_mnmajor<1>(tmem + kColDK, tmem + kColDP, q_mn, idesc_mn);   // dk += dS^T q
+          umma4_ts_mn<1>(tmem + kColDV, tmem + kColS, g_mn, idesc_mn);          // dv += P^T g
+          umma4_ts_mn<1>(tmem + kColDK, tmem + kColDP, q_mn, idesc_mn);         // dk += dS^T q
         }
+        umma4_ts_mn<1>(tmem + kColDV, tmem + kColS + 64, g_mn + 512, idesc_mn);
+        umma4_ts_mn<1>(tmem + kColDK, tmem + kColDP + 64, q_mn + 512, idesc_mn);
         umma_commit(&s.qg_empty[b]);
       }
       if (ok) umma_commit(&s.acc_done);
@@ -250,23 +262,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ P^T, dS^T; epilogue
-    const int r = (warp - 4) * 32 + lane;                 // key row = TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const int ew = warp - 4, hc = ew >> 2;                // column half of this warp
+    const int r = (ew & 3) * 32 + lane;                   // key row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((ew & 3) * 32) << 16;
     const int64_t jrow = (int64_t)kt * BN + r;
     const bool key_ok = jrow < a.Tk;
     const int kpos = key_ok ? (int)logical_pos(a.kv_chunk_map, a.chunk_len, jrow) : INT_MIN;
     const float sl2 = a.scale * 1.4426950408889634f;
-    int4* qinfo = s.qinfo[warp - 4];                      // this warp's own copy
+    int4* qinfo = s.qinfo[ew];                            // this warp's own copy
     bool ok = true;
     for (int it = 0; it < n_steps; ++it) {
       const int h = gkv * group + it / s.n_live, qt = s.live_qt[it % s.n_live];
-      // every warp stages the step's 128 query statistics in its own copy
-      // (lane l: queries l, l+32, l+64, l+96), so no barrier spans warps
+      // every warp stages the statistics of its 64 queries in its own copy
+      // (lane l: queries 64 hc + l and 64 hc + l + 32), so no barrier spans warps
       __syncwarp();
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 2; ++u) {
         const int c = lane + 32 * u;
-        const int64_t qi = (int64_t)qt * BM + c;
+        const int64_t qi = (int64_t)qt * BM + 64 * hc + c;
         int lo = INT_MAX, hi = INT_MIN;
         float l2 = -CUDART_INF_F, dd = 0.f;
         if (qi < a.Tq) {
@@ -286,7 +299,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int c4 = 0; c4 < BM / 32; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c4 = 2 * hc + c2;                       // 32-column chunk of the row
         uint32_t sr[32], dr[32];
         tmem_ld32(tmem + lane_base + kColS + 32 * c4, sr);
         tmem_ld32(tmem + lane_base + kColDP + 32 * c4, dr);
@@ -297,7 +311,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
           float pp[2], ds[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int4 qc = qinfo[32 * c4 + c + e];
+            const int4 qc = qinfo[32 * c2 + c + e];
             const bool allowed = kpos >= qc.x && kpos <= qc.y;
             const float x = fmaf(__uint_as_float(sr[c + e]), sl2, -__int_as_float(qc.z));
             pp[e] = allowed ? ex2_approx(x) : 0.f;
@@ -306,21 +320,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
           pk[c >> 1] = pack_bf16(pp[0], pp[1]);
           dk2[c >> 1] = pack_bf16(ds[0], ds[1]);
         }
-        tmem_st16(tmem + lane_base + kColS + 16 * c4, pk);
-        tmem_st16(tmem + lane_base + kColDP + 16 * c4, dk2);
+        // packed into this half's own columns, which it has already read:
+        // queries 64 hc .. 64 hc + 63 at columns 64 hc .. 64 hc + 31
+        tmem_st16(tmem + lane_base + kColS + 64 * hc + 16 * c2, pk);
+        tmem_st16(tmem + lane_base + kColDP + 64 * hc + 16 * c2, dk2);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&s.p_full);
     }
-    // epilogue: dv and scale * dk for this CTA's key rows (zero if no step)
+    // epilogue: dv and scale * dk for this CTA's key rows (zero if no step);
+    // this warp writes channels [64 hc, 64 hc + 64) of its rows
     const bool have = ok && n_steps > 0 &&
                       __all_sync(kFullMask, mbar_wait(&s.acc_done, 0, abort_flag, lim));
     if (have) tc_fence_after();
     float* dvrow = p.dv + jrow * p.dv_st + (int64_t)gkv * p.dv_sh;
     float* dkrow = p.dk + jrow * p.dk_st + (int64_t)gkv * p.dk_sh;
 #pragma unroll 1
-    for (int c4 = 0; c4 < HD / 32; ++c4) {
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int c4 = 2 * hc + c2;
       uint32_t vv[32], kk[32];
       if (have) {
         tmem_ld32(tmem + lane_base + kColDV + 32 * c4, vv);
@@ -385,7 +403,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
                                          ~uintptr_t(1023));
   const cpattn_attn_args& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x % p.n_qtiles, h = blockIdx.x / p.n_qtiles;
+  // Query tiles in descending order, heads minor: later query tiles see the
+  // most key tiles under a causal mask, so they are launched first.
+  const int qt = p.n_qtiles - 1 - (int)(blockIdx.x / a.Hq), h = blockIdx.x % a.Hq;
   const int gkv = h / (a.Hq / a.Hkv);
   volatile int* abort_flag = &s.abort;
   const uint64_t lim = wait_limit(a);
@@ -397,7 +417,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
       mbar_init(&s.kv_empty[i], 1);
     }
     mbar_init(&s.s_full, 1);
-    mbar_init(&s.p_full, 128);
+    mbar_init(&s.p_full, kElemThreads);
     mbar_init(&s.acc_done, 1);
     mbar_init(&s.drain, 1);
     s.abort = 0;
@@ -476,8 +496,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
         if (!mbar_wait(&s.p_full, it & 1, abort_flag, lim)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_mn = desc_lo(smem_u32(s.k[b]), kHalf);
-        if (it == 0) umma8_ts_mnmajor<0>(tmem + kColDQ, tmem + kColS, k_mn, idesc_mn);   // dq  = dS k
-        else umma8_ts_mnmajor<1>(tmem + kColDQ, tmem + kColS, k_mn, idesc_mn);           // dq += dS k
+        // dS of keys 0..63 at columns 0..31, of keys 64..127 at columns 64..95
+        if (it == 0) umma4_ts_mn<0>(tmem + kColDQ, tmem + kColS, k_mn, idesc_mn);   // dq  = dS k
+        else umma4_ts_mn<1>(tmem + kColDQ, tmem + kColS, k_mn, idesc_mn);           // dq += dS k
+        umma4_ts_mn<1>(tmem + kColDQ, tmem + kColS + 64, k_mn + 512, idesc_mn);
         umma_commit(&s.kv_empty[b]);
       }
       if (ok) umma_commit(&s.acc_done);
@@ -487,8 +509,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ dS; epilogue
-    const int r = (warp - 4) * 32 + lane;                 // query row = TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const int ew = warp - 4, hc = ew >> 2;                // column half of this warp
+    const int r = (ew & 3) * 32 + lane;                   // query row = TMEM lane
+    const uint32_t lane_base = (uint32_t)((ew & 3) * 32) << 16;
     const int64_t qi = (int64_t)qt * BM + r;
     KeyInterval iv{1, 0};
     float l2 = -CUDART_INF_F, dd = 0.f;
@@ -513,7 +536,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int c4 = 0; c4 < BN / 32; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c4 = 2 * hc + c2;                       // 32-key chunk of the row
         uint32_t sr[32], dr[32];
         tmem_ld32(tmem + lane_base + kColS + 32 * c4, sr);
         tmem_ld32(tmem + lane_base + kColDP + 32 * c4, dr);
@@ -531,7 +555,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
           }
           pk[c >> 1] = pack_bf16(ds[0], ds[1]);
         }
-        tmem_st16(tmem + lane_base + kColS + 16 * c4, pk);
+        tmem_st16(tmem + lane_base + kColS + 64 * hc + 16 * c2, pk);   // own columns, already read
       }
       tmem_wait_st();
       tc_fence_before();
@@ -542,7 +566,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
     if (have) tc_fence_after();
     float* dqrow = p.dq + qi * p.dq_st + (int64_t)h * p.dq_sh;
 #pragma unroll 1
-    for (int c4 = 0; c4 < HD / 32; ++c4) {
+    for (int c2 = 0; c2 < 2; ++c2) {                      // channels [64 hc, 64 hc + 64)
+      const int c4 = 2 * hc + c2;
       uint32_t qq[32];
       if (have) {
         tmem_ld32(tmem + lane_base + kColDQ + 32 * c4, qq);

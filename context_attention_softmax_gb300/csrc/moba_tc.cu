@@ -6,12 +6,15 @@
 // once per (query, head); grouping by block reads each block's keys once per
 // 128 selecting queries instead:
 //
-//   1. moba_count_kernel   - count the selections of every (head, block);
-//                            empty slots get LSE = -inf straight away.
+//   1. moba_count_head_kernel - count the selections of every (head, block)
+//                            in shared-memory histograms (one head, 512
+//                            queries per CTA); empty slots get LSE = -inf
+//                            straight away.
 //   2. moba_scan_kernel    - exclusive scan of the counts into list offsets
 //                            and a list of work units: (head, block, first
 //                            list entry, up to 128 entries).
-//   3. moba_scatter_kernel - place every (query, slot) into its block's list.
+//   3. moba_scatter_head_kernel - place every (query, slot) into its block's
+//                            list (one reservation per bin and CTA).
 //   4. moba_attn_kernel    - persistent tcgen05 kernel: per unit, gather the
 //                            unit's 128 query rows, attend to the
 //                            block's keys (128-key tiles, permitted relation
@@ -192,6 +195,71 @@ __global__ void moba_scatter_kernel(const int32_t* __restrict__ sel, int64_t Tq,
   lists[offsets[hb] + pos] = (int32_t)(q * S + s);
 }
 
+
+// The same count and scatter with shared-memory histograms: a block takes
+// one head and kCountQ queries, counts its (head, block) bins in shared
+// memory and touches each global counter or cursor once per bin, instead of
+// once per selection.  The list order inside a bin follows the blocks'
+// reservations; each (query, slot) result does not depend on it.
+constexpr int kCountQ = 512;
+constexpr int kMaxSmemBins = 6144;   // 2 x 24 KiB of bins
+
+__global__ void moba_count_head_kernel(const int32_t* __restrict__ sel, int64_t Tq, int H, int S,
+                                       int index_heads, int B, int Tk, int NB, int32_t* counts,
+                                       float* part_lse, int32_t* dev_status) {
+  extern __shared__ int32_t hist[];
+  const int h = blockIdx.y;
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) hist[b] = 0;
+  __syncthreads();
+  const int64_t q0 = (int64_t)blockIdx.x * kCountQ;
+  const int n = (int)min((int64_t)kCountQ, Tq - q0) * S;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int64_t q = q0 + e / S;
+    const int s = e % S;
+    const int32_t b = sel_at(sel, q, h, s, H, index_heads, S);
+    if (b == -1 || b < -1 || (int64_t)b * B >= Tk) {
+      if (b != -1) report_status(dev_status, CPATTN_ERR_BAD_INDEX);
+      part_lse[((int64_t)s * Tq + q) * H + h] = -CUDART_INF_F;
+      continue;
+    }
+    atomicAdd(&hist[b], 1);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < NB; b += blockDim.x)
+    if (hist[b] != 0) atomicAdd(counts + (int64_t)h * NB + b, hist[b]);
+}
+
+__global__ void moba_scatter_head_kernel(const int32_t* __restrict__ sel, int64_t Tq, int H, int S,
+                                         int index_heads, int B, int Tk, int NB,
+                                         const int32_t* offsets, int32_t* cursors, int32_t* lists) {
+  extern __shared__ int32_t sm[];
+  int32_t* hist = sm;        // [NB] this block's count, then its running rank
+  int32_t* base = sm + NB;   // [NB] this block's reserved start in each list
+  const int h = blockIdx.y;
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) hist[b] = 0;
+  __syncthreads();
+  const int64_t q0 = (int64_t)blockIdx.x * kCountQ;
+  const int n = (int)min((int64_t)kCountQ, Tq - q0) * S;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int32_t b = sel_at(sel, q0 + e / S, h, e % S, H, index_heads, S);
+    if (b >= 0 && (int64_t)b * B < Tk) atomicAdd(&hist[b], 1);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) {
+    const int c = hist[b];
+    base[b] = c != 0 ? offsets[(int64_t)h * NB + b] + atomicAdd(cursors + (int64_t)h * NB + b, c) : 0;
+    hist[b] = 0;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < n; e += blockDim.x) {
+    const int64_t q = q0 + e / S;
+    const int s = e % S;
+    const int32_t b = sel_at(sel, q, h, s, H, index_heads, S);
+    if (b < 0 || (int64_t)b * B >= Tk) continue;
+    const int li = atomicAdd(&hist[b], 1);
+    lists[base[b] + li] = (int32_t)(q * S + s);
+  }
+}
 
 struct MobaParams {
   cpattn_attn_args a;
@@ -633,13 +701,26 @@ cudaError_t launch_moba_tc(const cpattn_attn_args& a, const int32_t* sel, int32_
   if (e != cudaSuccess) return e;
   const int64_t n = d.entries;
   const unsigned blocks = (unsigned)((n + 255) / 256);
-  moba_count_kernel<<<blocks, 256, 0, stream>>>(sel, d.Tq, (int)d.H, slots, index_heads, block_size,
-                                                a.Tk, (int)d.NB, w.counts, w.part_lse, a.dev_status);
+  const bool smem_bins = d.NB <= kMaxSmemBins && d.H <= 65535;
+  const dim3 hgrid((unsigned)((d.Tq + kCountQ - 1) / kCountQ), (unsigned)d.H);
+  if (smem_bins)
+    moba_count_head_kernel<<<hgrid, 256, (size_t)d.NB * 4, stream>>>(
+        sel, d.Tq, (int)d.H, slots, index_heads, block_size, a.Tk, (int)d.NB, w.counts, w.part_lse,
+        a.dev_status);
+  else
+    moba_count_kernel<<<blocks, 256, 0, stream>>>(sel, d.Tq, (int)d.H, slots, index_heads,
+                                                  block_size, a.Tk, (int)d.NB, w.counts, w.part_lse,
+                                                  a.dev_status);
   moba_scan_kernel<<<1, 1024, 0, stream>>>(nhb, (int)d.NB, w.counts, w.cursors, w.offsets, w.units,
                                            w.n_units);
-  moba_scatter_kernel<<<blocks, 256, 0, stream>>>(sel, d.Tq, (int)d.H, slots, index_heads,
-                                                  block_size, a.Tk, (int)d.NB, w.offsets, w.cursors,
-                                                  w.lists);
+  if (smem_bins)
+    moba_scatter_head_kernel<<<hgrid, 256, (size_t)d.NB * 8, stream>>>(
+        sel, d.Tq, (int)d.H, slots, index_heads, block_size, a.Tk, (int)d.NB, w.offsets, w.cursors,
+        w.lists);
+  else
+    moba_scatter_kernel<<<blocks, 256, 0, stream>>>(sel, d.Tq, (int)d.H, slots, index_heads,
+                                                    block_size, a.Tk, (int)d.NB, w.offsets,
+                                                    w.cursors, w.lists);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

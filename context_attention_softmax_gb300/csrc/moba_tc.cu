@@ -381,9 +381,23 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     if (lane == 0) {
       int jt = 0, kn = 0, vn = 0;
       bool ok = true;
+      auto prefetch_unit = [&](int uu) {   // the unit's K and V tiles into L2
+        if (uu >= n_units) return;
+        const int4 un2 = p.units[uu];
+        const int g2 = un2.x / group, T2 = unit_tiles(p, un2.y);
+        for (int t = 0; t < T2; ++t)
+          for (int x = 0; x < 2; ++x) {
+            tma_prefetch_l2_3d(&tm_k, 64 * x, g2, un2.y * p.B + t * BN);
+            tma_prefetch_l2_3d(&tm_v, 64 * x, g2, un2.y * p.B + t * BN);
+          }
+      };
+      prefetch_unit(blockIdx.x);
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int4 un = p.units[u];
         const int g = un.x / group, T = unit_tiles(p, un.y);
+        // this CTA's next unit: its K/V stream from HBM into L2 while this
+        // unit runs, so the stage loads that follow hit L2
+        prefetch_unit(u + gridDim.x);
         for (int t = 0; t < T; ++t, ++jt) {
           const int st = jt % NS;
           const uint32_t ph = (jt / NS) & 1;
@@ -431,6 +445,17 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           const uint32_t dst = dst0 + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4);
           asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + 8 * c)
                        : "memory");
+        }
+      }
+      // the next unit's query rows into L2 while this unit's copies land
+      if (u + gridDim.x < n_units) {
+        const int4 nx = p.units[u + gridDim.x];
+        for (int rr = t; rr < nx.w; rr += 64) {
+          const int64_t q = __ldg(p.lists + nx.z + rr) / p.S;
+          const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                     q * a.q_stride_t + (int64_t)nx.x * a.q_stride_h;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 64));
         }
       }
       asm volatile("cp.async.wait_all;" ::: "memory");

@@ -15,14 +15,12 @@
 //                            list entry, up to 128 entries).
 //   3. moba_scatter_head_kernel - place every (query, slot) into its block's
 //                            list (one reservation per bin and CTA).
-//   4. moba_attn_kernel    - persistent tcgen05 kernel: per unit (up to 256
-//                            selections of one (head, block), as two
-//                            128-row blocks that ping-pong on the tensor
-//                            core), gather the query rows, attend to the
+//   4. moba_attn_kernel    - persistent tcgen05 kernel: per unit, gather the
+//                            unit's 128 query rows, attend to the
 //                            block's keys (128-key tiles, permitted relation
 //                            re-applied so the own block is causal), and
 //                            write the finalised summary (O_c, LSE_c) of
-//                            each (query, head, slot).
+//                            that (query, head, slot).
 //   5. the LSE merge (lse_merge.cu) folds the slots of every (query, head)
 //      by rescaling to the larger max ("Context parallel attention: exchange
 //      keys and merge softmax globally", para 3-4).
@@ -43,17 +41,16 @@ namespace {
 using namespace sm100;
 
 constexpr int BM = 128, BN = 128, HD = 128;
-constexpr int kUnitRows = 2 * BM;   // a unit: up to two 128-row blocks of one (head, key block)
 constexpr int NS = 2;
 constexpr int kThreads = 384;
-// Register split at a launch budget of 168 x 384: the control warpgroup
-// (producer, MMA issuer, gather) 64, the two softmax warpgroups 216.
-constexpr uint32_t kRegsControl = 64, kRegsSoftmax = 216;
-static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 168 * kThreads, "register split");
+// Register split at a launch budget of 168 x 384: control warps 64, softmax
+// warps 216, epilogue warps 80.
+constexpr uint32_t kRegsControl = 64, kRegsSoftmax = 216, kRegsEpilogue = 80;
+static_assert(128 * (kRegsControl + kRegsSoftmax + kRegsEpilogue) <= 168 * kThreads, "register split");
 constexpr uint32_t kTileBytes = BN * HD * 2;   // 32 KiB
 constexpr uint32_t kHalf = 16384;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;     // S_A, S_B at 0 / 128; O_A, O_B at 256 / 384
+constexpr uint32_t kColS = 0, kColO = 256;     // S double buffer at 0 / 128, O double buffer at 256 / 384
 constexpr float kRescaleThreshold = 8.f;
 
 struct MobaWs {
@@ -80,7 +77,7 @@ Dims moba_dims(const cpattn_attn_args& a, int32_t slots, int32_t block_size) {
   d.S = slots;
   d.NB = (a.Tk + block_size - 1) / block_size;
   d.entries = d.Tq * d.H * d.S;
-  d.max_units = d.entries / kUnitRows + d.H * d.NB + 1;
+  d.max_units = d.entries / BM + d.H * d.NB + 1;
   return d;
 }
 
@@ -132,7 +129,7 @@ __global__ void moba_count_kernel(const int32_t* __restrict__ sel, int64_t Tq, i
 }
 
 // One CTA of 1024 threads: offsets = exclusive scan of counts; units: every
-// list cut into chunks of up to kUnitRows entries; cursors reset to 0.
+// list cut into chunks of up to 128 entries; cursors reset to 0.
 __global__ void __launch_bounds__(1024) moba_scan_kernel(int n, int NB, const int32_t* counts,
                                                           int32_t* cursors, int32_t* offsets,
                                                           int4* units, int32_t* n_units) {
@@ -144,7 +141,7 @@ __global__ void __launch_bounds__(1024) moba_scan_kernel(int n, int NB, const in
   for (int base = 0; base < n; base += 1024) {
     const int i = base + t;
     const int c = i < n ? counts[i] : 0;
-    const int u = (c + kUnitRows - 1) / kUnitRows;
+    const int u = (c + BM - 1) / BM;
     int ic = c, iu = u;   // inclusive warp scans
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -170,7 +167,7 @@ __global__ void __launch_bounds__(1024) moba_scan_kernel(int n, int NB, const in
       offsets[i] = ec;
       cursors[i] = 0;
       for (int k = 0; k < u; ++k)
-        units[eu + k] = make_int4(i / NB, i % NB, ec + k * kUnitRows, min(kUnitRows, c - k * kUnitRows));
+        units[eu + k] = make_int4(i / NB, i % NB, ec + k * BM, min(BM, c - k * BM));
     }
     __syncthreads();
     if (t == 1023) { carry_c += warp_c[31]; carry_u += warp_u[31]; }
@@ -277,16 +274,16 @@ struct MobaParams {
 };
 
 struct MSmem {
-  uint8_t q[2][kTileBytes];        // the unit's two query blocks
+  uint8_t q[2][kTileBytes];
   uint8_t k[NS][kTileBytes];
   uint8_t v[NS][kTileBytes];
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
-  uint64_t s_full[2], p_full[2], o_ready[2];
-  uint64_t drain;
+  uint64_t s_full[2], p_full[2];
+  uint64_t pv_done, o_full[2], o_free[2], st_full[2], drain;
+  float4 stats[2][BM];             // (m, l, -, -) of each row at the end of a unit
   uint32_t tmem_base;
   int abort;
-  int k_issued, v_issued;          // producer's counts, for the drain on abort
 };
 constexpr size_t kMSmemBytes = sizeof(MSmem) + 1024;
 
@@ -316,19 +313,13 @@ __device__ __forceinline__ int unit_tiles(const MobaParams& p, int b) {
   return (keys + BN - 1) / BN;
 }
 
-// A unit is up to 256 selections of one (head, key block): block A = its
-// first 128 rows, block B = the rest (absent when the unit has <= 128).
-// The two blocks read the same K/V tiles and ping-pong on the tensor core:
-//   S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ...
-// so each softmax warpgroup has the other block's MMAs to hide behind.
-// TMEM: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512); P_X is
-// written over S_X.  Roles (384 threads): warp 0 K/V TMA producer, warp 1
-// MMA issuer + TMEM owner, warps 2-3 gather the unit's query rows
-// (cp.async), warps 4-7 / 8-11 softmax and epilogue of blocks A / B (row =
-// TMEM lane).  A block's epilogue (its rows' finalised summaries from O_X)
-// runs before it arrives on p_full for the next unit's first tile, which the
-// PV that overwrites O_X waits for.  Units are taken in a fixed stride by
-// persistent CTAs; all roles walk the same sequence.
+// Roles (256 threads): warp 0 K/V TMA producer, warp 1 MMA issuer + TMEM
+// owner, warps 2-3 gather the unit's query rows (cp.async),
+// warps 4-7 softmax + epilogue (row = TMEM lane).  Units are taken in a
+// fixed stride (blockIdx.x, + gridDim.x, ...); all roles walk the same
+// sequence, with a global tile counter jt across units.  S is double
+// buffered in TMEM, so S(jt+1) runs while softmax(jt) does; P(jt) goes over
+// S(jt); O is reused across units once the previous epilogue released it.
 __global__ void __launch_bounds__(kThreads, 1)
 moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const MobaParams p) {
@@ -343,22 +334,26 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   const int group = a.Hq / a.Hkv;
 
   if (threadIdx.x == 0) {
-    mbar_init(&s.q_full, 64);
-    mbar_init(&s.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.q_full[i], 64);
+      mbar_init(&s.q_empty[i], 1);
+      mbar_init(&s.s_full[i], 1);
+      mbar_init(&s.p_full[i], 128);
+    }
     for (int i = 0; i < NS; ++i) {
       mbar_init(&s.k_full[i], 1);
       mbar_init(&s.k_empty[i], 1);
       mbar_init(&s.v_full[i], 1);
       mbar_init(&s.v_empty[i], 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&s.s_full[x], 1);
-      mbar_init(&s.p_full[x], 128);
-      mbar_init(&s.o_ready[x], 1);
+    mbar_init(&s.pv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.o_full[i], 1);
+      mbar_init(&s.o_free[i], 128);
+      mbar_init(&s.st_full[i], 128);
     }
     mbar_init(&s.drain, 1);
     s.abort = 0;
-    s.k_issued = s.v_issued = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -379,25 +374,11 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
   if (warp == 0) {
     // ------------------------------------------------------------ K/V producer
     if (lane == 0) {
-      int jt = 0, kn = 0, vn = 0;
+      int jt = 0;
       bool ok = true;
-      auto prefetch_unit = [&](int uu) {   // the unit's K and V tiles into L2
-        if (uu >= n_units) return;
-        const int4 un2 = p.units[uu];
-        const int g2 = un2.x / group, T2 = unit_tiles(p, un2.y);
-        for (int t = 0; t < T2; ++t)
-          for (int x = 0; x < 2; ++x) {
-            tma_prefetch_l2_3d(&tm_k, 64 * x, g2, un2.y * p.B + t * BN);
-            tma_prefetch_l2_3d(&tm_v, 64 * x, g2, un2.y * p.B + t * BN);
-          }
-      };
-      prefetch_unit(blockIdx.x);
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const int4 un = p.units[u];
         const int g = un.x / group, T = unit_tiles(p, un.y);
-        // this CTA's next unit: its K/V stream from HBM into L2 while this
-        // unit runs, so the stage loads that follow hit L2
-        prefetch_unit(u + gridDim.x);
         for (int t = 0; t < T; ++t, ++jt) {
           const int st = jt % NS;
           const uint32_t ph = (jt / NS) & 1;
@@ -406,40 +387,43 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           mbar_arrive_expect_tx(&s.k_full[st], kTileBytes);
           tma_load_3d(s.k[st], &tm_k, &s.k_full[st], 0, g, row0);
           tma_load_3d(s.k[st] + kHalf, &tm_k, &s.k_full[st], 64, g, row0);
-          ++kn;
           if (!mbar_wait(&s.v_empty[st], ph ^ 1, abort_flag, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.v_full[st], kTileBytes);
           tma_load_3d(s.v[st], &tm_v, &s.v_full[st], 0, g, row0);
           tma_load_3d(s.v[st] + kHalf, &tm_v, &s.v_full[st], 64, g, row0);
-          ++vn;
         }
       }
-      s.k_issued = kn;
-      s.v_issued = vn;
+      if (!ok) {  // let copies in flight land
+        int no_abort = 0;
+        for (int j = max(0, jt - NS); j <= jt; ++j) {
+          mbar_wait(&s.k_full[j % NS], (j / NS) & 1, &no_abort, 200000000ull);
+          mbar_wait(&s.v_full[j % NS], (j / NS) & 1, &no_abort, 200000000ull);
+        }
+      }
     }
   } else if (warp == 2 || warp == 3) {
     // ------------------------------------------------------------ query-row gather
-    // 64 threads, rows t, t + 64, t + 128, t + 192 of the unit (the last two
-    // only when block B is present); each row's 16 chunks of 16 bytes go to
+    // 64 threads, rows t and t + 64; each row's 16 chunks of 16 bytes go to
     // the 128-byte-swizzled K-major layout (chunk c of row r of a 64-column
     // box at r * 128 + ((c ^ (r % 8)) * 16)); cp.async, then a proxy fence
-    // so the tensor core sees the rows.  Rows past the unit's count repeat
-    // its first entry (masked later).
+    // so the tensor core sees the rows.
     const int t = threadIdx.x - 64;
     int ui = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
       const int4 un = p.units[u];
-      ok = __all_sync(kFullMask, mbar_wait(&s.q_empty, (ui & 1) ^ 1, abort_flag, lim));
+      const int qb = ui & 1;
+      ok = __all_sync(kFullMask, mbar_wait(&s.q_empty[qb], ((ui >> 1) & 1) ^ 1, abort_flag, lim));
       if (!ok) break;
-      const int n_rows = un.w > BM ? kUnitRows : BM;
-      for (int rr = t; rr < n_rows; rr += 64) {
-        const int32_t e = __ldg(p.lists + un.z + (rr < un.w ? rr : 0));
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int r = t + 64 * k;
+        // rows past the unit's count repeat its first entry (masked later)
+        const int32_t e = __ldg(p.lists + un.z + (r < un.w ? r : 0));
         const int64_t q = e / p.S;
         const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(a.q) + q * a.q_stride_t +
                                    (int64_t)un.x * a.q_stride_h;
-        const int r = rr & (BM - 1);
-        const uint32_t dst0 = smem_u32(s.q[rr >> 7]) + r * 128;
+        const uint32_t dst0 = smem_u32(s.q[qb]) + r * 128;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           const uint32_t dst = dst0 + (c >> 3) * kHalf + (((c & 7) ^ (r & 7)) << 4);
@@ -447,111 +431,89 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
                        : "memory");
         }
       }
-      // the next unit's query rows into L2 while this unit's copies land
-      if (u + gridDim.x < n_units) {
-        const int4 nx = p.units[u + gridDim.x];
-        for (int rr = t; rr < nx.w; rr += 64) {
-          const int64_t q = __ldg(p.lists + nx.z + rr) / p.S;
-          const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(a.q) +
-                                     q * a.q_stride_t + (int64_t)nx.x * a.q_stride_h;
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 64));
-        }
-      }
       asm volatile("cp.async.wait_all;" ::: "memory");
       fence_proxy_async_smem();
-      mbar_arrive(&s.q_full);
+      mbar_arrive(&s.q_full[qb]);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);
-      const uint32_t q_lo[2] = {desc_lo(smem_u32(s.q[0]), 16), desc_lo(smem_u32(s.q[1]), 16)};
+      const uint32_t q_lo0 = desc_lo(smem_u32(s.q[0]), 16), q_lo1 = desc_lo(smem_u32(s.q[1]), 16);
       const uint32_t k_lo0 = desc_lo(smem_u32(s.k[0]), 16), k_lo1 = desc_lo(smem_u32(s.k[1]), 16);
       const uint32_t v_lo0 = desc_lo(smem_u32(s.v[0]), kHalf), v_lo1 = desc_lo(smem_u32(s.v[1]), kHalf);
-      int jt = 0, ui = 0, c0 = 0, c1 = 0;   // tiles so far; per-block S/P events so far
+      int jt = 0, ui = 0;
       bool ok = true;
+      // the previous tile, whose PV is still to be issued
+      int prev = -1, prev_first = 0, prev_last = 0, prev_ui = 0;
+      auto issue_pv = [&]() -> bool {
+        const int j = prev;
+        if (!mbar_wait(&s.p_full[j & 1], (j >> 1) & 1, abort_flag, lim) ||
+            !mbar_wait(&s.v_full[j % NS], (j / NS) & 1, abort_flag, lim)) return false;
+        // O of unit u lives in buffer u & 1; its first PV waits until the
+        // epilogue has read unit u - 2 out of that buffer
+        const int ob = prev_ui & 1;
+        if (prev_first && prev_ui >= 2 &&
+            !mbar_wait(&s.o_free[ob], ((prev_ui - 2) >> 1) & 1, abort_flag, lim)) return false;
+        tc_fence_after();
+        const uint32_t vb = (j % NS) ? v_lo1 : v_lo0;
+        const uint32_t pa = tmem + kColS + (j & 1) * BN;
+        const uint32_t od = tmem + kColO + ob * HD;
+        if (prev_first) umma8_ts_mnmajor<0>(od, pa, vb, idesc_pv);
+        else umma8_ts_mnmajor<1>(od, pa, vb, idesc_pv);
+        umma_commit(&s.v_empty[j % NS]);
+        umma_commit(&s.pv_done);
+        if (prev_last) umma_commit(&s.o_full[ob]);
+        return true;
+      };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
         const int4 un = p.units[u];
-        const int T = unit_tiles(p, un.y);
-        const int nb = un.w > BM ? 2 : 1;   // blocks present
-        if (!mbar_wait(&s.q_full, ui & 1, abort_flag, lim) ||
-            !mbar_wait(&s.k_full[jt % NS], (jt / NS) & 1, abort_flag, lim)) { ok = false; break; }
-        tc_fence_after();
-        for (int x = 0; x < nb; ++x) {
-          umma8_ss_kmajor(tmem + kColS + x * BN, q_lo[x], (jt % NS) ? k_lo1 : k_lo0, idesc_qk);
-          umma_commit(&s.s_full[x]);
+        const int T = unit_tiles(p, un.y), qb = ui & 1;
+        if (!mbar_wait(&s.q_full[qb], (ui >> 1) & 1, abort_flag, lim)) { ok = false; break; }
+        for (int t = 0; t < T; ++t, ++jt) {
+          const int st = jt % NS;
+          if (!mbar_wait(&s.k_full[st], (jt / NS) & 1, abort_flag, lim)) { ok = false; break; }
+          tc_fence_after();
+          umma8_ss_kmajor(tmem + kColS + (jt & 1) * BN, qb ? q_lo1 : q_lo0, st ? k_lo1 : k_lo0,
+                          idesc_qk);
+          umma_commit(&s.s_full[jt & 1]);
+          umma_commit(&s.k_empty[st]);
+          if (t == T - 1) umma_commit(&s.q_empty[qb]);
+          if (prev >= 0 && !issue_pv()) { ok = false; break; }
+          prev = jt;
+          prev_first = (t == 0);
+          prev_last = (t == T - 1);
+          prev_ui = ui;
         }
-        umma_commit(&s.k_empty[jt % NS]);
-        if (T == 1) umma_commit(&s.q_empty);
-        for (int t = 0; t < T && ok; ++t) {
-          const int j = jt + t, st = j % NS, st1 = (j + 1) % NS;
-          if (!mbar_wait(&s.v_full[st], (j / NS) & 1, abort_flag, lim)) { ok = false; break; }
-          for (int x = 0; x < nb; ++x) {
-            const int cx = (x ? c1 : c0) + t;
-            if (!mbar_wait(&s.p_full[x], cx & 1, abort_flag, lim)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t d = tmem + kColO + x * HD, pa = tmem + kColS + x * BN;
-            const uint32_t vb = st ? v_lo1 : v_lo0;
-            if (t > 0) umma8_ts_mnmajor<1>(d, pa, vb, idesc_pv);
-            else umma8_ts_mnmajor<0>(d, pa, vb, idesc_pv);
-            if (x == nb - 1) umma_commit(&s.v_empty[st]);
-            if (t + 1 < T) {
-              if (x == 0 && !mbar_wait(&s.k_full[st1], ((j + 1) / NS) & 1, abort_flag, lim)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              umma8_ss_kmajor(tmem + kColS + x * BN, q_lo[x], st1 ? k_lo1 : k_lo0, idesc_qk);
-              umma_commit(&s.s_full[x]);
-            } else {
-              umma_commit(&s.o_ready[x]);
-            }
-          }
-          if (ok && t + 1 < T) {
-            umma_commit(&s.k_empty[st1]);
-            if (t + 2 == T) umma_commit(&s.q_empty);   // the unit's last S MMAs are issued
-          }
-        }
-        jt += T;
-        c0 += T;
-        if (nb == 2) c1 += T;
       }
+      if (ok && prev >= 0) issue_pv();
       umma_commit(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }
   }
-  } else {
+  } else if (warp < 8) {
     regs_inc<kRegsSoftmax>();
-    // ------------------------------------------------------------ softmax + epilogue
-    const int X = (warp - 4) >> 2;
+    // ------------------------------------------------------------ softmax
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_col = tmem + lane_base + kColS + X * BN;
-    const uint32_t o_col = tmem + lane_base + kColO + X * HD;
     const float sl2 = a.scale * 1.4426950408889634f;
-    int cx = 0, ux = 0;   // S/P events and units of this block so far
+    int jt = 0, ui = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
       const int4 un = p.units[u];
-      if (X == 1 && un.w <= BM) continue;   // block B absent from this unit
       const int T = unit_tiles(p, un.y);
-      const int row = X * BM + r;
-      const bool row_live = row < un.w;
+      const bool row_live = r < un.w;
       int64_t q = 0;
-      int slot = 0;
       KeyInterval iv{1, 0};
       if (row_live) {
-        const int32_t e = __ldg(p.lists + un.z + row);
+        const int32_t e = __ldg(p.lists + un.z + r);
         q = e / p.S;
-        slot = e - (int)q * p.S;
         iv = allowed_interval(a, query_pos(a, q));
       }
       float m2 = -CUDART_INF_F, l = 0.f;
-      for (int t = 0; t < T; ++t) {
+      for (int t = 0; t < T; ++t, ++jt) {
         const int64_t kbase = (int64_t)un.y * p.B + t * BN;
         const int kvalid = min(BN, a.Tk - (int)kbase);
         int lo_c = 1, hi_c = 0;
@@ -559,9 +521,10 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           lo_c = (int)max((int64_t)0, min((int64_t)BN, iv.lo - kbase));
           hi_c = (int)max((int64_t)-1, min((int64_t)kvalid - 1, iv.hi - kbase));
         }
-        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[X], (cx + t) & 1, abort_flag, lim));
+        ok = __all_sync(kFullMask, mbar_wait(&s.s_full[jt & 1], (jt >> 1) & 1, abort_flag, lim));
         if (!ok) break;
         tc_fence_after();
+        const uint32_t s_col = tmem + lane_base + kColS + (jt & 1) * BN;
         float sv[BN];
         {   // the row's 128 scores in four loads and one wait
           uint32_t rr[BN];
@@ -617,37 +580,64 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         float a0, a1;
         f2_unpack(f2_add(rs2[0], rs2[1]), a0, a1);
         l = l * alpha + (a0 + a1);
-        // O holds PV_X(t-1): it finished before S_X(t), issued after it
         if (__any_sync(kFullMask, rescale)) {
+          // O holds PV of this unit's earlier tiles: wait for the last one
+          ok = __all_sync(kFullMask, mbar_wait(&s.pv_done, (jt - 1) & 1, abort_flag, lim));
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
           for (int c4 = 0; c4 < HD / 32; ++c4) {
             uint32_t oo[32];
-            tmem_ld32_sync(o_col + c4 * 32, oo);
+            const uint32_t addr = tmem + lane_base + kColO + (ui & 1) * HD + c4 * 32;
+            tmem_ld32_sync(addr, oo);
 #pragma unroll
             for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
-            tmem_st32(o_col + c4 * 32, oo);
+            tmem_st32(addr, oo);
           }
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(&s.p_full[X]);
+        mbar_arrive(&s.p_full[jt & 1]);
       }
       if (!ok) break;
-      cx += T;
-      ok = __all_sync(kFullMask, mbar_wait(&s.o_ready[X], ux & 1, abort_flag, lim));
-      ++ux;
+      // the row's running summary to the epilogue warps
+      s.stats[ui & 1][r] = make_float4(m2, l, 0.f, 0.f);
+      mbar_arrive(&s.st_full[ui & 1]);
+    }
+  } else {
+    regs_dec<kRegsEpilogue>();
+    // ------------------------------------------------------------ epilogue
+    // Finalised summary (O_c, LSE_c) of each (query, head, slot) of a unit,
+    // from O in TMEM buffer ui & 1 and the row's (m, l); the softmax
+    // warps meanwhile run the next unit.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    int ui = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
+      const int4 un = p.units[u];
+      const int ob = ui & 1;
+      ok = __all_sync(kFullMask, mbar_wait(&s.o_full[ob], (ui >> 1) & 1, abort_flag, lim) &&
+                                     mbar_wait(&s.st_full[ob], (ui >> 1) & 1, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();
-      // epilogue: the finalised summary (O_c, LSE_c) of this row's (query,
-      // head, slot); O = z / l in bf16, LSE = m + ln l
-      const bool live = row_live && l > 0.f;
-      const float inv = live ? 1.f / l : 0.f;
+      const float4 st = s.stats[ob][r];
+      const bool row_live = r < un.w;
+      int64_t q = 0;
+      int slot = 0;
+      if (row_live) {
+        const int32_t e = __ldg(p.lists + un.z + r);
+        q = e / p.S;
+        slot = e - (int)q * p.S;
+      }
+      const bool live = row_live && st.y > 0.f;
+      const float inv = live ? 1.f / st.y : 0.f;
       const int64_t prow = ((int64_t)slot * a.Tq + q) * a.Hq + un.x;
       __nv_bfloat16* orow = p.part_o + prow * HD;
 #pragma unroll
       for (int c4 = 0; c4 < HD / 32; ++c4) {
         uint32_t oo[32];
-        tmem_ld32_sync(o_col + c4 * 32, oo);
+        tmem_ld32_sync(tmem + lane_base + kColO + ob * HD + c4 * 32, oo);
         if (row_live) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
@@ -660,22 +650,15 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
           }
         }
       }
-      if (row_live) p.part_lse[prow] = live ? (m2 + log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+      if (row_live) p.part_lse[prow] = live ? (st.x + log2f(st.y)) * 0.6931471805599453f : -CUDART_INF_F;
+      tc_fence_before();
+      mbar_arrive(&s.o_free[ob]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (s.abort && warp == 0 && lane == 0) {
-    // every role has stopped: let the copies in flight land (at most the
-    // last NS loads of each ring; earlier ones were consumed)
-    int no_abort = 0;
-    for (int j = max(0, s.k_issued - NS); j < s.k_issued; ++j)
-      mbar_wait(&s.k_full[j % NS], (j / NS) & 1, &no_abort, 200000000ull);
-    for (int j = max(0, s.v_issued - NS); j < s.v_issued; ++j)
-      mbar_wait(&s.v_full[j % NS], (j / NS) & 1, &no_abort, 200000000ull);
-  }
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0 && s.abort) report_status(a.dev_status, CPATTN_ERR_TIMEOUT);
 }

@@ -102,16 +102,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Brings a 3-D tile of the tensor map into L2 (no shared memory, no barrier):
-// a later tma_load_3d of the same tile then reads it from L2.
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32_t c0, int32_t c1,
-                                                   int32_t c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // Writes by ordinary stores to shared memory become visible to the tensor
 // core (async proxy).
 __device__ __forceinline__ void fence_proxy_async_smem() {

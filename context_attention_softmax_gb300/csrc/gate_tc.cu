@@ -380,14 +380,49 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         int n_top = 0;
 #pragma unroll
         for (int j = 0; j < kGateMaxTopk; ++j) { tv[j] = -CUDART_INF; tb[j] = 0x7fffffff; }
-        for (int w = 0; w < 4; ++w) {
-          for (uint32_t m = mL[w]; m != 0u; m &= m - 1u) {
-            const int b = 32 * w + __ffs(m) - 1;
+        // The members of U, four at a time: their float64 means are loaded
+        // and their gates reduced together, so the loads' latency overlaps;
+        // then each is inserted into the ranked list in ascending block order.
+        int w = 0;
+        uint32_t mcur = mL[0];
+        while (true) {
+          int bs[4];
+          int nb = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            while (mcur == 0u && w < 3) {
+              ++w;
+              mcur = w == 1 ? mL[1] : (w == 2 ? mL[2] : mL[3]);
+            }
+            if (mcur != 0u) {
+              bs[i] = 32 * w + __ffs(mcur) - 1;
+              mcur &= mcur - 1u;
+              ++nb;
+            } else {
+              bs[i] = -1;
+            }
+          }
+          if (nb == 0) break;
+          double vs[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int b = bs[i] >= 0 ? bs[i] : 0;
             const double* mu = p.mu64 + ((int64_t)b * a.Hkv + g) * GD + 4 * lane;
             const double2 u0 = *reinterpret_cast<const double2*>(mu);
             const double2 u1 = *reinterpret_cast<const double2*>(mu + 2);
-            double v = warp_sum_f64(fma(q3, u1.y, fma(q2, u1.x, fma(q1, u0.y, q0 * u0.x))));
-            int vb = b;
+            vs[i] = fma(q3, u1.y, fma(q2, u1.x, fma(q1, u0.y, q0 * u0.x)));
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vs[i] += __shfl_xor_sync(kFullMask, vs[i], o);
+          }
+          for (int i = 0; i < nb; ++i) {
+            double v = vs[0];
+            int vb = bs[0];
+#pragma unroll
+            for (int x = 1; x < 4; ++x)
+              if (x == i) { v = vs[x]; vb = bs[x]; }
             bool placed = false;   // insert (v, vb) into the ranked list of the best k
 #pragma unroll
             for (int j = 0; j < kGateMaxTopk; ++j) {

@@ -341,6 +341,7 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last();
       int cur_mt = -1;
       bool ok = true;
       for (int tile = t0; tile < t1 && ok; ++tile) {
@@ -358,7 +359,8 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
           const int st = b_fills % kKvStages;
           if (!mbar_wait(&s.b_empty[st], ((b_fills / kKvStages) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.b_full[st], kKvBBox);
-          tma_load_3d(s.b[st], &tm_b, &s.b_full[st], ks * GK, nt * KN, 0);
+          // every CTA streams all of wkv_b: keep it in L2 against the output stream
+          tma_load_3d_hint(s.b[st], &tm_b, &s.b_full[st], ks * GK, nt * KN, 0, keep);
         }
       }
     }
@@ -400,7 +402,7 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
     const int r = (warp - 4) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
     const int per_head = p.N + p.V;
-    const int64_t n_rows = (int64_t)p.n_tiles * KN;   // padded N
+    const uint64_t stream = l2_policy_evict_first();   // K/V are written once
     int ti = 0;
     for (int tile = t0; tile < t1; ++tile, ++ti) {
       const int buf = ti & 1;
@@ -414,7 +416,6 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
         const int col = nt * KN + half * GN;
         const int h = col / per_head;
         const bool valid = h < p.H && t < p.M;
-        (void)n_rows;
         const int part = col - h * per_head;
         __nv_bfloat16* dst = part < p.N ? p.k_out + t * p.k_st + (int64_t)h * p.k_sh + part
                                         : p.v_out + t * p.v_st + (int64_t)h * p.v_sh + (part - p.N);
@@ -437,7 +438,7 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
               val.y = pack2_bf16(__uint_as_float(acc[i + 2]), __uint_as_float(acc[i + 3]));
               val.z = pack2_bf16(__uint_as_float(acc[i + 4]), __uint_as_float(acc[i + 5]));
               val.w = pack2_bf16(__uint_as_float(acc[i + 6]), __uint_as_float(acc[i + 7]));
-              *reinterpret_cast<uint4*>(dst + c4 * 32 + i) = val;
+              st_global_v4_hint(dst + c4 * 32 + i, val, stream);
             }
           }
         }
@@ -445,14 +446,14 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
           uint4* kd = reinterpret_cast<uint4*>(p.k_out + t * p.k_st + (int64_t)h * p.k_sh + p.N);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            if (i < n_rope) kd[i] = rope_v[i];
+            if (i < n_rope) st_global_v4_hint(kd + i, rope_v[i], stream);
           for (int i0 = 8; i0 < n_rope; i0 += 8) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               if (i0 + i < n_rope) rope_v[i] = __ldg(rsrc + i0 + i);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              if (i0 + i < n_rope) kd[i0 + i] = rope_v[i];
+              if (i0 + i < n_rope) st_global_v4_hint(kd + i0 + i, rope_v[i], stream);
           }
         }
       }

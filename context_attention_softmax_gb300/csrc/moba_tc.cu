@@ -612,6 +612,9 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     // warps meanwhile run the next unit.
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // the slot summaries are read once, by the merge: let them leave L2
+    // first, before the K/V tiles that a neighbouring unit may still read
+    const uint64_t stream = l2_policy_evict_first();
     int ui = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
@@ -646,7 +649,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
             val.y = pack_bf16(__uint_as_float(oo[i + 2]) * inv, __uint_as_float(oo[i + 3]) * inv);
             val.z = pack_bf16(__uint_as_float(oo[i + 4]) * inv, __uint_as_float(oo[i + 5]) * inv);
             val.w = pack_bf16(__uint_as_float(oo[i + 6]) * inv, __uint_as_float(oo[i + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c4 * 32 + i) = val;
+            st_global_v4_hint(orow + c4 * 32 + i, val, stream);
           }
         }
       }

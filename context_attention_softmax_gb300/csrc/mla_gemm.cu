@@ -15,13 +15,16 @@
 //    each 128-column tile to the key or the value of its head and appends
 //    the head-shared key to every head's key row.
 //
-// Tiles of 128 x 128 outputs, K in steps of 64 (one 128-byte swizzled box of
-// bf16 per operand), six stages of 32 KiB.  Roles (256 threads): warp 0 TMA
-// producer, warp 1 MMA issuer and TMEM owner (two 128-column accumulators,
-// so the epilogue of one tile overlaps the main loop of the next), warps 4-7
-// epilogue (TMEM lane = output row).  Persistent CTAs take tiles in a fixed
-// stride; consecutive tiles share their A rows (materialisation) or their
-// head's weight (up-projection), so those reads come from L2.
+// The up-projection: tiles of 128 x 128 outputs, K in steps of 64 (one
+// 128-byte swizzled box of bf16 per operand), six stages of 32 KiB.  The
+// materialisation: tiles of 128 x 256, four stages of 48 KiB (see
+// mla_kv_kernel).  Roles (256 threads): warp 0 TMA producer, warp 1 MMA
+// issuer and TMEM owner (two accumulators, so the epilogue of one tile
+// overlaps the main loop of the next), warps 4-7 epilogue (TMEM lane =
+// output row).  Persistent CTAs take tiles in a fixed stride (up-projection:
+// consecutive tiles share their head's weight) or in contiguous runs
+// (materialisation: the CTAs running at one time share their A rows), so
+// those reads come from L2.
 //
 // Every wait is bounded (wait_limit_ns, 2 s by default); on expiry the CTA
 // drains its copies and MMAs in flight, frees TMEM and reports
@@ -42,10 +45,7 @@ constexpr uint32_t kABytes = GM * GK * 2;   // 16 KiB
 constexpr uint32_t kBBytes = GN * GK * 2;   // 16 KiB
 constexpr uint32_t kBHalf = GK * 64 * 2;    // MN-major B: 64 K-rows x 64 N-columns, 8 KiB
 
-enum { kModeVUp = 0, kModeKv = 1 };
-
 struct GemmParams {
-  int mode;
   int M;              // output rows (tokens)
   int m_tiles, n_tiles, batches, k_steps;
   int n_total_tiles;  // m_tiles * n_tiles * batches
@@ -146,14 +146,9 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
           const int st = it % kStages;
           if (!mbar_wait(&s.empty[st], ((it / kStages) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
           mbar_arrive_expect_tx(&s.full[st], kABytes + kBBytes);
-          if (p.mode == kModeVUp) {
-            tma_load_3d(s.a[st], &tm_a, &s.full[st], ks * GK, b, mt * GM);
-            tma_load_3d(s.b[st], &tm_b, &s.full[st], nt * GN, ks * GK, b);
-            tma_load_3d(s.b[st] + kBHalf, &tm_b, &s.full[st], nt * GN + 64, ks * GK, b);
-          } else {
-            tma_load_3d(s.a[st], &tm_a, &s.full[st], ks * GK, 0, mt * GM);
-            tma_load_3d(s.b[st], &tm_b, &s.full[st], ks * GK, nt * GN, 0);
-          }
+          tma_load_3d(s.a[st], &tm_a, &s.full[st], ks * GK, b, mt * GM);
+          tma_load_3d(s.b[st], &tm_b, &s.full[st], nt * GN, ks * GK, b);
+          tma_load_3d(s.b[st] + kBHalf, &tm_b, &s.full[st], nt * GN + 64, ks * GK, b);
         }
       }
       if (!ok || *abort_flag) {   // let the copies in flight land before the CTA exits
@@ -202,32 +197,7 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       int b, mt, nt;
       tile_coords(p, tile, b, mt, nt);
       const int64_t t = (int64_t)mt * GM + r;
-      __nv_bfloat16* dst;
-      bool rope = false;
-      int h = b;
-      if (p.mode == kModeVUp) {
-        dst = p.out + t * p.out_st + (int64_t)b * p.out_sh + nt * GN;
-      } else {
-        const int col = nt * GN, per_head = p.N + p.V;
-        h = col / per_head;
-        const int part = col - h * per_head;
-        if (part < p.N) {
-          dst = p.k_out + t * p.k_st + (int64_t)h * p.k_sh + part;
-          rope = part + GN == p.N;
-        } else {
-          dst = p.v_out + t * p.v_st + (int64_t)h * p.v_sh + (part - p.N);
-        }
-      }
-      // the head-shared key after this head's last key tile: every load is
-      // issued before the accumulator is read, so their latency overlaps it
-      constexpr int kRopeRegs = 8;   // up to 64 channels in registers per pass
-      uint4 rope_v[kRopeRegs];
-      const bool do_rope = rope && t < p.M;
-      const uint4* rsrc = reinterpret_cast<const uint4*>(p.k_shared + (do_rope ? t : 0) * p.ks_st);
-      const int n_rope = do_rope ? p.R / 8 : 0;
-#pragma unroll
-      for (int i = 0; i < kRopeRegs; ++i)
-        if (i < n_rope) rope_v[i] = __ldg(rsrc + i);
+      __nv_bfloat16* dst = p.out + t * p.out_st + (int64_t)b * p.out_sh + nt * GN;
 #pragma unroll
       for (int c4 = 0; c4 < GN / 32; ++c4) {
         uint32_t acc[32];
@@ -246,20 +216,6 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty[buf]);
-      if (do_rope) {
-        uint4* kd = reinterpret_cast<uint4*>(p.k_out + t * p.k_st + (int64_t)h * p.k_sh + p.N);
-#pragma unroll
-        for (int i = 0; i < kRopeRegs; ++i)
-          if (i < n_rope) kd[i] = rope_v[i];
-        for (int i0 = kRopeRegs; i0 < n_rope; i0 += kRopeRegs) {   // R > 64: further passes
-#pragma unroll
-          for (int i = 0; i < kRopeRegs; ++i)
-            if (i0 + i < n_rope) rope_v[i] = __ldg(rsrc + i0 + i);
-#pragma unroll
-          for (int i = 0; i < kRopeRegs; ++i)
-            if (i0 + i < n_rope) kd[i0 + i] = rope_v[i];
-        }
-      }
     }
   }
 
@@ -271,27 +227,29 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 }
 
 // ---------------------------------------------------------------- K/V materialisation
-// The materialisation's A block (128 tokens x L <= 512 latent channels) is
-// reused by every 256-wide N tile of its row block, so a CTA keeps it in
-// shared memory (eight 16 KiB boxes) and streams only wkv_b through a
-// three-stage ring of 256 x 64 boxes.  Per tile that is 256 KiB of operands
-// for 33.5 MFLOP, against 256 KiB for 16.8 MFLOP with 128 x 128 tiles, so
-// the kernel is no longer bound by the L2-to-SM bandwidth.  CTAs take
-// contiguous runs of tiles in (row block, N tile) order, so a CTA loads a
-// new A block only when its run crosses a row block.
+// 128 x 256 output tiles: per K step a stage holds the A box (128 tokens x 64
+// latent channels, 16 KiB) and the B box (256 rows of wkv_b x 64, 32 KiB),
+// four stages deep so that enough bytes are in flight to keep the operand
+// stream from L2 going (a 128 x 512 A block kept resident left room for only
+// three 32 KiB B stages and ran at ~20 B/clk per SM).  A 256-wide tile reads
+// 384 KiB of operands for 33.5 MFLOP (87 FLOP/B, against 64 for 128 x 128
+// tiles).  CTAs take contiguous runs of tiles in (row block, N tile) order,
+// so the CTAs running at one time share their A rows in L2; wkv_b (33.5 MB)
+// is loaded with an evict-last policy so that it stays in L2 against the
+// K/V output stream, which is written evict-first.
 constexpr int KN = 256;                       // N tile
-constexpr int kKvStages = 3;
-constexpr int kMaxKSteps = 8;                 // L <= 512
+constexpr int kKvStages = 4;
 constexpr uint32_t kKvABox = GM * GK * 2;     // 16 KiB
 constexpr uint32_t kKvBBox = KN * GK * 2;     // 32 KiB
 
 struct KvSmem {
-  uint8_t a[kMaxKSteps][kKvABox];
+  uint8_t a[kKvStages][kKvABox];
   uint8_t b[kKvStages][kKvBBox];
-  uint64_t a_full, a_empty, b_full[kKvStages], b_empty[kKvStages];
+  uint64_t full[kKvStages], empty[kKvStages];
   uint64_t acc_full[2], acc_empty[2], drain;
   uint32_t tmem_base;
   int abort;
+  int fills;                     // stage fills issued (for the drain on abort)
 };
 constexpr size_t kKvSmemBytes = sizeof(KvSmem) + 1024;
 static_assert(kKvSmemBytes <= 232448, "shared memory budget");
@@ -310,11 +268,9 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
   const int t1 = (int)((int64_t)(blockIdx.x + 1) * p.n_total_tiles / gridDim.x);
 
   if (threadIdx.x == 0) {
-    mbar_init(&s.a_full, 1);
-    mbar_init(&s.a_empty, 1);
     for (int i = 0; i < kKvStages; ++i) {
-      mbar_init(&s.b_full[i], 1);
-      mbar_init(&s.b_empty[i], 1);
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.acc_full[i], 1);
@@ -322,6 +278,7 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
     }
     mbar_init(&s.drain, 1);
     s.abort = 0;
+    s.fills = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -336,62 +293,46 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
-  int a_loads = 0, b_fills = 0;   // producer's counts, for the drain on abort
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();
-      int cur_mt = -1;
+      int fills = 0;
       bool ok = true;
       for (int tile = t0; tile < t1 && ok; ++tile) {
         const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
-        if (mt != cur_mt) {
-          // the previous row block's MMAs are done with the resident A
-          if (a_loads > 0 && !mbar_wait(&s.a_empty, (a_loads - 1) & 1, abort_flag, lim)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.a_full, (uint32_t)p.k_steps * kKvABox);
-          for (int ks = 0; ks < p.k_steps; ++ks)
-            tma_load_3d(s.a[ks], &tm_a, &s.a_full, ks * GK, 0, mt * GM);
-          ++a_loads;
-          cur_mt = mt;
-        }
-        for (int ks = 0; ks < p.k_steps; ++ks, ++b_fills) {
-          const int st = b_fills % kKvStages;
-          if (!mbar_wait(&s.b_empty[st], ((b_fills / kKvStages) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
-          mbar_arrive_expect_tx(&s.b_full[st], kKvBBox);
+        for (int ks = 0; ks < p.k_steps; ++ks, ++fills) {
+          const int st = fills % kKvStages;
+          if (!mbar_wait(&s.empty[st], ((fills / kKvStages) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
+          mbar_arrive_expect_tx(&s.full[st], kKvABox + kKvBBox);
+          tma_load_3d(s.a[st], &tm_a, &s.full[st], ks * GK, 0, mt * GM);
           // every CTA streams all of wkv_b: keep it in L2 against the output stream
-          tma_load_3d_hint(s.b[st], &tm_b, &s.b_full[st], ks * GK, nt * KN, 0, keep);
+          tma_load_3d_hint(s.b[st], &tm_b, &s.full[st], ks * GK, nt * KN, 0, keep);
         }
       }
+      s.fills = fills;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(GM, KN, 0, 0);
-      int cur_mt = -1, n_a = 0, it = 0, ti = 0;
+      int it = 0, ti = 0;
       bool ok = true;
       for (int tile = t0; tile < t1 && ok; ++tile, ++ti) {
-        const int mt = tile / p.n_tiles;
         const int buf = ti & 1;
-        if (mt != cur_mt) {
-          if (!mbar_wait(&s.a_full, n_a & 1, abort_flag, lim)) { ok = false; break; }
-          ++n_a;
-          cur_mt = mt;
-        }
         if (!mbar_wait(&s.acc_empty[buf], ((ti >> 1) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * KN);
         for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
           const int st = it % kKvStages;
-          if (!mbar_wait(&s.b_full[st], (it / kKvStages) & 1, abort_flag, lim)) { ok = false; break; }
+          if (!mbar_wait(&s.full[st], (it / kKvStages) & 1, abort_flag, lim)) { ok = false; break; }
           tc_fence_after();
-          mma_stage<0>(d, desc_lo(smem_u32(s.a[ks]), 16), desc_lo(smem_u32(s.b[st]), 16), idesc, ks > 0);
-          umma_commit(&s.b_empty[st]);
+          mma_stage<0>(d, desc_lo(smem_u32(s.a[st]), 16), desc_lo(smem_u32(s.b[st]), 16), idesc, ks > 0);
+          umma_commit(&s.empty[st]);
         }
         if (!ok) break;
         umma_commit(&s.acc_full[buf]);
-        // the last tile of this row block in the run: A may be replaced
-        if (tile + 1 >= t1 || (tile + 1) / p.n_tiles != mt) umma_commit(&s.a_empty);
       }
       umma_commit(&s.drain);
       int no_abort = 0;
@@ -466,12 +407,11 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
   __syncthreads();
   tc_fence_after();
   if (s.abort && warp == 0 && lane == 0) {
-    // every role has stopped: let the copies in flight land (the last A load
-    // and at most the last kKvStages B fills; earlier ones were consumed)
+    // every role has stopped: let the copies in flight land (at most the
+    // last kKvStages fills; earlier ones were consumed)
     int no_abort = 0;
-    if (a_loads > 0) mbar_wait(&s.a_full, (a_loads - 1) & 1, &no_abort, 200000000ull);
-    for (int j = max(0, b_fills - kKvStages); j < b_fills; ++j)
-      mbar_wait(&s.b_full[j % kKvStages], (j / kKvStages) & 1, &no_abort, 200000000ull);
+    for (int j = max(0, s.fills - kKvStages); j < s.fills; ++j)
+      mbar_wait(&s.full[j % kKvStages], (j / kKvStages) & 1, &no_abort, 200000000ull);
   }
   if (warp == 1) tmem_dealloc(tmem, 512);
   if (threadIdx.x == 0 && s.abort) report_status(p.dev_status, CPATTN_ERR_TIMEOUT);
@@ -479,18 +419,14 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-cudaError_t launch_gemm(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
-                        bool b_mn, cudaStream_t stream) {
-  const void* kern = b_mn ? reinterpret_cast<const void*>(mla_gemm_kernel<1>)
-                          : reinterpret_cast<const void*>(mla_gemm_kernel<0>);
-  cudaError_t e = ensure_smem_attr(kern, (int)kGemmSmemBytes);
+cudaError_t launch_v_up(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                        cudaStream_t stream) {
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(mla_gemm_kernel<1>),
+                                   (int)kGemmSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_sm = device_sm_count();
   const int grid = p.n_total_tiles < n_sm ? p.n_total_tiles : n_sm;
-  if (b_mn)
-    mla_gemm_kernel<1><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, p);
-  else
-    mla_gemm_kernel<0><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, p);
+  mla_gemm_kernel<1><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
@@ -511,7 +447,6 @@ cpattn_status mla_v_up_impl(const void* o_latent, int64_t o_st, int64_t o_sh,
   if (!encode_bf16_3d(&ta, o_latent, ad, as, ab) || !encode_bf16_3d(&tb, up_v_weight, bd, bs, bb))
     return report_error(CPATTN_ERR_INVALID_ARG, "cpattn_mla_v_up: a TMA descriptor cannot describe the operands");
   GemmParams p{};
-  p.mode = kModeVUp;
   p.M = T;
   p.m_tiles = (T + GM - 1) / GM;
   p.n_tiles = V / GN;
@@ -523,7 +458,7 @@ cpattn_status mla_v_up_impl(const void* o_latent, int64_t o_st, int64_t o_sh,
   p.out_sh = out_sh;
   p.dev_status = dev_status;
   p.limit = wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : 2000000000ull;
-  const cudaError_t e = launch_gemm(p, ta, tb, true, stream);
+  const cudaError_t e = launch_v_up(p, ta, tb, stream);
   if (e != cudaSuccess) return report_error(CPATTN_ERR_CUDA, cudaGetErrorString(e));
   return CPATTN_OK;
 }
@@ -536,22 +471,20 @@ cpattn_status mla_kv_impl(const void* kv_c, int64_t c_st, const void* k_shared, 
   if (T == 0) return CPATTN_OK;
   CUtensorMap ta, tb;
   const int64_t n_rows = (int64_t)H * (N + V);
-  const bool resident_a = L <= kMaxKSteps * GK;   // the A block fits shared memory
   const uint64_t ad[3] = {(uint64_t)L, 1, (uint64_t)T};
   const uint64_t as[2] = {(uint64_t)c_st * 2, (uint64_t)c_st * 2};
   const uint32_t ab[3] = {GK, 1, GM};
   const uint64_t bd[3] = {(uint64_t)L, (uint64_t)n_rows, 1};
   const uint64_t bs[2] = {(uint64_t)L * 2, (uint64_t)n_rows * L * 2};
-  const uint32_t bb[3] = {GK, (uint32_t)(resident_a ? KN : GN), 1};
+  const uint32_t bb[3] = {GK, (uint32_t)KN, 1};
   if (!encode_bf16_3d(&ta, kv_c, ad, as, ab) || !encode_bf16_3d(&tb, wkv_b, bd, bs, bb))
     return report_error(CPATTN_ERR_INVALID_ARG,
                         "cpattn_mla_kv_materialise: a TMA descriptor cannot describe the operands");
   GemmParams p{};
-  p.mode = kModeKv;
   p.M = T;
   p.H = H;
   p.m_tiles = (T + GM - 1) / GM;
-  p.n_tiles = resident_a ? (int)((n_rows + KN - 1) / KN) : (int)(n_rows / GN);
+  p.n_tiles = (int)((n_rows + KN - 1) / KN);
   p.batches = 1;
   p.k_steps = L / GK;
   p.n_total_tiles = p.m_tiles * p.n_tiles;
@@ -568,17 +501,12 @@ cpattn_status mla_kv_impl(const void* kv_c, int64_t c_st, const void* k_shared, 
   p.R = R;
   p.dev_status = dev_status;
   p.limit = wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : 2000000000ull;
-  cudaError_t e;
-  if (resident_a) {
-    e = ensure_smem_attr(reinterpret_cast<const void*>(mla_kv_kernel), (int)kKvSmemBytes);
-    if (e == cudaSuccess) {
-      const int n_sm = device_sm_count();
-      const int grid = p.n_total_tiles < n_sm ? p.n_total_tiles : n_sm;
-      mla_kv_kernel<<<grid, kGemmThreads, kKvSmemBytes, stream>>>(ta, tb, p);
-      e = cudaGetLastError();
-    }
-  } else {
-    e = launch_gemm(p, ta, tb, false, stream);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(mla_kv_kernel), (int)kKvSmemBytes);
+  if (e == cudaSuccess) {
+    const int n_sm = device_sm_count();
+    const int grid = p.n_total_tiles < n_sm ? p.n_total_tiles : n_sm;
+    mla_kv_kernel<<<grid, kGemmThreads, kKvSmemBytes, stream>>>(ta, tb, p);
+    e = cudaGetLastError();
   }
   if (e != cudaSuccess) return report_error(CPATTN_ERR_CUDA, cudaGetErrorString(e));
   return CPATTN_OK;

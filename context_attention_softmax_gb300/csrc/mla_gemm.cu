@@ -236,7 +236,10 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
 // tiles).  CTAs take contiguous runs of tiles in (row block, N tile) order,
 // so the CTAs running at one time share their A rows in L2; wkv_b (33.5 MB)
 // is loaded with an evict-last policy so that it stays in L2 against the
-// K/V output stream, which is written evict-first.
+// K/V output stream, which is written evict-first.  The epilogue writes each
+// 64-column box of a tile (and the shared rope key) into a swizzled staging
+// buffer and stores it with one TMA store, instead of 16-byte stores of 128
+// different rows per warp instruction.
 constexpr int KN = 256;                       // N tile
 constexpr int kKvStages = 4;
 constexpr uint32_t kKvABox = GM * GK * 2;     // 16 KiB
@@ -245,6 +248,7 @@ constexpr uint32_t kKvBBox = KN * GK * 2;     // 32 KiB
 struct KvSmem {
   uint8_t a[kKvStages][kKvABox];
   uint8_t b[kKvStages][kKvBBox];
+  uint8_t out[2][GM * 128];      // two 128 x 64 bf16 output boxes (swizzled) for TMA stores
   uint64_t full[kKvStages], empty[kKvStages];
   uint64_t acc_full[2], acc_empty[2], drain;
   uint32_t tmem_base;
@@ -256,6 +260,7 @@ static_assert(kKvSmemBytes <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
 mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+              const __grid_constant__ CUtensorMap tm_ko, const __grid_constant__ CUtensorMap tm_vo,
               const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   KvSmem& s = *reinterpret_cast<KvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -340,14 +345,35 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
+    // Per 64-column box: wait until the store of the box before last has
+    // read its buffer, fill the buffer (thread r = row r, its 128 bytes as
+    // eight 16-byte pieces at r * 128 + ((c ^ (r % 8)) * 16), the 128-byte
+    // swizzle the map describes), fence for the async proxy, and one thread
+    // issues the TMA store.  Rows beyond the last token are not written.
     const int r = (warp - 4) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+    const bool issuer = threadIdx.x == 128;
     const int per_head = p.N + p.V;
     const uint64_t stream = l2_policy_evict_first();   // K/V are written once
-    int ti = 0;
+    int ti = 0, bx = 0;
+    auto box_begin = [&]() {
+      if (issuer) bulk_wait_group_read<1>();   // the buffer's previous store has read it
+      named_bar_sync(1, 128);
+      return s.out[bx & 1];
+    };
+    auto box_end = [&](const CUtensorMap* map, int c0, int h, int t0) {
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (issuer) {
+        tma_store_3d_hint(map, s.out[bx & 1], c0, h, t0, stream);
+        bulk_commit_group();
+      }
+      ++bx;
+    };
     for (int tile = t0; tile < t1; ++tile, ++ti) {
       const int buf = ti & 1;
-      const bool ok = __all_sync(kFullMask, mbar_wait(&s.acc_full[buf], (ti >> 1) & 1, abort_flag, lim));
+      // all 128 threads leave together (they share named barriers below)
+      const bool ok = named_bar_and(2, 128, mbar_wait(&s.acc_full[buf], (ti >> 1) & 1, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();
       const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
@@ -356,51 +382,49 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
       for (int half = 0; half < 2; ++half) {
         const int col = nt * KN + half * GN;
         const int h = col / per_head;
-        const bool valid = h < p.H && t < p.M;
         const int part = col - h * per_head;
-        __nv_bfloat16* dst = part < p.N ? p.k_out + t * p.k_st + (int64_t)h * p.k_sh + part
-                                        : p.v_out + t * p.v_st + (int64_t)h * p.v_sh + (part - p.N);
-        const bool rope = valid && part < p.N && part + GN == p.N;
-        uint4 rope_v[8];
-        const uint4* rsrc = reinterpret_cast<const uint4*>(p.k_shared + (rope ? t : 0) * p.ks_st);
-        const int n_rope = rope ? p.R / 8 : 0;
+        const bool present = h < p.H;                  // the padded last tile's second half is not
+        const bool is_key = part < p.N;
+#pragma unroll 1
+        for (int x = 0; x < 2; ++x) {                 // two 64-column boxes of the half
+          uint32_t acc[2][32];
+          tmem_ld32(tmem + lane_base + (uint32_t)(buf * KN + half * GN + x * 64), acc[0]);
+          tmem_ld32(tmem + lane_base + (uint32_t)(buf * KN + half * GN + x * 64 + 32), acc[1]);
+          tmem_wait_ld();
+          if (!present) continue;
+          uint8_t* stage = box_begin();
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < n_rope) rope_v[i] = __ldg(rsrc + i);
-#pragma unroll
-        for (int c4 = 0; c4 < GN / 32; ++c4) {
-          uint32_t acc[32];
-          tmem_ld32_wait(tmem + lane_base + (uint32_t)(buf * KN + half * GN + c4 * 32), acc);
-          if (valid) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 val;
-              val.x = pack2_bf16(__uint_as_float(acc[i + 0]), __uint_as_float(acc[i + 1]));
-              val.y = pack2_bf16(__uint_as_float(acc[i + 2]), __uint_as_float(acc[i + 3]));
-              val.z = pack2_bf16(__uint_as_float(acc[i + 4]), __uint_as_float(acc[i + 5]));
-              val.w = pack2_bf16(__uint_as_float(acc[i + 6]), __uint_as_float(acc[i + 7]));
-              st_global_v4_hint(dst + c4 * 32 + i, val, stream);
-            }
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t* a4 = acc[c >> 2] + 8 * (c & 3);
+            uint4 val;
+            val.x = pack2_bf16(__uint_as_float(a4[0]), __uint_as_float(a4[1]));
+            val.y = pack2_bf16(__uint_as_float(a4[2]), __uint_as_float(a4[3]));
+            val.z = pack2_bf16(__uint_as_float(a4[4]), __uint_as_float(a4[5]));
+            val.w = pack2_bf16(__uint_as_float(a4[6]), __uint_as_float(a4[7]));
+            *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) << 4)) = val;
           }
+          box_end(is_key ? &tm_ko : &tm_vo, (is_key ? part : part - p.N) + 64 * x, h, mt * GM);
         }
-        if (rope) {
-          uint4* kd = reinterpret_cast<uint4*>(p.k_out + t * p.k_st + (int64_t)h * p.k_sh + p.N);
+        if (present && is_key && part + GN == p.N) {
+          // the head-shared key after this head's last key tile, 64 channels per box
+          for (int c0 = 0; c0 < p.R; c0 += 64) {
+            uint8_t* stage = box_begin();
+            const bool row_ok = t < p.M;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            if (i < n_rope) st_global_v4_hint(kd + i, rope_v[i], stream);
-          for (int i0 = 8; i0 < n_rope; i0 += 8) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i0 + i < n_rope) rope_v[i] = __ldg(rsrc + i0 + i);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i0 + i < n_rope) st_global_v4_hint(kd + i0 + i, rope_v[i], stream);
+            for (int c = 0; c < 8; ++c) {
+              const int ch = c0 + 8 * c;
+              uint4 val = make_uint4(0u, 0u, 0u, 0u);
+              if (row_ok && ch < p.R) val = __ldg(reinterpret_cast<const uint4*>(p.k_shared + t * p.ks_st + ch));
+              *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ (r & 7)) << 4)) = val;
+            }
+            box_end(&tm_ko, p.N + c0, h, mt * GM);
           }
         }
       }
       tc_fence_before();
       mbar_arrive(&s.acc_empty[buf]);
     }
+    if (issuer) bulk_wait_group_all();   // every store complete before the buffers go away
   }
 
   tc_fence_before();
@@ -501,11 +525,20 @@ cpattn_status mla_kv_impl(const void* kv_c, int64_t c_st, const void* k_shared, 
   p.R = R;
   p.dev_status = dev_status;
   p.limit = wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : 2000000000ull;
+  CUtensorMap tko, tvo;
+  const uint64_t kd[3] = {(uint64_t)(N + R), (uint64_t)H, (uint64_t)T};
+  const uint64_t ks[2] = {(uint64_t)k_sh * 2, (uint64_t)k_st * 2};
+  const uint64_t vd[3] = {(uint64_t)V, (uint64_t)H, (uint64_t)T};
+  const uint64_t vs[2] = {(uint64_t)v_sh * 2, (uint64_t)v_st * 2};
+  const uint32_t ob[3] = {64, 1, GM};
+  if (!encode_bf16_3d(&tko, k_out, kd, ks, ob) || !encode_bf16_3d(&tvo, v_out, vd, vs, ob))
+    return report_error(CPATTN_ERR_INVALID_ARG,
+                        "cpattn_mla_kv_materialise: a TMA descriptor cannot describe the outputs");
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(mla_kv_kernel), (int)kKvSmemBytes);
   if (e == cudaSuccess) {
     const int n_sm = device_sm_count();
     const int grid = p.n_total_tiles < n_sm ? p.n_total_tiles : n_sm;
-    mla_kv_kernel<<<grid, kGemmThreads, kKvSmemBytes, stream>>>(ta, tb, p);
+    mla_kv_kernel<<<grid, kGemmThreads, kKvSmemBytes, stream>>>(ta, tb, tko, tvo, p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return report_error(CPATTN_ERR_CUDA, cudaGetErrorString(e));

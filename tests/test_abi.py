@@ -171,3 +171,89 @@ def test_indexer_needs_weights_outputs_and_its_workspace(lib):
     assert "aligned" in lib.cpattn_last_error().decode()
     a.Tq = 0     # nothing to select: no workspace needed
     assert lib.cpattn_workspace_size(_lib.OP_DSA_INDEXER, ctypes.byref(a), 16, 1) == 0
+
+
+def _bwd_call(lib, a, d_out=0x90000, dq=0xA0000, dk=0xB0000, dv=0xC0000):
+    return lib.cpattn_chunk_bwd(ctypes.byref(a), d_out, 16 * 128, 128, dq, 16 * 128, 128,
+                                dk, 4 * 128, 128, dv, 4 * 128, 128, None, 0, None)
+
+
+@pytest.mark.parametrize("mutate,kw,status,msg", [
+    (lambda a: setattr(a, "lse", None), {}, 1, "lse (the forward's) is NULL"),
+    (lambda a: None, {"dq": None}, 1, "dq"),
+    (lambda a: None, {"d_out": None}, 1, "d_out"),
+    (lambda a: None, {"dk": None}, 1, "dk"),
+    (lambda a: setattr(a, "dtype", _lib.CPATTN_FP32), {}, 2, "bf16"),
+    (lambda a: (setattr(a, "Dv", 64), setattr(a, "v_stride_h", 64)), {}, 2, "head dims 128"),
+    (lambda a: (setattr(a, "kv_chunk_len", 128), setattr(a, "partial_o", 0x50000),
+                setattr(a, "partial_lse", 0x58000)), {}, 1, "kv_chunk_len = 0"),
+])
+def test_chunk_bwd_rejects_bad_arguments(lib, mutate, kw, status, msg):
+    """Host validation of the backward: nothing is launched on rejection."""
+    a = _valid_args()
+    a.lse = 0x48000
+    mutate(a)
+    assert _bwd_call(lib, a, **kw) == status
+    assert msg in lib.cpattn_last_error().decode()
+
+
+def test_chunk_bwd_with_no_queries_and_no_keys_is_a_no_op(lib):
+    a = _valid_args()
+    a.Tq, a.Tk = 0, 0
+    assert _bwd_call(lib, a, d_out=None, dq=None, dk=None, dv=None) == 0
+
+
+def _v_up(lib, o=0x10000, w=0x20000, T=8, H=4, L=512, V=128, out=0x30000, limit=0):
+    return lib.cpattn_mla_v_up(o, H * L, L, w, T, H, L, V, out, H * V, V, None, limit, None)
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    ({"L": 32}, 2, "L=32"),
+    ({"V": 64}, 2, "V=64"),
+    ({"H": 0}, 1, "H=0"),
+    ({"T": -1}, 1, "T=-1"),
+    ({"limit": -1}, 1, "wait_limit_ns"),
+    ({"w": None}, 1, "up_v_weight"),
+    ({"w": 0x20008}, 1, "up_v_weight"),
+    ({"o": None}, 1, "o_latent"),
+    ({"out": None}, 1, "out"),
+])
+def test_mla_v_up_rejects_bad_arguments(lib, kw, status, msg):
+    assert _v_up(lib, **kw) == status
+    assert msg in lib.cpattn_last_error().decode()
+
+
+def test_mla_v_up_with_no_tokens_is_a_no_op(lib):
+    assert _v_up(lib, o=None, w=None, T=0, out=None) == 0
+
+
+def _kv(lib, c=0x10000, ks=0x20000, wb=0x30000, T=8, L=512, H=4, N=128, R=64, V=128,
+        k=0x40000, v=0x50000, c_st=None, limit=0):
+    c_st = L if c_st is None else c_st
+    return lib.cpattn_mla_kv_materialise(c, c_st, ks, R, wb, T, L, H, N, R, V,
+                                         k, H * (N + R), N + R, v, H * V, V, None, limit, None)
+
+
+@pytest.mark.parametrize("kw,status,msg", [
+    ({"R": 4}, 2, "R=4"),
+    ({"N": 64}, 2, "N=64"),
+    ({"V": 192}, 2, "V=192"),
+    ({"L": 96}, 2, "L=96"),
+    ({"H": 0}, 1, "H=0"),
+    ({"limit": -1}, 1, "wait_limit_ns"),
+    ({"c": None}, 1, "kv_c"),
+    ({"c_st": 500}, 1, "kv_c"),
+    ({"wb": 0x30008}, 1, "wkv_b"),
+    ({"ks": None}, 1, "k_shared"),
+    ({"k": None}, 1, "k_out"),
+    ({"v": None}, 1, "v_out"),
+])
+def test_mla_kv_materialise_rejects_bad_arguments(lib, kw, status, msg):
+    assert _kv(lib, **kw) == status
+    assert msg in lib.cpattn_last_error().decode()
+
+
+def test_mla_kv_materialise_without_shared_key_and_with_no_tokens(lib):
+    # R = 0: k_shared is never read, so NULL is valid; T = 0 launches nothing
+    assert _kv(lib, c=None, ks=None, wb=None, T=0, k=None, v=None) == 0
+    assert _kv(lib, T=0, R=0, ks=None) == 0

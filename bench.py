@@ -67,16 +67,24 @@ L2_NOTE = "flushed by a 256 MiB write before every timed step"
 # dominant kernel from one ncu capture (summarised under profiles/), valid
 # only while the kernel's sources hash to the value they had then.
 TRAFFIC = {
-    "dense_gqa": {"bytes": 21_195_008 + 0, "kernel": "dense_tc_kernel",
+    "dense_gqa": {"bytes": 21_195_264 + 0, "kernel": "dense_tc_kernel",
                   "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                  "sha": "e207fd27a5d08658"},
-    "dsa": {"bytes": 662_182_656 + 505_942_016, "kernel": "dsa_attn_kernel",
-            "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "1a2d63f8b3cc8586"},
-    "mla_kv": {"bytes": 250_570_240 + 2_629_161_472, "kernel": "mla_gemm_kernel",
-               "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "8dfc188bab9ff2ce"},
-    "dense_gqa_bwd": {"bytes": 29_677_568 + 153_600, "kernel": "bwd_dkdv_kernel",
+                  "sha": "41f85c8be9eca783"},
+    "dense_gqa_4chunks": {"bytes": 21_157_376 + 13_576_448, "kernel": "dense_tc_kernel<1>",
+                          "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh",
+                                      "common.cuh"],
+                          "sha": "41f85c8be9eca783"},
+    "dsa": {"bytes": 661_784_576 + 506_544_128, "kernel": "dsa_attn_kernel",
+            "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "6d9adf29f0d1fc91"},
+    "mla_kv": {"bytes": 566_199_296 + 2_627_799_552, "kernel": "mla_kv_kernel",
+               "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "7694db41bfcf00d2"},
+    "mla_v_up": {"bytes": 553_843_456 + 112_686_336, "kernel": "mla_gemm_kernel<1>",
+                 "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "7694db41bfcf00d2"},
+    "dense_gqa_bwd": {"bytes": 29_792_256 + 205_056, "kernel": "bwd_dkdv_kernel",
                       "sources": ["dense_bwd.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                      "sha": "4af28464f5940964"},
+                      "sha": "6e468e42c43df353"},
+    "moba": {"bytes": 1_156_865_536 + 259_025_664, "kernel": "moba_attn_kernel",
+             "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "4bd05f662df3ed35"},
 }
 
 

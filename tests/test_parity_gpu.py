@@ -405,6 +405,38 @@ def test_moba_gate_ties_and_few_candidates():
     assert sel2[0, 0].tolist() == [0, 1, -1, -1]
 
 
+def test_moba_attention_slot_patterns():
+    """Block-grouped attention on hand-made selections: rows whose every slot
+    is empty (-1), rows with only the own block, rows naming a block twice
+    (each occurrence counts), and rows naming a block wholly after the query
+    (no permitted key there) - equal to the float64 oracle, with O = 0 and
+    LSE = -inf where nothing is permitted."""
+    w = inputs.moba(seed=9, Tq=384, Tk=2048, offset=1664, H=2, block_size=128, topk=3)
+    q, k, v = to_gpu(w)
+    rng = np.random.default_rng(9)
+    B, S = w.block_size, w.topk + 1
+    own = (w.causal_offset + np.arange(w.Tq)) // B
+    sel = np.full((w.Tq, 2, S), -1, dtype=np.int32)
+    for i in range(w.Tq):
+        for h in range(2):
+            kind = (i + h) % 5
+            if kind == 1:
+                sel[i, h, 0] = own[i]
+            elif kind == 2:
+                b = rng.integers(0, own[i])
+                sel[i, h, :3] = [b, b, own[i]]
+            elif kind == 3:
+                sel[i, h, :2] = [min(own[i] + 1, 15), rng.integers(0, own[i])]
+            elif kind == 4:
+                sel[i, h] = sorted(rng.choice(own[i], 3, replace=False).tolist()) + [own[i]]
+    o, lse = cpattn_topk_sparse_fwd(q, k, v, torch.from_numpy(sel).cuda(), block_size=B,
+                                    scale=w.scale, causal_offset=w.causal_offset)
+    qf, kf, vf = f64(w)
+    O, L, bad = orc.sparse_attention(qf, kf, vf, w.scale, layout_of(w), sel, B)
+    assert bad == 0 and np.isneginf(L).sum() >= 150   # the all-empty rows at least
+    assert_matches(o, lse, O, L, "bf16", "moba slot patterns")
+
+
 @pytest.mark.parametrize("dtype,D", [("fp32", 64), ("bf16", 72), ("fp32", 136)])
 def test_moba_gate_other_shapes_and_fp32(dtype, D):
     """The SIMT gate over the vectorised block means: fp32 inputs, head dims

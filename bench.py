@@ -218,7 +218,7 @@ class DenseBwdRunner(Runner):
     LSE and a seeded d_out (prep, dk/dv kernel, dq kernel)."""
 
     name = "dense_gqa_bwd"
-    kernel = "cpattn_chunk_bwd (bwd_dkdv_kernel + bwd_dq_kernel)"
+    kernel = "cpattn_chunk_bwd (bwd_prep_kernel, then bwd_kernel: dk/dv and dq CTAs in one launch)"
     launches_per_step = 4   # interval init, prep, dk/dv, dq
 
     def __init__(self, device):

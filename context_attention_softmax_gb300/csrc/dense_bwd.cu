@@ -12,16 +12,18 @@
 // dk and dv of a KV head summed over its query heads (GQA).
 //
 // Three launches, no atomics (the results do not depend on scheduling):
-//   bwd_prep_kernel  D_i and LSE_i in log2 units per (query, head), and the
+//   bwd_iv_init_kernel, bwd_prep_kernel
+//                    D_i and LSE_i in log2 units per (query, head), and the
 //                    union of the permitted key intervals of every 128-query
 //                    tile (one interval per query: own sequence, cut at qpos);
-//   bwd_dkdv_kernel  one CTA per (128-key tile, KV head): for every query
-//                    head of the group and every query tile whose interval
-//                    meets the key tile,
+//   bwd_kernel       two kinds of CTA in one grid:
+//     dk/dv CTAs     one per (128-key tile, KV head): for every query head
+//                    of the group and every query tile whose interval meets
+//                    the key tile,
 //                      S^T = K Q^T, dP^T = V g^T      (TMEM, key row = lane)
 //                      P^T, dS^T written as bf16 over S^T, dP^T
 //                      dv += P^T g,  dk += dS^T Q      (A operand from TMEM)
-//   bwd_dq_kernel    one CTA per (128-query tile, query head): for every live
+//     dq CTAs        one per (128-query tile, query head): for every live
 //                    key tile, S = Q K^T, dP = g V^T, dS over S, dq += dS K.
 // TMA loads 128 x 128 tiles as two 64-column 128-byte-swizzled boxes; one
 // tile serves as a K-major operand (the S and dP products) and as an
@@ -137,10 +139,10 @@ constexpr size_t kDkdvSmem = sizeof(DkdvSmem) + 1024;
 
 constexpr uint32_t kColDP = 128, kColDV = 256, kColDK = 384;   // S or S^T at kColS = 0
 
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-    const BwdParams p) {
+// One CTA of the dk/dv work: key tile kt of KV head gkv, from CTA index bid.
+__device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                         const CUtensorMap& tm_v, const CUtensorMap& tm_g,
+                                         const BwdParams& p, int bid) {
   extern __shared__ uint8_t smem_raw[];
   DkdvSmem& s = *reinterpret_cast<DkdvSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(
   // Key tiles in ascending order, KV heads minor: under a causal mask the
   // early key tiles meet the most query tiles, so the heaviest CTAs are
   // launched first and the light ones fill in behind them.
-  const int kt = blockIdx.x / a.Hkv, gkv = blockIdx.x % a.Hkv;
+  const int kt = bid / a.Hkv, gkv = bid % a.Hkv;
   const int group = a.Hq / a.Hkv;
   volatile int* abort_flag = &s.abort;
   const uint64_t lim = wait_limit(a);
@@ -394,10 +396,10 @@ constexpr size_t kDqSmem = sizeof(DqSmem) + 1024;
 
 constexpr uint32_t kColDQ = 256;
 
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-    const BwdParams p) {
+// One CTA of the dq work: query tile qt of query head h, from CTA index bid.
+__device__ __forceinline__ void dq_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                       const CUtensorMap& tm_v, const CUtensorMap& tm_g,
+                                       const BwdParams& p, int bid) {
   extern __shared__ uint8_t smem_raw[];
   DqSmem& s = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                          ~uintptr_t(1023));
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Query tiles in descending order, heads minor: later query tiles see the
   // most key tiles under a causal mask, so they are launched first.
-  const int qt = p.n_qtiles - 1 - (int)(blockIdx.x / a.Hq), h = blockIdx.x % a.Hq;
+  const int qt = p.n_qtiles - 1 - bid / a.Hq, h = bid % a.Hq;
   const int gkv = h / (a.Hq / a.Hkv);
   volatile int* abort_flag = &s.abort;
   const uint64_t lim = wait_limit(a);
@@ -599,6 +601,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(
   if (threadIdx.x == 0 && s.abort) report_status(a.dev_status, CPATTN_ERR_TIMEOUT);
 }
 
+// dk/dv and dq in one launch: the two are independent, and each alone is
+// 1.7 waves of CTAs on 152 SMs, so the dq CTAs (listed after the dk/dv
+// ones, heaviest first in each part) fill the SMs that the dk/dv tail
+// leaves idle.
+constexpr size_t kBwdSmem = kDkdvSmem > kDqSmem ? kDkdvSmem : kDqSmem;
+
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+    const BwdParams p) {
+  const int n_dkdv = p.n_ktiles * p.a.Hkv;
+  if ((int)blockIdx.x < n_dkdv) dkdv_cta(tm_q, tm_k, tm_v, tm_g, p, (int)blockIdx.x);
+  else dq_cta(tm_q, tm_k, tm_v, tm_g, p, (int)blockIdx.x - n_dkdv);
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
@@ -650,14 +667,10 @@ cudaError_t launch_dense_bwd(const cpattn_attn_args& a, const void* g, int64_t g
   bwd_prep_kernel<<<(unsigned)((prep_threads + 255) / 256), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_dkdv_kernel), (int)kDkdvSmem);
+  e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_kernel), (int)kBwdSmem);
   if (e != cudaSuccess) return e;
-  e = ensure_smem_attr(reinterpret_cast<const void*>(bwd_dq_kernel), (int)kDqSmem);
-  if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<<<(unsigned)(p.n_ktiles * a.Hkv), kBwdThreads, kDkdvSmem, stream>>>(tq, tk, tv, tg, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  bwd_dq_kernel<<<(unsigned)(p.n_qtiles * a.Hq), kBwdThreads, kDqSmem, stream>>>(tq, tk, tv, tg, p);
+  const unsigned grid = (unsigned)(p.n_ktiles * a.Hkv + p.n_qtiles * a.Hq);
+  bwd_kernel<<<grid, kBwdThreads, kBwdSmem, stream>>>(tq, tk, tv, tg, p);
   return cudaGetLastError();
 }
 

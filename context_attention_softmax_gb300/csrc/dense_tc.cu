@@ -90,15 +90,43 @@ struct Smem {
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
 
-// Finalised summary of one chunk for this thread's row: z from the 128 O
-// columns at o_col (every lane of the warp loads; rows past Tq store nothing).
+// Per softmax warp, a staging slice for its rows' partial summaries: 32 rows
+// x 16 columns with a row stride of 20 floats (a lane's four 16-byte writes
+// and the eight-lane phases of the reads fall on distinct banks).
+constexpr int kStageCols = 16, kStageStride = 20;
+constexpr size_t kStageBytes = 8 * 32 * kStageStride * sizeof(float);
+constexpr size_t kStageOffset = (sizeof(Smem) + 15) / 16 * 16;   // from the 1024-aligned base
+constexpr size_t kSmemBytesChunks = kStageOffset + kStageBytes + 1024;
+static_assert(kSmemBytesChunks <= 232448, "shared memory budget");
+
+// Finalised summary of one chunk for the warp's 32 rows (one per lane): z
+// from the 128 O columns at o_col, scaled by 1/l.  Every lane loads its row
+// from TMEM; 16 columns at a time go through the warp's staging slice, and
+// lane L then stores columns 4 (L % 4) .. + 3 of row 8 j + L / 4, so one
+// store instruction writes eight rows' 64 contiguous bytes instead of 32
+// rows' scattered 16-byte pieces.  Rows past Tq store nothing.  Called by
+// all lanes of the warp together; ends with the rows written and visible to
+// the whole warp.
 __device__ __forceinline__ void write_partial(const cpattn_attn_args& a, int c, int64_t tok, int h,
-                                              uint32_t o_col, float l, float m2, bool from_tmem) {
+                                              uint32_t o_col, float l, float m2, bool from_tmem,
+                                              float (*stage)[kStageStride]) {
+  const int lane = threadIdx.x & 31;
   const bool live = from_tmem && l > 0.f;
   const float inv = live ? 1.f / l : 0.f;
+  const bool valid = tok < a.Tq;
   const int64_t row = ((int64_t)c * a.Tq + tok) * a.Hq + h;
   float* po = a.partial_o + row * HD;
+  // the rows this lane stores: 8 j + lane / 4, j = 0..3
+  float* dst[4];
+  bool dst_ok[4];
 #pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int src = 8 * j + (lane >> 2);
+    dst[j] = reinterpret_cast<float*>(
+        __shfl_sync(kFullMask, reinterpret_cast<unsigned long long>(po), src)) + 4 * (lane & 3);
+    dst_ok[j] = __shfl_sync(kFullMask, valid, src);
+  }
+#pragma unroll 1
   for (int c4 = 0; c4 < HD / 32; ++c4) {
     uint32_t oo[32];
     if (from_tmem) {
@@ -107,16 +135,26 @@ __device__ __forceinline__ void write_partial(const cpattn_attn_args& a, int c, 
 #pragma unroll
       for (int i = 0; i < 32; ++i) oo[i] = 0u;
     }
-    if (tok < a.Tq) {
 #pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(po + c4 * 32 + i) =
-            make_float4(__uint_as_float(oo[i]) * inv, __uint_as_float(oo[i + 1]) * inv,
-                        __uint_as_float(oo[i + 2]) * inv, __uint_as_float(oo[i + 3]) * inv);
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int i = 0; i < kStageCols; i += 4)
+        *reinterpret_cast<float4*>(&stage[lane][i]) =
+            make_float4(__uint_as_float(oo[16 * half + i]) * inv,
+                        __uint_as_float(oo[16 * half + i + 1]) * inv,
+                        __uint_as_float(oo[16 * half + i + 2]) * inv,
+                        __uint_as_float(oo[16 * half + i + 3]) * inv);
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(&stage[8 * j + (lane >> 2)][4 * (lane & 3)]);
+        if (dst_ok[j]) *reinterpret_cast<float4*>(dst[j] + c4 * 32 + kStageCols * half) = v;
+      }
+      __syncwarp();
     }
   }
-  if (tok < a.Tq)
-    a.partial_lse[row] = live ? (m2 + log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+  if (valid) a.partial_lse[row] = live ? (m2 + log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
+  __syncwarp();   // orders the rows' stores before the lanes' own reads of them
 }
 
 template <bool CHUNKS>
@@ -399,6 +437,9 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_base + kColS + X * BN;
     const uint32_t o_col = tmem + lane_base + kColO + X * HD;
+    // CHUNKS: this warp's staging slice (softmax warps 4..11) after the Smem block
+    float (*stage)[kStageStride] = reinterpret_cast<float (*)[kStageStride]>(
+        reinterpret_cast<uint8_t*>(&s) + kStageOffset + (size_t)(warp - 4) * 32 * kStageStride * sizeof(float));
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in exp2 units
     float m2 = -CUDART_INF_F, l = 0.f;
     int jt = 0;
@@ -438,11 +479,11 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               if (!ok) break;
               tc_fence_after();
             }
-            write_partial(a, cur_c, tok_row, my_head, o_col, l, m2, true);
+            write_partial(a, cur_c, tok_row, my_head, o_col, l, m2, true, stage);
             ++cur_c;
           }
           for (; cur_c < c_tile; ++cur_c)
-            write_partial(a, cur_c, tok_row, my_head, o_col, 0.f, 0.f, false);
+            write_partial(a, cur_c, tok_row, my_head, o_col, 0.f, 0.f, false, stage);
           m2 = -CUDART_INF_F;
           l = 0.f;
         }
@@ -537,10 +578,10 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // this row's partials: L = max_c LSE_c, w_c = exp(LSE_c - L),
       // O = sum_c w_c O_c / sum_c w_c, LSE = L + ln sum_c w_c
       if (ok && jt > 0) {
-        write_partial(a, cur_c, tok, h, o_col, l, m2, true);
+        write_partial(a, cur_c, tok, h, o_col, l, m2, true, stage);
         ++cur_c;
       }
-      for (; cur_c < p.n_parts; ++cur_c) write_partial(a, cur_c, tok, h, o_col, 0.f, 0.f, false);
+      for (; cur_c < p.n_parts; ++cur_c) write_partial(a, cur_c, tok, h, o_col, 0.f, 0.f, false, stage);
       if (tok < a.Tq && a.o != nullptr) {   // o == NULL: the partial summaries only
         const int64_t stride = (int64_t)a.Tq * a.Hq;
         const int64_t row0 = tok * a.Hq + h;
@@ -658,9 +699,10 @@ cudaError_t launch_dense_tc(const cpattn_attn_args& a, cudaStream_t stream, bool
   p.part_tiles = a.kv_chunk_len > 0 ? a.kv_chunk_len / BN : 1;
   p.n_parts = a.kv_chunk_len > 0 ? (a.Tk + a.kv_chunk_len - 1) / a.kv_chunk_len : 1;
   auto kern = a.kv_chunk_len > 0 ? dense_tc_kernel<true> : dense_tc_kernel<false>;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)kSmemBytes);
+  const size_t smem = a.kv_chunk_len > 0 ? kSmemBytesChunks : kSmemBytes;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)p.n_units, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  kern<<<(unsigned)p.n_units, kThreads, smem, stream>>>(tq, tk, tv, p);
   *launched = true;
   return cudaGetLastError();
 }

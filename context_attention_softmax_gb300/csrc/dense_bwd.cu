@@ -336,8 +336,15 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
     const bool have = ok && n_steps > 0 &&
                       __all_sync(kFullMask, mbar_wait(&s.acc_done, 0, abort_flag, lim));
     if (have) tc_fence_after();
+    // Stores go row-contiguously through a staging slice per warp in the
+    // first query tile buffer, which no copy or MMA touches any more once
+    // acc_done has completed; without it (abort or no step) rows are written
+    // directly.
     float* dvrow = p.dv + jrow * p.dv_st + (int64_t)gkv * p.dv_sh;
     float* dkrow = p.dk + jrow * p.dk_st + (int64_t)gkv * p.dk_sh;
+    float (*stage)[kStageStride] =
+        reinterpret_cast<float (*)[kStageStride]>(s.q[0] + (size_t)(warp - 4) * kStageSliceBytes);
+    const StagedRows tv = staged_rows(dvrow, key_ok), tk = staged_rows(dkrow, key_ok);
 #pragma unroll 1
     for (int c2 = 0; c2 < 2; ++c2) {
       const int c4 = 2 * hc + c2;
@@ -346,19 +353,13 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
         tmem_ld32(tmem + lane_base + kColDV + 32 * c4, vv);
         tmem_ld32(tmem + lane_base + kColDK + 32 * c4, kk);
         tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) vv[i] = kk[i] = 0u;
-      }
-      if (key_ok) {
+        store_rows32(stage, tv, vv, 1.f, 32 * c4);
+        store_rows32(stage, tk, kk, a.scale, 32 * c4);
+      } else if (key_ok) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          *reinterpret_cast<float4*>(dvrow + 32 * c4 + i) =
-              make_float4(__uint_as_float(vv[i]), __uint_as_float(vv[i + 1]),
-                          __uint_as_float(vv[i + 2]), __uint_as_float(vv[i + 3]));
-          *reinterpret_cast<float4*>(dkrow + 32 * c4 + i) =
-              make_float4(__uint_as_float(kk[i]) * a.scale, __uint_as_float(kk[i + 1]) * a.scale,
-                          __uint_as_float(kk[i + 2]) * a.scale, __uint_as_float(kk[i + 3]) * a.scale);
+          *reinterpret_cast<float4*>(dvrow + 32 * c4 + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(dkrow + 32 * c4 + i) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
     }
@@ -566,7 +567,12 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_q, const CUtensorMa
     const bool have = ok && n_steps > 0 &&
                       __all_sync(kFullMask, mbar_wait(&s.acc_done, 0, abort_flag, lim));
     if (have) tc_fence_after();
+    // row-contiguous stores through a staging slice per warp in the first
+    // key tile buffer (idle once acc_done has completed), as for dk and dv
     float* dqrow = p.dq + qi * p.dq_st + (int64_t)h * p.dq_sh;
+    float (*stage)[kStageStride] =
+        reinterpret_cast<float (*)[kStageStride]>(s.k[0] + (size_t)(warp - 4) * kStageSliceBytes);
+    const StagedRows tq = staged_rows(dqrow, qi < a.Tq);
 #pragma unroll 1
     for (int c2 = 0; c2 < 2; ++c2) {                      // channels [64 hc, 64 hc + 64)
       const int c4 = 2 * hc + c2;
@@ -574,16 +580,11 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_q, const CUtensorMa
       if (have) {
         tmem_ld32(tmem + lane_base + kColDQ + 32 * c4, qq);
         tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) qq[i] = 0u;
-      }
-      if (qi < a.Tq) {
+        store_rows32(stage, tq, qq, a.scale, 32 * c4);
+      } else if (qi < a.Tq) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(dqrow + 32 * c4 + i) =
-              make_float4(__uint_as_float(qq[i]) * a.scale, __uint_as_float(qq[i + 1]) * a.scale,
-                          __uint_as_float(qq[i + 2]) * a.scale, __uint_as_float(qq[i + 3]) * a.scale);
+          *reinterpret_cast<float4*>(dqrow + 32 * c4 + i) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
   }

@@ -90,42 +90,26 @@ struct Smem {
 
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment slack
 
-// Per softmax warp, a staging slice for its rows' partial summaries: 32 rows
-// x 16 columns with a row stride of 20 floats (a lane's four 16-byte writes
-// and the eight-lane phases of the reads fall on distinct banks).
-constexpr int kStageCols = 16, kStageStride = 20;
-constexpr size_t kStageBytes = 8 * 32 * kStageStride * sizeof(float);
+// Per softmax warp, a staging slice (store_rows32) for its rows' partial
+// summaries, after the Smem block.
+constexpr size_t kStageBytes = 8 * kStageSliceBytes;
 constexpr size_t kStageOffset = (sizeof(Smem) + 15) / 16 * 16;   // from the 1024-aligned base
 constexpr size_t kSmemBytesChunks = kStageOffset + kStageBytes + 1024;
 static_assert(kSmemBytesChunks <= 232448, "shared memory budget");
 
 // Finalised summary of one chunk for the warp's 32 rows (one per lane): z
-// from the 128 O columns at o_col, scaled by 1/l.  Every lane loads its row
-// from TMEM; 16 columns at a time go through the warp's staging slice, and
-// lane L then stores columns 4 (L % 4) .. + 3 of row 8 j + L / 4, so one
-// store instruction writes eight rows' 64 contiguous bytes instead of 32
-// rows' scattered 16-byte pieces.  Rows past Tq store nothing.  Called by
+// from the 128 O columns at o_col, scaled by 1/l, stored row-contiguously
+// through the warp's staging slice.  Rows past Tq store nothing.  Called by
 // all lanes of the warp together; ends with the rows written and visible to
 // the whole warp.
 __device__ __forceinline__ void write_partial(const cpattn_attn_args& a, int c, int64_t tok, int h,
                                               uint32_t o_col, float l, float m2, bool from_tmem,
                                               float (*stage)[kStageStride]) {
-  const int lane = threadIdx.x & 31;
   const bool live = from_tmem && l > 0.f;
   const float inv = live ? 1.f / l : 0.f;
   const bool valid = tok < a.Tq;
   const int64_t row = ((int64_t)c * a.Tq + tok) * a.Hq + h;
-  float* po = a.partial_o + row * HD;
-  // the rows this lane stores: 8 j + lane / 4, j = 0..3
-  float* dst[4];
-  bool dst_ok[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int src = 8 * j + (lane >> 2);
-    dst[j] = reinterpret_cast<float*>(
-        __shfl_sync(kFullMask, reinterpret_cast<unsigned long long>(po), src)) + 4 * (lane & 3);
-    dst_ok[j] = __shfl_sync(kFullMask, valid, src);
-  }
+  const StagedRows t = staged_rows(a.partial_o + row * HD, valid);
 #pragma unroll 1
   for (int c4 = 0; c4 < HD / 32; ++c4) {
     uint32_t oo[32];
@@ -135,23 +119,7 @@ __device__ __forceinline__ void write_partial(const cpattn_attn_args& a, int c, 
 #pragma unroll
       for (int i = 0; i < 32; ++i) oo[i] = 0u;
     }
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-      for (int i = 0; i < kStageCols; i += 4)
-        *reinterpret_cast<float4*>(&stage[lane][i]) =
-            make_float4(__uint_as_float(oo[16 * half + i]) * inv,
-                        __uint_as_float(oo[16 * half + i + 1]) * inv,
-                        __uint_as_float(oo[16 * half + i + 2]) * inv,
-                        __uint_as_float(oo[16 * half + i + 3]) * inv);
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float4 v = *reinterpret_cast<const float4*>(&stage[8 * j + (lane >> 2)][4 * (lane & 3)]);
-        if (dst_ok[j]) *reinterpret_cast<float4*>(dst[j] + c4 * 32 + kStageCols * half) = v;
-      }
-      __syncwarp();
-    }
+    store_rows32(stage, t, oo, inv, c4 * 32);
   }
   if (valid) a.partial_lse[row] = live ? (m2 + log2f(l)) * 0.6931471805599453f : -CUDART_INF_F;
   __syncwarp();   // orders the rows' stores before the lanes' own reads of them
@@ -439,7 +407,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const uint32_t o_col = tmem + lane_base + kColO + X * HD;
     // CHUNKS: this warp's staging slice (softmax warps 4..11) after the Smem block
     float (*stage)[kStageStride] = reinterpret_cast<float (*)[kStageStride]>(
-        reinterpret_cast<uint8_t*>(&s) + kStageOffset + (size_t)(warp - 4) * 32 * kStageStride * sizeof(float));
+        reinterpret_cast<uint8_t*>(&s) + kStageOffset + (size_t)(warp - 4) * kStageSliceBytes);
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in exp2 units
     float m2 = -CUDART_INF_F, l = 0.f;
     int jt = 0;

@@ -85,6 +85,59 @@ __device__ __forceinline__ Block folded_block_of(int Hq, int n_qtiles, int u, in
   return Block{2 * pr + X, (X ? n_qtiles - 1 - t : t) * BM};
 }
 
+// Row-contiguous stores of one warp's rows (lane = row, fp32 values held per
+// lane) through a staging slice of shared memory: 32 rows x 16 columns with
+// a row stride of 20 floats, so that a lane's four 16-byte writes and the
+// eight-lane phases of the reads fall on distinct banks.  Lane L then stores
+// columns 4 (L % 4) .. + 3 of row 8 j + L / 4: one store instruction writes
+// eight rows' 64 contiguous bytes instead of 32 rows' scattered 16-byte
+// pieces.  Every lane of the warp calls these together.
+constexpr int kStageStride = 20;
+constexpr size_t kStageSliceBytes = 32 * kStageStride * sizeof(float);
+
+struct StagedRows {
+  float* dst[4];   // rows 8 j + lane / 4, already offset by 4 (lane % 4) columns
+  bool ok[4];
+};
+
+__device__ __forceinline__ StagedRows staged_rows(float* row, bool row_ok) {
+  const int lane = threadIdx.x & 31;
+  StagedRows t;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int src = 8 * j + (lane >> 2);
+    t.dst[j] = reinterpret_cast<float*>(
+                   __shfl_sync(kFullMask, reinterpret_cast<unsigned long long>(row), src)) +
+               4 * (lane & 3);
+    t.ok[j] = __shfl_sync(kFullMask, row_ok, src);
+  }
+  return t;
+}
+
+// Columns col0 .. col0 + 31 of the warp's rows: v (this lane's row) x mul.
+// Ends with the stage free again; __syncwarp orders the stores for the warp.
+__device__ __forceinline__ void store_rows32(float (*stage)[kStageStride], const StagedRows& t,
+                                             const uint32_t (&v)[32], float mul, int col0) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 4)
+      *reinterpret_cast<float4*>(&stage[lane][i]) =
+          make_float4(__uint_as_float(v[16 * half + i]) * mul,
+                      __uint_as_float(v[16 * half + i + 1]) * mul,
+                      __uint_as_float(v[16 * half + i + 2]) * mul,
+                      __uint_as_float(v[16 * half + i + 3]) * mul);
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 x = *reinterpret_cast<const float4*>(&stage[8 * j + (lane >> 2)][4 * (lane & 3)]);
+      if (t.ok[j]) *reinterpret_cast<float4*>(t.dst[j] + col0 + 16 * half) = x;
+    }
+    __syncwarp();
+  }
+}
+
 // [rows, heads, 128] bf16 with element strides (st_t, st_h); box = 64 x 1 x 128.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int64_t st_t,
               int64_t st_h) {

@@ -428,6 +428,17 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         mbar_arrive(&s.p_full[gj & 1]);
       }
       if (!ok) break;
+      {   // this head's channels 0..255 of the next item's query, into L2 while
+          // the epilogue runs: the TMEM fill that follows then reads L2
+        const int nx = it + (int)gridDim.x;
+        if (nx < p.n_items) {
+          const char* nq = reinterpret_cast<const char*>(
+              reinterpret_cast<const __nv_bfloat16*>(a.q) + (int64_t)(nx >> 1) * a.q_stride_t +
+              (int64_t)r * a.q_stride_h);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(nq + 128 * k));
+        }
+      }
       ok = __all_sync(kFullMask, mbar_wait(&s.o_full, ui & 1, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();

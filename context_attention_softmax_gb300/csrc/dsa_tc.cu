@@ -94,9 +94,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&t);
 }
 
-// Roles (384 threads): warp 0 Q loader (TMA, channels 256..575), warp 1 MMA
-// issuer + TMEM owner, warps 2-3 and 8-11 key-row gather, warps 4-7
-// softmax, Q^T TMEM fill and epilogue (row = head).
+// Roles (384 threads): warp 9 Q loader (TMA, channels 256..575), warp 1 MMA
+// issuer + TMEM owner, warps 0, 2, 3, 8, 10, 11 key-row gather, warps 4-7
+// softmax, Q^T TMEM fill and epilogue (row = head).  Warp w runs on
+// sub-partition w % 4: the MMA thread's (1) holds only a softmax warp and
+// the light Q loader besides it.
 __global__ void __launch_bounds__(kThreads, 1)
 dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -128,7 +130,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
     s.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_q);
+  if (warp == 9 && lane == 0) tma_prefetch_desc(&tm_q);
   if (warp == 1) {
     tmem_alloc(&s.tmem_base, kTmemCols);
     tmem_relinquish();
@@ -139,7 +141,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
   const uint32_t tmem = s.tmem_base;
   const int T = p.n_tiles;
 
-  if (warp == 0) {
+  if (warp == 9) {
     // ------------------------------------------------------------ Q channels 256..575
     if (lane == 0) {
       int ui = 0;
@@ -156,18 +158,20 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         mbar_wait(&s.qs_full, ui & 1, &no_abort, 200000000ull);
       }
     }
-  } else if (warp == 2 || warp == 3 || warp >= 8) {
+  } else if (warp == 0 || warp == 2 || warp == 3 || warp == 8 || warp == 10 || warp == 11) {
     // ------------------------------------------------------------ key-row gather
     // A stage is filled in two parts with their own barriers: part A (the
     // five 64-channel chunks that this half's PV does not read) is free again
     // as soon as S is done, part B (the four value chunks 4c..4c+3) only
-    // after PV.  Warps 2, 3, 8 fetch part A and warps 9-11 part B, so part A
-    // of the next tiles never queues behind a part B that waits for PV.  A
+    // after PV.  Warps 0, 2, 3 fetch part A and warps 8, 10, 11 part B, so
+    // part A of the next tiles never queues behind a part B that waits for
+    // PV; none of them shares a sub-partition with the MMA thread (warp 1),
+    // whose issue slots the copies' address arithmetic would take.  A
     // warp takes key slots w, w + 3, ... and its lanes copy consecutive
     // 16-byte pieces of the row (whole 32-byte sectors).  The barriers are
     // arrived on by the copies themselves when they land.
-    const bool part_a = warp <= 3 || warp == 8;
-    const int gw = warp <= 3 ? warp - 2 : (warp == 8 ? 2 : warp - 9);   // 0..2
+    const bool part_a = warp <= 3;
+    const int gw = (warp == 0 || warp == 8) ? 0 : (part_a ? warp - 1 : warp - 9);   // 0..2
     const __nv_bfloat16* kbase = reinterpret_cast<const __nv_bfloat16*>(a.k);
     uint64_t* empty = part_a ? s.ka_empty : s.kb_empty;
     uint64_t* full = part_a ? s.ka_full : s.kb_full;

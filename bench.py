@@ -67,22 +67,22 @@ L2_NOTE = "flushed by a 256 MiB write before every timed step"
 # dominant kernel from one ncu capture (summarised under profiles/), valid
 # only while the kernel's sources hash to the value they had then.
 TRAFFIC = {
-    "dense_gqa": {"bytes": 21_195_264 + 0, "kernel": "dense_tc_kernel",
+    "dense_gqa": {"bytes": 21_194_496 + 0, "kernel": "dense_tc_kernel<0>",
                   "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                  "sha": "41f85c8be9eca783"},
-    "dense_gqa_4chunks": {"bytes": 21_157_376 + 13_576_448, "kernel": "dense_tc_kernel<1>",
+                  "sha": "4b0c149101c5a7cc"},
+    "dense_gqa_4chunks": {"bytes": 21_081_856 + 13_488_640, "kernel": "dense_tc_kernel<1>",
                           "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh",
                                       "common.cuh"],
-                          "sha": "41f85c8be9eca783"},
-    "dsa": {"bytes": 661_784_576 + 506_544_128, "kernel": "dsa_attn_kernel",
-            "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "6d9adf29f0d1fc91"},
+                          "sha": "4b0c149101c5a7cc"},
+    "dsa": {"bytes": 662_260_736 + 506_345_216, "kernel": "dsa_attn_kernel",
+            "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "f09990023241a7b9"},
     "mla_kv": {"bytes": 566_199_296 + 2_627_799_552, "kernel": "mla_kv_kernel",
                "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "7694db41bfcf00d2"},
     "mla_v_up": {"bytes": 553_843_456 + 112_686_336, "kernel": "mla_gemm_kernel<1>",
                  "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "7694db41bfcf00d2"},
-    "dense_gqa_bwd": {"bytes": 29_792_256 + 205_056, "kernel": "bwd_dkdv_kernel",
+    "dense_gqa_bwd": {"bytes": 30_985_472 + 6_564_608, "kernel": "bwd_kernel",
                       "sources": ["dense_bwd.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                      "sha": "6e468e42c43df353"},
+                      "sha": "ee19e0b8b42dce2a"},
     "moba": {"bytes": 1_156_865_536 + 259_025_664, "kernel": "moba_attn_kernel",
              "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "4bd05f662df3ed35"},
 }

@@ -77,9 +77,9 @@ TRAFFIC = {
     "dsa": {"bytes": 662_260_736 + 506_345_216, "kernel": "dsa_attn_kernel",
             "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "f09990023241a7b9"},
     "mla_kv": {"bytes": 566_199_296 + 2_627_799_552, "kernel": "mla_kv_kernel",
-               "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "7694db41bfcf00d2"},
+               "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "473aca57ddd7ce60"},
     "mla_v_up": {"bytes": 553_843_456 + 112_686_336, "kernel": "mla_gemm_kernel<1>",
-                 "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "7694db41bfcf00d2"},
+                 "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "473aca57ddd7ce60"},
     "dense_gqa_bwd": {"bytes": 30_985_472 + 6_564_608, "kernel": "bwd_kernel",
                       "sources": ["dense_bwd.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
                       "sha": "ee19e0b8b42dce2a"},

@@ -441,8 +441,6 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
   if (threadIdx.x == 0 && s.abort) report_status(p.dev_status, CPATTN_ERR_TIMEOUT);
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 cudaError_t launch_v_up(const GemmParams& p, const CUtensorMap& ta, const CUtensorMap& tb,
                         cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(mla_gemm_kernel<1>),

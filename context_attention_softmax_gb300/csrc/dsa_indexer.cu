@@ -30,6 +30,7 @@
 //     float64 and the best k - |in| of them join, ties to the lower key.
 #include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace cpattn {
 namespace {
@@ -147,11 +148,18 @@ idx_score_kernel(const cpattn_attn_args a, const float* __restrict__ w, float* _
     }
   };
 
-  float sc[8][8], acc[8][8];
+  // acc2[i][jp] holds the dots of row i with columns 2 jp and 2 jp + 1 as a
+  // packed pair: one f32x2 fma does both (each lane an ordinary fp32 fma,
+  // so every dot still accumulates over d in order).
+  float sc[8][8];
+  uint64_t acc2[8][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 8; ++i) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) sc[i][j] = acc[i][j] = 0.f;
+    for (int j = 0; j < 8; ++j) sc[i][j] = 0.f;
+#pragma unroll
+    for (int jp = 0; jp < 4; ++jp) acc2[i][jp] = 0ull;
+  }
   load(0);
   for (int c = 0; c < nc; ++c) {
     const int buf = c & 1;
@@ -165,20 +173,26 @@ idx_score_kernel(const cpattn_attn_args a, const float* __restrict__ w, float* _
       const float4 b0 = *reinterpret_cast<const float4*>(&s.b[buf][d][tx * 4]);
       const float4 b1 = *reinterpret_cast<const float4*>(&s.b[buf][d][64 + tx * 4]);
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const uint64_t bp[4] = {sm100::f2_pack(b0.x, b0.y), sm100::f2_pack(b0.z, b0.w),
+                              sm100::f2_pack(b1.x, b1.y), sm100::f2_pack(b1.z, b1.w)};
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+      for (int i = 0; i < 8; ++i) {
+        const uint64_t ai = sm100::f2_pack(av[i], av[i]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int jp = 0; jp < 4; ++jp) acc2[i][jp] = sm100::f2_fma(ai, bp[jp], acc2[i][jp]);
+      }
     }
     if ((c + 1) % nd == 0) {   // a head's dots are complete: relu, weight, add
       const float wh = w[c / nd];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          sc[i][j] = fmaf(wh, fmaxf(acc[i][j], 0.f), sc[i][j]);
-          acc[i][j] = 0.f;
+        for (int jp = 0; jp < 4; ++jp) {
+          float d0, d1;
+          sm100::f2_unpack(acc2[i][jp], d0, d1);
+          sc[i][2 * jp] = fmaf(wh, fmaxf(d0, 0.f), sc[i][2 * jp]);
+          sc[i][2 * jp + 1] = fmaf(wh, fmaxf(d1, 0.f), sc[i][2 * jp + 1]);
+          acc2[i][jp] = 0ull;
         }
     }
   }

@@ -285,7 +285,7 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_3d(s.v[st] + kHalf, &tm_v, &s.v_full[st], 64, g, kt * BN);
         ++v_issued;
       }
-      if (*abort_flag, lim) {  // let every copy in flight land before the CTA exits
+      if (*abort_flag) {  // let every copy in flight land before the CTA exits
         int no_abort = 0;
         if (q_issued) mbar_wait(&s.q_full, 0, &no_abort, 200000000ull);
         for (int j = max(0, k_issued - NS); j < k_issued; ++j)

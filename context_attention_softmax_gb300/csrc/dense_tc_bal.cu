@@ -568,7 +568,7 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           ++gj;
         }
       }
-      if (*abort_flag, lim) {  // let every copy in flight land before the CTA exits
+      if (*abort_flag) {  // let every copy in flight land before the CTA exits
         int no_abort = 0;
         if (pc > 0) mbar_wait(&s.q_full, (pc - 1) & 1, &no_abort, 200000000ull);
         for (int j = max(0, k_issued - NS); j < k_issued; ++j)

@@ -208,7 +208,7 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tma_load_3d(s.q[st][0], &tm_q, &s.q_full[st], 0, h, qt * GM);
         tma_load_3d(s.q[st][1], &tm_q, &s.q_full[st], 64, h, qt * GM);
       }
-      if (*abort_flag, lim) {   // let copies in flight land before the CTA exits
+      if (*abort_flag) {   // let copies in flight land before the CTA exits
         int no_abort = 0;
         if (n_mu > 0) mbar_wait(&s.mu_full, (n_mu - 1) & 1, &no_abort, 200000000ull);
         for (int j = max(0, ti - 2); j < ti; ++j)

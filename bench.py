@@ -36,6 +36,7 @@ inputs copied in and the outputs copied out inside each step.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import platform
@@ -649,52 +650,100 @@ def hbm_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled in the background."""
+    """nvidia-smi clocks and throttle reasons sampled in the background.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    start() returns once nvidia-smi has written its first sample, so the
+    sampler is running before the timed steps begin; mark() records the host
+    time at the start and at the end of the timed steps; stop() waits for
+    one sample after the end and reports the samples inside that window,
+    widened to the nearest sample on either side when the window is shorter
+    than the sampling interval (a few-millisecond timed region)."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.proc = None
         self.gpu = gpu_index
+        self.window = [None, None]
+
+    def _rows(self):
+        self.f.flush()
+        with open(self.f.name) as fh:
+            rows = [r.split(",") for r in fh.read().strip().splitlines() if r.count(",") >= 9]
+        out = []
+        for r in rows:
+            try:
+                sm, smax = float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            try:   # host time of the sample; None if the format is not the expected one
+                t = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                t = None
+            out.append((t, sm, smax, [v.strip().lower() for v in r[6:10]]))
+        return out
+
+    def _wait_rows(self, pred, timeout_s):
+        t_end = time.time() + timeout_s
+        while time.time() < t_end:
+            if pred(self._rows()):
+                return True
+            time.sleep(0.01)
+        return False
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+            return
+        self._wait_rows(lambda rows: len(rows) > 0, 5.0)
+
+    def mark(self, which):
+        self.window[which] = time.time()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        t0, t1 = self.window
+        if t1 is not None:   # one sample after the timed steps
+            self._wait_rows(lambda rows: any(t is not None and t > t1 for t, *_ in rows), 2.0)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        self.f.flush()
-        self.f.seek(0)
-        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.count(",") >= 8]
+        rows = self._rows()
         os.unlink(self.f.name)
-        sm, smax, reasons = [], [], set()
+        timed = [r for r in rows if r[0] is not None]
+        have_window = t0 is not None and t1 is not None
+        inside = [r for r in timed if have_window and t0 <= r[0] <= t1]
+        chosen = inside
+        if not inside and have_window:
+            before = [r for r in timed if r[0] < t0][-1:]
+            after = [r for r in timed if r[0] > t1][:1]
+            chosen = before + after
+        if not chosen:
+            chosen = rows
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-            except ValueError:
-                continue
-            for n, val in zip(names, r[5:9]):
-                if val.strip().lower() == "active":
+        reasons = set()
+        for _, _, _, flags in chosen:
+            for n, val in zip(names, flags):
+                if val == "active":
                     reasons.add(n)
+        sm = [r[1] for r in chosen]
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_max_mhz": max(r[2] for r in chosen) if chosen else None,
+                "reasons": sorted(reasons), "samples": len(chosen),
+                "samples_in_timed_region": len(inside),
+                "timed_region_ms": None if t0 is None or t1 is None else round(1e3 * (t1 - t0), 2)}
 
 
 def dist_setup():
@@ -726,8 +775,11 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
-def time_steps(fn, steps, warmup, flush, world):
-    """Per-step device times (ms) of `steps` timed calls of fn, L2 flushed before each."""
+def time_steps(fn, steps, warmup, flush, world, marks=None):
+    """Per-step device times (ms) of `steps` timed calls of fn, L2 flushed before each.
+
+    marks(0) / marks(1), if given, are called on the host right before the
+    first timed step is enqueued and right after the last one has finished."""
     for _ in range(warmup):
         fn()
     stream = torch.cuda.current_stream()
@@ -739,12 +791,16 @@ def time_steps(fn, steps, warmup, flush, world):
     # enqueued the first step before the GPU reaches it
     for _ in range(16):
         flush.zero_()
+    if marks is not None:
+        marks(0)
     for s in range(steps):
         flush.zero_()
         ev[s][0].record(stream)
         fn()
         ev[s][1].record(stream)
     torch.cuda.synchronize()
+    if marks is not None:
+        marks(1)
     barrier(world)
     return [a.elapsed_time(b) for a, b in ev]
 
@@ -828,7 +884,8 @@ def measure(runner, args, world, dev, flush, with_cpu):
     ins = runner.device_inputs()
     clocks = ClockSampler(dev.index or 0)
     clocks.start()
-    times = time_steps(lambda: runner.step(*ins), args.steps, args.warmup, flush, world)
+    times = time_steps(lambda: runner.step(*ins), args.steps, args.warmup, flush, world,
+                       marks=clocks.mark)
     clk = clocks.stop()
     mean_ms = max_over_ranks(statistics.mean(times), world)
     rec = {

@@ -68,13 +68,13 @@ L2_NOTE = "flushed by a 256 MiB write before every timed step"
 # dominant kernel from one ncu capture (summarised under profiles/), valid
 # only while the kernel's sources hash to the value they had then.
 TRAFFIC = {
-    "dense_gqa": {"bytes": 21_194_496 + 0, "kernel": "dense_tc_kernel<0>",
+    "dense_gqa": {"bytes": 21_194_240 + 0, "kernel": "dense_tc_kernel<0>",
                   "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                  "sha": "4b0c149101c5a7cc"},
-    "dense_gqa_4chunks": {"bytes": 21_081_856 + 13_488_640, "kernel": "dense_tc_kernel<1>",
+                  "sha": "096fba09849c7b44"},
+    "dense_gqa_4chunks": {"bytes": 21_085_440 + 13_801_472, "kernel": "dense_tc_kernel<1>",
                           "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh",
                                       "common.cuh"],
-                          "sha": "4b0c149101c5a7cc"},
+                          "sha": "096fba09849c7b44"},
     "dsa": {"bytes": 662_260_736 + 506_345_216, "kernel": "dsa_attn_kernel",
             "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "f09990023241a7b9"},
     "mla_kv": {"bytes": 566_199_296 + 2_627_799_552, "kernel": "mla_kv_kernel",
@@ -84,6 +84,8 @@ TRAFFIC = {
     "dense_gqa_bwd": {"bytes": 30_985_472 + 6_564_608, "kernel": "bwd_kernel",
                       "sources": ["dense_bwd.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
                       "sha": "ee19e0b8b42dce2a"},
+    "dsa_indexer": {"bytes": 21_542_912 + 243_081_984, "kernel": "idx_score_kernel",
+                    "sources": ["dsa_indexer.cu", "sm100.cuh", "common.cuh"], "sha": "324f649f320c94c3"},
     "moba": {"bytes": 1_156_865_536 + 259_025_664, "kernel": "moba_attn_kernel",
              "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "4bd05f662df3ed35"},
 }

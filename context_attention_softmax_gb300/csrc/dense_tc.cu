@@ -296,10 +296,16 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One thread issues both blocks' MMAs in the ping-pong order
+    // The warp issues both blocks' MMAs in the ping-pong order
     //   S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
-    // MMAs from one thread execute in issue order.
-    if (lane == 0) {
+    // from one elected lane (MMAs from one thread execute in issue order).
+    // The whole warp runs the loop, converged, with every wait's outcome
+    // made warp-uniform: a converged issuer loses fewer issue slots to the
+    // softmax warps of its sub-partition than a single-lane branch.
+    {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);   // Q, K both K-major
       const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);   // P (TMEM), V MN-major
       // Descriptor low words: K-major Q and K step 32 B along K inside a
@@ -317,21 +323,21 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return s.live_kt[j] / p.part_tiles != s.live_kt[j - 1] / p.part_tiles;
       };
       auto issue_s = [&](int j, int x) {   // S_x(j) = Q_x K_j^T
-        umma8_ss_kmajor(tmem + kColS + x * BN, x ? q_lo1 : q_lo0, (j & 1) ? k_lo1 : k_lo0, idesc_qk);
-        umma_commit(&s.s_full[x]);
+        umma8_ss_kmajor<true>(tmem + kColS + x * BN, x ? q_lo1 : q_lo0, (j & 1) ? k_lo1 : k_lo0, idesc_qk);
+        umma_commit<true>(&s.s_full[x]);
       };
       auto issue_pv = [&](int j, int x) {  // O_x += P_x(j) V_j
         const uint32_t d = tmem + kColO + x * HD, pa = tmem + kColS + x * BN;
         const uint32_t vb = (j & 1) ? v_lo1 : v_lo0;
-        if (!opens_chunk(j)) umma8_ts_mnmajor<1>(d, pa, vb, idesc_pv);
-        else umma8_ts_mnmajor<0>(d, pa, vb, idesc_pv);
+        if (!opens_chunk(j)) umma8_ts_mnmajor<1, true>(d, pa, vb, idesc_pv);
+        else umma8_ts_mnmajor<0, true>(d, pa, vb, idesc_pv);
       };
-      bool ok = n > 0 && mbar_wait(&s.q_full, 0, abort_flag, lim) && mbar_wait(&s.k_full[0], 0, abort_flag, lim);
+      bool ok = n > 0 && wait_w(&s.q_full, 0) && wait_w(&s.k_full[0], 0);
       if (ok) {
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
           if ((x ? nx1 : nx0) > 0) issue_s(0, x);
-        umma_commit(&s.k_empty[0]);
+        umma_commit<true>(&s.k_empty[0]);
       }
       // Step jt: for each block still running, PV_X(jt) then S_X(jt+1).  A
       // block past its last tile drops out; the V stage is released after the
@@ -339,27 +345,27 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t q_lo_l = Lb ? q_lo1 : q_lo0;
       for (int jt = 0; jt < n && ok; ++jt) {
         const int st = jt & 1, st1 = (jt + 1) & 1;
-        if (!mbar_wait(&s.v_full[st], (jt >> 1) & 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.v_full[st], (jt >> 1) & 1)) { ok = false; break; }
         if (tail2 && jt >= n_short) {
           // tail step: PV(jt) from the buffer holding P(jt), then S(jt+2) into it
           const int u = jt - n_short, xb = (u & 1) ? Sb : Lb;
-          if (!mbar_wait(&s.p_full[xb], (n_short + (u >> 1)) & 1, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.p_full[xb], (n_short + (u >> 1)) & 1)) { ok = false; break; }
           tc_fence_after();
           if (CHUNKS && opens_chunk(jt))
-            umma8_ts_mnmajor<0>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
+            umma8_ts_mnmajor<0, true>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
                                 idesc_pv);
           else
-            umma8_ts_mnmajor<1>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
+            umma8_ts_mnmajor<1, true>(tmem + kColO + Lb * HD, tmem + kColS + xb * BN, st ? v_lo1 : v_lo0,
                                 idesc_pv);
-          umma_commit(&s.v_empty[st]);
-          umma_commit(&s.pv_done);
-          if (jt + 1 == n) umma_commit(&s.o_ready[Lb]);
+          umma_commit<true>(&s.v_empty[st]);
+          umma_commit<true>(&s.pv_done);
+          if (jt + 1 == n) umma_commit<true>(&s.o_ready[Lb]);
           if (jt + 2 < n) {
-            if (!mbar_wait(&s.k_full[st], ((jt + 2) >> 1) & 1, abort_flag, lim)) { ok = false; break; }
+            if (!wait_w(&s.k_full[st], ((jt + 2) >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
-            umma8_ss_kmajor(tmem + kColS + xb * BN, q_lo_l, st ? k_lo1 : k_lo0, idesc_qk);
-            umma_commit(&s.s_full[xb]);
-            umma_commit(&s.k_empty[st]);
+            umma8_ss_kmajor<true>(tmem + kColS + xb * BN, q_lo_l, st ? k_lo1 : k_lo0, idesc_qk);
+            umma_commit<true>(&s.s_full[xb]);
+            umma_commit<true>(&s.k_empty[st]);
           }
           continue;
         }
@@ -367,34 +373,34 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int x = 0; x < 2 && ok; ++x) {
           const int nxx = x ? nx1 : nx0;
           if (jt >= nxx) continue;
-          if (!mbar_wait(&s.p_full[x], jt & 1, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.p_full[x], jt & 1)) { ok = false; break; }
           tc_fence_after();
           issue_pv(jt, x);
-          if (x == 1 || jt >= nx1) umma_commit(&s.v_empty[st]);
+          if (x == 1 || jt >= nx1) umma_commit<true>(&s.v_empty[st]);
           if (jt + 1 == nxx) {
-            umma_commit(&s.o_ready[x]);
+            umma_commit<true>(&s.o_ready[x]);
           } else {
             if (!k_ready) {
-              if (!mbar_wait(&s.k_full[st1], ((jt + 1) >> 1) & 1, abort_flag, lim)) { ok = false; break; }
+              if (!wait_w(&s.k_full[st1], ((jt + 1) >> 1) & 1)) { ok = false; break; }
               tc_fence_after();
               k_ready = true;
             }
             issue_s(jt + 1, x);
           }
         }
-        if (ok && k_ready) umma_commit(&s.k_empty[st1]);
+        if (ok && k_ready) umma_commit<true>(&s.k_empty[st1]);
         if (ok && tail2 && jt + 1 == n_short && n_short + 1 < n) {
           // first tail tile's successor: S(n_short+1) into Sb's columns, which
           // PV_Sb(n_short-1), issued before it, has finished reading
-          if (!mbar_wait(&s.k_full[st], ((n_short + 1) >> 1) & 1, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.k_full[st], ((n_short + 1) >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
-          umma8_ss_kmajor(tmem + kColS + Sb * BN, q_lo_l, st ? k_lo1 : k_lo0, idesc_qk);
-          umma_commit(&s.s_full[Sb]);
-          umma_commit(&s.k_empty[st]);
+          umma8_ss_kmajor<true>(tmem + kColS + Sb * BN, q_lo_l, st ? k_lo1 : k_lo0, idesc_qk);
+          umma_commit<true>(&s.s_full[Sb]);
+          umma_commit<true>(&s.k_empty[st]);
         }
       }
       // every MMA issued so far must finish before TMEM is released
-      umma_commit(&s.drain);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }

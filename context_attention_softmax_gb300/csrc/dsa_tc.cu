@@ -257,8 +257,8 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
       };
       for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++ui) {
         const int hc = it & 1;
-        // The previous item's last PV goes first: its epilogue frees the Q^T
-        // columns that this item's S needs (qt_full follows o_full).
+        // The previous item's last PV goes first: the softmax warps fill
+        // this item's Q^T only after that item's last P.
         if (prev >= 0) {
           if (!issue_pv()) { ok = false; break; }
           prev = -1;
@@ -324,32 +324,46 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
     const int r = (warp & 3) * 32 + lane;   // head
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const float sl2 = a.scale * 1.4426950408889634f;
+    // Q channels 0..255 of (query, head r) into TMEM as bf16 pairs.  An
+    // item's fill runs as soon as the previous item's last S is complete
+    // (before that item's epilogue), so the MMA thread can start this
+    // item's S while the epilogue drains O.
+    auto fill_qt = [&](int item) {
+      const uint4* qsrc = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(a.q) + (int64_t)(item >> 1) * a.q_stride_t +
+          (int64_t)r * a.q_stride_h);
+#pragma unroll
+      for (int cc = 0; cc < kQT; ++cc) {
+        uint32_t w[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = __ldg(qsrc + cc * 8 + v);
+          w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_base + kColQ + 32 * cc, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&s.qt_full);
+    };
     int gj = 0, ui = 0;
     bool ok = true;
+    if ((int)blockIdx.x < p.n_items) fill_qt(blockIdx.x);
     for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++ui) {
       const int i = it >> 1, c = it & 1;
       const KeyInterval iv = allowed_interval(a, query_pos(a, i));
-      // Q channels 0..255 of (query i, head r) into TMEM as bf16 pairs.  The
-      // previous item's MMAs finished with them (its epilogue waited o_full).
-      {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const __nv_bfloat16*>(a.q) + (int64_t)i * a.q_stride_t +
-            (int64_t)r * a.q_stride_h);
-#pragma unroll
-        for (int cc = 0; cc < kQT; ++cc) {
-          uint32_t w[32];
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint4 x = __ldg(qsrc + cc * 8 + v);
-            w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
-          }
-          tmem_st32(tmem + lane_base + kColQ + 32 * cc, w);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&s.qt_full);
-      }
       float m2 = -CUDART_INF_F, l = 0.f;
+      {   // this head's channels 0..255 of the next item's query, into L2, so
+          // the TMEM fill after the last tile reads L2
+        const int nx = it + (int)gridDim.x;
+        if (nx < p.n_items) {
+          const char* nq = reinterpret_cast<const char*>(
+              reinterpret_cast<const __nv_bfloat16*>(a.q) + (int64_t)(nx >> 1) * a.q_stride_t +
+              (int64_t)r * a.q_stride_h);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(nq + 128 * k));
+        }
+      }
       for (int j = 0; j < T; ++j, ++gj) {
         // column mask of the tile: the index is present, in range and
         // permitted for this query (lane holds keys lane and lane + 32)
@@ -432,17 +446,9 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         mbar_arrive(&s.p_full[gj & 1]);
       }
       if (!ok) break;
-      {   // this head's channels 0..255 of the next item's query, into L2 while
-          // the epilogue runs: the TMEM fill that follows then reads L2
-        const int nx = it + (int)gridDim.x;
-        if (nx < p.n_items) {
-          const char* nq = reinterpret_cast<const char*>(
-              reinterpret_cast<const __nv_bfloat16*>(a.q) + (int64_t)(nx >> 1) * a.q_stride_t +
-              (int64_t)r * a.q_stride_h);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(nq + 128 * k));
-        }
-      }
+      // Every S of this item is complete (s_full of its last tile was
+      // observed), so Q^T may be overwritten with the next item's.
+      if (it + (int)gridDim.x < p.n_items) fill_qt(it + (int)gridDim.x);
       ok = __all_sync(kFullMask, mbar_wait(&s.o_full, ui & 1, abort_flag, lim));
       if (!ok) break;
       tc_fence_after();

@@ -309,130 +309,163 @@ __device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kDescHiSw128));
 }
 
+// The grouped MMA helpers below come in two issue forms.  W = false: the
+// caller is a single thread (a divergent branch of its warp).  W = true: the
+// whole warp calls with identical arguments and one lane, picked by
+// elect.sync, issues; a converged issuing warp loses fewer issue slots to
+// busy warps of its sub-partition.
+#define CPATTN_ELECT_DECL ".reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+
 // Eight MMAs along K = 128 (16 per instruction) in one PTX block, both
 // operands K-major in 64-column 128-byte-swizzled boxes: step k reads the
 // descriptors lo + (k / 4) * 1024 + (k % 4) * 2 (16 KiB per box, 32 B per
 // step).  The first MMA overwrites D, the rest accumulate.
+#define CPATTN_UMMA8_SS_TEXT(DECL, P)                                   \
+  "{\n\t.reg .b32 a<8>, b<8>;\n\t.reg .b64 da<8>, db<8>;\n\t" DECL     \
+  "add.u32 a0, %1, 0;    add.u32 b0, %2, 0;\n\t"                       \
+  "add.u32 a1, %1, 2;    add.u32 b1, %2, 2;\n\t"                       \
+  "add.u32 a2, %1, 4;    add.u32 b2, %2, 4;\n\t"                       \
+  "add.u32 a3, %1, 6;    add.u32 b3, %2, 6;\n\t"                       \
+  "add.u32 a4, %1, 1024; add.u32 b4, %2, 1024;\n\t"                    \
+  "add.u32 a5, %1, 1026; add.u32 b5, %2, 1026;\n\t"                    \
+  "add.u32 a6, %1, 1028; add.u32 b6, %2, 1028;\n\t"                    \
+  "add.u32 a7, %1, 1030; add.u32 b7, %2, 1030;\n\t"                    \
+  "mov.b64 da0, {a0, %4}; mov.b64 db0, {b0, %4};\n\t"                  \
+  "mov.b64 da1, {a1, %4}; mov.b64 db1, {b1, %4};\n\t"                  \
+  "mov.b64 da2, {a2, %4}; mov.b64 db2, {b2, %4};\n\t"                  \
+  "mov.b64 da3, {a3, %4}; mov.b64 db3, {b3, %4};\n\t"                  \
+  "mov.b64 da4, {a4, %4}; mov.b64 db4, {b4, %4};\n\t"                  \
+  "mov.b64 da5, {a5, %4}; mov.b64 db5, {b5, %4};\n\t"                  \
+  "mov.b64 da6, {a6, %4}; mov.b64 db6, {b6, %4};\n\t"                  \
+  "mov.b64 da7, {a7, %4}; mov.b64 db7, {b7, %4};\n\t"                  \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da0, db0, %3, 0;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da1, db1, %3, 1;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da2, db2, %3, 1;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da3, db3, %3, 1;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da4, db4, %3, 1;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da5, db5, %3, 1;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da6, db6, %3, 1;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da7, db7, %3, 1;\n\t}"
+template <bool W = false>
 __device__ __forceinline__ void umma8_ss_kmajor(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                                 uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .b32 a<8>, b<8>;\n\t.reg .b64 da<8>, db<8>;\n\t"
-      "add.u32 a0, %1, 0;    add.u32 b0, %2, 0;\n\t"
-      "add.u32 a1, %1, 2;    add.u32 b1, %2, 2;\n\t"
-      "add.u32 a2, %1, 4;    add.u32 b2, %2, 4;\n\t"
-      "add.u32 a3, %1, 6;    add.u32 b3, %2, 6;\n\t"
-      "add.u32 a4, %1, 1024; add.u32 b4, %2, 1024;\n\t"
-      "add.u32 a5, %1, 1026; add.u32 b5, %2, 1026;\n\t"
-      "add.u32 a6, %1, 1028; add.u32 b6, %2, 1028;\n\t"
-      "add.u32 a7, %1, 1030; add.u32 b7, %2, 1030;\n\t"
-      "mov.b64 da0, {a0, %4}; mov.b64 db0, {b0, %4};\n\t"
-      "mov.b64 da1, {a1, %4}; mov.b64 db1, {b1, %4};\n\t"
-      "mov.b64 da2, {a2, %4}; mov.b64 db2, {b2, %4};\n\t"
-      "mov.b64 da3, {a3, %4}; mov.b64 db3, {b3, %4};\n\t"
-      "mov.b64 da4, {a4, %4}; mov.b64 db4, {b4, %4};\n\t"
-      "mov.b64 da5, {a5, %4}; mov.b64 db5, {b5, %4};\n\t"
-      "mov.b64 da6, {a6, %4}; mov.b64 db6, {b6, %4};\n\t"
-      "mov.b64 da7, {a7, %4}; mov.b64 db7, {b7, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da0, db0, %3, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da1, db1, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da2, db2, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da3, db3, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da4, db4, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da5, db5, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da6, db6, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da7, db7, %3, 1;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128));
+  if constexpr (W)
+    asm volatile(CPATTN_UMMA8_SS_TEXT(CPATTN_ELECT_DECL, "@e ") ::"r"(d_tmem), "r"(a_lo),
+                 "r"(b_lo), "r"(idesc), "n"(kDescHiSw128));
+  else
+    asm volatile(CPATTN_UMMA8_SS_TEXT("", "") ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(idesc),
+                 "n"(kDescHiSw128));
 }
 
 // Eight MMAs along K = 128 with A (16-bit, M x K) in tensor memory at column
 // a_tmem + 8 k and B MN-major in shared memory, stepping b_lo by 128 (2 KiB,
 // 16 K-rows) per MMA.  acc0 = 0: the first MMA overwrites D.
-template <int ACC0>
+#define CPATTN_UMMA8_TS_MN_TEXT(DECL, P)                                \
+  "{\n\t.reg .b32 b<8>, t<8>;\n\t.reg .b64 db<8>;\n\t" DECL            \
+  "add.u32 b0, %2, 0;   add.u32 t0, %1, 0;\n\t"                        \
+  "add.u32 b1, %2, 128; add.u32 t1, %1, 8;\n\t"                        \
+  "add.u32 b2, %2, 256; add.u32 t2, %1, 16;\n\t"                       \
+  "add.u32 b3, %2, 384; add.u32 t3, %1, 24;\n\t"                       \
+  "add.u32 b4, %2, 512; add.u32 t4, %1, 32;\n\t"                       \
+  "add.u32 b5, %2, 640; add.u32 t5, %1, 40;\n\t"                       \
+  "add.u32 b6, %2, 768; add.u32 t6, %1, 48;\n\t"                       \
+  "add.u32 b7, %2, 896; add.u32 t7, %1, 56;\n\t"                       \
+  "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"                  \
+  "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"                  \
+  "mov.b64 db4, {b4, %4}; mov.b64 db5, {b5, %4};\n\t"                  \
+  "mov.b64 db6, {b6, %4}; mov.b64 db7, {b7, %4};\n\t"                  \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"  \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t4], db4, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t5], db5, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t6], db6, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], db7, %3, 1;\n\t}"
+template <int ACC0, bool W = false>
 __device__ __forceinline__ void umma8_ts_mnmajor(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                                  uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .b32 b<8>, t<8>;\n\t.reg .b64 db<8>;\n\t"
-      "add.u32 b0, %2, 0;   add.u32 t0, %1, 0;\n\t"
-      "add.u32 b1, %2, 128; add.u32 t1, %1, 8;\n\t"
-      "add.u32 b2, %2, 256; add.u32 t2, %1, 16;\n\t"
-      "add.u32 b3, %2, 384; add.u32 t3, %1, 24;\n\t"
-      "add.u32 b4, %2, 512; add.u32 t4, %1, 32;\n\t"
-      "add.u32 b5, %2, 640; add.u32 t5, %1, 40;\n\t"
-      "add.u32 b6, %2, 768; add.u32 t6, %1, 48;\n\t"
-      "add.u32 b7, %2, 896; add.u32 t7, %1, 56;\n\t"
-      "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"
-      "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"
-      "mov.b64 db4, {b4, %4}; mov.b64 db5, {b5, %4};\n\t"
-      "mov.b64 db6, {b6, %4}; mov.b64 db7, {b7, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t4], db4, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t5], db5, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t6], db6, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], db7, %3, 1;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+  if constexpr (W)
+    asm volatile(CPATTN_UMMA8_TS_MN_TEXT(CPATTN_ELECT_DECL, "@e ") ::"r"(d_tmem), "r"(a_tmem),
+                 "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+  else
+    asm volatile(CPATTN_UMMA8_TS_MN_TEXT("", "") ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo),
+                 "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
 }
 
 // Four MMAs (K = 64) with both operands K-major in one 128-byte-swizzled
 // 64-column box: steps advance both descriptors by 32 B (2 in >> 4 units).
-template <int ACC0>
+#define CPATTN_UMMA4_SS_K_TEXT(DECL, P)                                 \
+  "{\n\t.reg .b32 a<4>, b<4>;\n\t.reg .b64 da<4>, db<4>;\n\t" DECL     \
+  "add.u32 a0, %1, 0; add.u32 b0, %2, 0;\n\t"                          \
+  "add.u32 a1, %1, 2; add.u32 b1, %2, 2;\n\t"                          \
+  "add.u32 a2, %1, 4; add.u32 b2, %2, 4;\n\t"                          \
+  "add.u32 a3, %1, 6; add.u32 b3, %2, 6;\n\t"                          \
+  "mov.b64 da0, {a0, %4}; mov.b64 db0, {b0, %4};\n\t"                  \
+  "mov.b64 da1, {a1, %4}; mov.b64 db1, {b1, %4};\n\t"                  \
+  "mov.b64 da2, {a2, %4}; mov.b64 db2, {b2, %4};\n\t"                  \
+  "mov.b64 da3, {a3, %4}; mov.b64 db3, {b3, %4};\n\t"                  \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da0, db0, %3, %5;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da1, db1, %3, 1;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da2, db2, %3, 1;\n\t"    \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], da3, db3, %3, 1;\n\t}"
+template <int ACC0, bool W = false>
 __device__ __forceinline__ void umma4_ss_k(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                            uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .b32 a<4>, b<4>;\n\t.reg .b64 da<4>, db<4>;\n\t"
-      "add.u32 a0, %1, 0; add.u32 b0, %2, 0;\n\t"
-      "add.u32 a1, %1, 2; add.u32 b1, %2, 2;\n\t"
-      "add.u32 a2, %1, 4; add.u32 b2, %2, 4;\n\t"
-      "add.u32 a3, %1, 6; add.u32 b3, %2, 6;\n\t"
-      "mov.b64 da0, {a0, %4}; mov.b64 db0, {b0, %4};\n\t"
-      "mov.b64 da1, {a1, %4}; mov.b64 db1, {b1, %4};\n\t"
-      "mov.b64 da2, {a2, %4}; mov.b64 db2, {b2, %4};\n\t"
-      "mov.b64 da3, {a3, %4}; mov.b64 db3, {b3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da0, db0, %3, %5;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da1, db1, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da2, db2, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], da3, db3, %3, 1;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+  if constexpr (W)
+    asm volatile(CPATTN_UMMA4_SS_K_TEXT(CPATTN_ELECT_DECL, "@e ") ::"r"(d_tmem), "r"(a_lo),
+                 "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+  else
+    asm volatile(CPATTN_UMMA4_SS_K_TEXT("", "") ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(idesc),
+                 "n"(kDescHiSw128), "n"(ACC0));
 }
 // Four MMAs (K = 64) with A in tensor memory (columns a_tmem + 8 k) and B
 // K-major in one swizzled box (b_lo + 2 k).
-template <int ACC0>
+#define CPATTN_UMMA4_TS_K_TEXT(DECL, P)                                 \
+  "{\n\t.reg .b32 b<4>, t<4>;\n\t.reg .b64 db<4>;\n\t" DECL            \
+  "add.u32 b0, %2, 0; add.u32 t0, %1, 0;\n\t"                          \
+  "add.u32 b1, %2, 2; add.u32 t1, %1, 8;\n\t"                          \
+  "add.u32 b2, %2, 4; add.u32 t2, %1, 16;\n\t"                         \
+  "add.u32 b3, %2, 6; add.u32 t3, %1, 24;\n\t"                         \
+  "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"                  \
+  "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"                  \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"  \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t}"
+template <int ACC0, bool W = false>
 __device__ __forceinline__ void umma4_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                            uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .b32 b<4>, t<4>;\n\t.reg .b64 db<4>;\n\t"
-      "add.u32 b0, %2, 0; add.u32 t0, %1, 0;\n\t"
-      "add.u32 b1, %2, 2; add.u32 t1, %1, 8;\n\t"
-      "add.u32 b2, %2, 4; add.u32 t2, %1, 16;\n\t"
-      "add.u32 b3, %2, 6; add.u32 t3, %1, 24;\n\t"
-      "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"
-      "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+  if constexpr (W)
+    asm volatile(CPATTN_UMMA4_TS_K_TEXT(CPATTN_ELECT_DECL, "@e ") ::"r"(d_tmem), "r"(a_tmem),
+                 "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+  else
+    asm volatile(CPATTN_UMMA4_TS_K_TEXT("", "") ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo),
+                 "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
 }
 // Four MMAs (K = 64) with A in tensor memory and B MN-major (16 K-rows =
 // 2 KiB per step, b_lo + 128 k; leading offset carried in b_lo).
-template <int ACC0>
+#define CPATTN_UMMA4_TS_MN_TEXT(DECL, P)                                \
+  "{\n\t.reg .b32 b<4>, t<4>;\n\t.reg .b64 db<4>;\n\t" DECL            \
+  "add.u32 b0, %2, 0;   add.u32 t0, %1, 0;\n\t"                        \
+  "add.u32 b1, %2, 128; add.u32 t1, %1, 8;\n\t"                        \
+  "add.u32 b2, %2, 256; add.u32 t2, %1, 16;\n\t"                       \
+  "add.u32 b3, %2, 384; add.u32 t3, %1, 24;\n\t"                       \
+  "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"                  \
+  "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"                  \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"  \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"   \
+  P "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t}"
+template <int ACC0, bool W = false>
 __device__ __forceinline__ void umma4_ts_mn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                             uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .b32 b<4>, t<4>;\n\t.reg .b64 db<4>;\n\t"
-      "add.u32 b0, %2, 0;   add.u32 t0, %1, 0;\n\t"
-      "add.u32 b1, %2, 128; add.u32 t1, %1, 8;\n\t"
-      "add.u32 b2, %2, 256; add.u32 t2, %1, 16;\n\t"
-      "add.u32 b3, %2, 384; add.u32 t3, %1, 24;\n\t"
-      "mov.b64 db0, {b0, %4}; mov.b64 db1, {b1, %4};\n\t"
-      "mov.b64 db2, {b2, %4}; mov.b64 db3, {b3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], db0, %3, %5;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], db1, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], db2, %3, 1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], db3, %3, 1;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+  if constexpr (W)
+    asm volatile(CPATTN_UMMA4_TS_MN_TEXT(CPATTN_ELECT_DECL, "@e ") ::"r"(d_tmem), "r"(a_tmem),
+                 "r"(b_lo), "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
+  else
+    asm volatile(CPATTN_UMMA4_TS_MN_TEXT("", "") ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo),
+                 "r"(idesc), "n"(kDescHiSw128), "n"(ACC0));
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]; A (M x K, 16-bit, two elements per 32-bit
@@ -490,12 +523,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread
-// has completed.
+// has completed.  W = true: the whole warp calls, the elected lane commits.
+template <bool W = false>
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
+  if constexpr (W)
+    asm volatile(
+        "{\n\t" CPATTN_ELECT_DECL
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
 }
 
 }  // namespace sm100

@@ -232,7 +232,12 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop, converged, and one elected lane
+    // issues each MMA group (waits made warp-uniform).
+    {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc_s = idesc_bf16_f32(HQ, BNK, 0, 0);    // A (TMEM or smem) K-major
       const uint32_t idesc_pv = idesc_bf16_f32(HQ, DVH, 0, 1);   // P (TMEM), V MN-major
       const uint32_t qs_lo = desc_lo(smem_u32(s.qs[0]), 16);
@@ -241,18 +246,18 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
       int prev = -1, prev_first = 0, prev_last = 0, prev_ui = 0, prev_c = 0;
       auto issue_pv = [&]() -> bool {
         const int g = prev;
-        if (!mbar_wait(&s.p_full[g & 1], (g >> 1) & 1, abort_flag, lim)) return false;
-        if (prev_first && prev_ui > 0 && !mbar_wait(&s.o_free, (prev_ui - 1) & 1, abort_flag, lim))
+        if (!wait_w(&s.p_full[g & 1], (g >> 1) & 1)) return false;
+        if (prev_first && prev_ui > 0 && !wait_w(&s.o_free, (prev_ui - 1) & 1))
           return false;
         tc_fence_after();
         // value channels [256c, 256c + 256) = chunks 4c..4c+3 of the key rows
         const uint32_t vb = desc_lo(smem_u32(s.kv[g % NS]) + 4 * prev_c * kKChunkBytes, kKChunkBytes);
         const uint32_t pa = tmem + kColS + (g & 1) * BNK;
-        if (prev_first) umma4_ts_mn<0>(tmem + kColO, pa, vb, idesc_pv);
-        else umma4_ts_mn<1>(tmem + kColO, pa, vb, idesc_pv);
-        umma_commit(&s.kb_empty[g % NS]);
-        umma_commit(&s.pv_done);
-        if (prev_last) umma_commit(&s.o_full);
+        if (prev_first) umma4_ts_mn<0, true>(tmem + kColO, pa, vb, idesc_pv);
+        else umma4_ts_mn<1, true>(tmem + kColO, pa, vb, idesc_pv);
+        umma_commit<true>(&s.kb_empty[g % NS]);
+        umma_commit<true>(&s.pv_done);
+        if (prev_last) umma_commit<true>(&s.o_full);
         return true;
       };
       for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x, ++ui) {
@@ -263,12 +268,12 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
           if (!issue_pv()) { ok = false; break; }
           prev = -1;
         }
-        if (!mbar_wait(&s.qt_full, ui & 1, abort_flag, lim) ||
-            !mbar_wait(&s.qs_full, ui & 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.qt_full, ui & 1) ||
+            !wait_w(&s.qs_full, ui & 1)) { ok = false; break; }
         for (int j = 0; j < T; ++j, ++gj) {
           const int st = gj % NS;
           const uint32_t ph = (gj / NS) & 1;
-          if (!mbar_wait(&s.ka_full[st], ph, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.ka_full[st], ph)) { ok = false; break; }
           fence_proxy_async_smem();   // the gathered rows were written by cp.async
           tc_fence_after();
           const uint32_t d = tmem + kColS + (gj & 1) * BNK;
@@ -278,35 +283,35 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
           // channels), channels 256..575 A = Q from shared memory.  Part A
           // chunks first, then the value chunks of this half.
           if (hc == 0) {
-            umma4_ss_k<0>(d, qs_lo, kb + 4 * kC, idesc_s);
+            umma4_ss_k<0, true>(d, qs_lo, kb + 4 * kC, idesc_s);
 #pragma unroll
-            for (int c = 1; c < kQS; ++c) umma4_ss_k<1>(d, qs_lo + c * kQC, kb + (kQT + c) * kC, idesc_s);
+            for (int c = 1; c < kQS; ++c) umma4_ss_k<1, true>(d, qs_lo + c * kQC, kb + (kQT + c) * kC, idesc_s);
           } else {
-            umma4_ts_k<0>(d, tmem + kColQ + 0, kb + 0 * kC, idesc_s);
-            umma4_ts_k<1>(d, tmem + kColQ + 32, kb + 1 * kC, idesc_s);
-            umma4_ts_k<1>(d, tmem + kColQ + 64, kb + 2 * kC, idesc_s);
-            umma4_ts_k<1>(d, tmem + kColQ + 96, kb + 3 * kC, idesc_s);
-            umma4_ss_k<1>(d, qs_lo + 4 * kQC, kb + 8 * kC, idesc_s);
+            umma4_ts_k<0, true>(d, tmem + kColQ + 0, kb + 0 * kC, idesc_s);
+            umma4_ts_k<1, true>(d, tmem + kColQ + 32, kb + 1 * kC, idesc_s);
+            umma4_ts_k<1, true>(d, tmem + kColQ + 64, kb + 2 * kC, idesc_s);
+            umma4_ts_k<1, true>(d, tmem + kColQ + 96, kb + 3 * kC, idesc_s);
+            umma4_ss_k<1, true>(d, qs_lo + 4 * kQC, kb + 8 * kC, idesc_s);
           }
-          umma_commit(&s.ka_empty[st]);
+          umma_commit<true>(&s.ka_empty[st]);
           // PV of the previous tile goes between the two parts of S, so that
           // its value chunks are released as early as possible.
           if (prev >= 0 && !issue_pv()) { ok = false; break; }
           prev = -1;
-          if (!mbar_wait(&s.kb_full[st], ph, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.kb_full[st], ph)) { ok = false; break; }
           fence_proxy_async_smem();
           tc_fence_after();
           if (hc == 0) {
-            umma4_ts_k<1>(d, tmem + kColQ + 0, kb + 0 * kC, idesc_s);
-            umma4_ts_k<1>(d, tmem + kColQ + 32, kb + 1 * kC, idesc_s);
-            umma4_ts_k<1>(d, tmem + kColQ + 64, kb + 2 * kC, idesc_s);
-            umma4_ts_k<1>(d, tmem + kColQ + 96, kb + 3 * kC, idesc_s);
+            umma4_ts_k<1, true>(d, tmem + kColQ + 0, kb + 0 * kC, idesc_s);
+            umma4_ts_k<1, true>(d, tmem + kColQ + 32, kb + 1 * kC, idesc_s);
+            umma4_ts_k<1, true>(d, tmem + kColQ + 64, kb + 2 * kC, idesc_s);
+            umma4_ts_k<1, true>(d, tmem + kColQ + 96, kb + 3 * kC, idesc_s);
           } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) umma4_ss_k<1>(d, qs_lo + c * kQC, kb + (kQT + c) * kC, idesc_s);
+            for (int c = 0; c < 4; ++c) umma4_ss_k<1, true>(d, qs_lo + c * kQC, kb + (kQT + c) * kC, idesc_s);
           }
-          umma_commit(&s.s_full[gj & 1]);
-          if (j == T - 1) umma_commit(&s.qs_empty);
+          umma_commit<true>(&s.s_full[gj & 1]);
+          if (j == T - 1) umma_commit<true>(&s.qs_empty);
           prev = gj;
           prev_first = (j == 0);
           prev_last = (j == T - 1);
@@ -315,7 +320,7 @@ dsa_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const DsaParams p) {
         }
       }
       if (ok && prev >= 0) issue_pv();
-      umma_commit(&s.drain);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }

@@ -437,7 +437,12 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop, converged, and one elected lane
+    // issues each MMA group (waits made warp-uniform).
+    {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);
       const uint32_t q_lo0 = desc_lo(smem_u32(s.q[0]), 16), q_lo1 = desc_lo(smem_u32(s.q[1]), 16);
@@ -449,37 +454,37 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
       int prev = -1, prev_first = 0, prev_last = 0, prev_ui = 0;
       auto issue_pv = [&]() -> bool {
         const int j = prev;
-        if (!mbar_wait(&s.p_full[j & 1], (j >> 1) & 1, abort_flag, lim) ||
-            !mbar_wait(&s.v_full[j % NS], (j / NS) & 1, abort_flag, lim)) return false;
+        if (!wait_w(&s.p_full[j & 1], (j >> 1) & 1) ||
+            !wait_w(&s.v_full[j % NS], (j / NS) & 1)) return false;
         // O of unit u lives in buffer u & 1; its first PV waits until the
         // epilogue has read unit u - 2 out of that buffer
         const int ob = prev_ui & 1;
         if (prev_first && prev_ui >= 2 &&
-            !mbar_wait(&s.o_free[ob], ((prev_ui - 2) >> 1) & 1, abort_flag, lim)) return false;
+            !wait_w(&s.o_free[ob], ((prev_ui - 2) >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t vb = (j % NS) ? v_lo1 : v_lo0;
         const uint32_t pa = tmem + kColS + (j & 1) * BN;
         const uint32_t od = tmem + kColO + ob * HD;
-        if (prev_first) umma8_ts_mnmajor<0>(od, pa, vb, idesc_pv);
-        else umma8_ts_mnmajor<1>(od, pa, vb, idesc_pv);
-        umma_commit(&s.v_empty[j % NS]);
-        umma_commit(&s.pv_done);
-        if (prev_last) umma_commit(&s.o_full[ob]);
+        if (prev_first) umma8_ts_mnmajor<0, true>(od, pa, vb, idesc_pv);
+        else umma8_ts_mnmajor<1, true>(od, pa, vb, idesc_pv);
+        umma_commit<true>(&s.v_empty[j % NS]);
+        umma_commit<true>(&s.pv_done);
+        if (prev_last) umma_commit<true>(&s.o_full[ob]);
         return true;
       };
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ui) {
         const int4 un = p.units[u];
         const int T = unit_tiles(p, un.y), qb = ui & 1;
-        if (!mbar_wait(&s.q_full[qb], (ui >> 1) & 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.q_full[qb], (ui >> 1) & 1)) { ok = false; break; }
         for (int t = 0; t < T; ++t, ++jt) {
           const int st = jt % NS;
-          if (!mbar_wait(&s.k_full[st], (jt / NS) & 1, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.k_full[st], (jt / NS) & 1)) { ok = false; break; }
           tc_fence_after();
-          umma8_ss_kmajor(tmem + kColS + (jt & 1) * BN, qb ? q_lo1 : q_lo0, st ? k_lo1 : k_lo0,
+          umma8_ss_kmajor<true>(tmem + kColS + (jt & 1) * BN, qb ? q_lo1 : q_lo0, st ? k_lo1 : k_lo0,
                           idesc_qk);
-          umma_commit(&s.s_full[jt & 1]);
-          umma_commit(&s.k_empty[st]);
-          if (t == T - 1) umma_commit(&s.q_empty[qb]);
+          umma_commit<true>(&s.s_full[jt & 1]);
+          umma_commit<true>(&s.k_empty[st]);
+          if (t == T - 1) umma_commit<true>(&s.q_empty[qb]);
           if (prev >= 0 && !issue_pv()) { ok = false; break; }
           prev = jt;
           prev_first = (t == 0);
@@ -488,7 +493,7 @@ moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         }
       }
       if (ok && prev >= 0) issue_pv();
-      umma_commit(&s.drain);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }

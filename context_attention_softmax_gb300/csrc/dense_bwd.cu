@@ -227,38 +227,43 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_steps > 0) {
+    // The whole warp runs the issue loop, converged, and one elected lane
+    // issues each MMA group (waits made warp-uniform).
+    if (n_steps > 0) {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc_kk = idesc_bf16_f32(BM, BN, 0, 0);
       const uint32_t idesc_mn = idesc_bf16_f32(BM, HD, 0, 1);
       const uint32_t k_lo = desc_lo(smem_u32(s.k), 16), v_lo = desc_lo(smem_u32(s.v), 16);
-      bool ok = mbar_wait(&s.kv_full, 0, abort_flag, lim);
+      bool ok = wait_w(&s.kv_full, 0);
       for (int it = 0; it < n_steps && ok; ++it) {
         const int b = it & 1;
-        if (!mbar_wait(&s.qg_full[b], (it >> 1) & 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.qg_full[b], (it >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t q_lo = desc_lo(smem_u32(s.q[b]), 16), g_lo = desc_lo(smem_u32(s.g[b]), 16);
-        umma8_ss_kmajor(tmem + kColS, k_lo, q_lo, idesc_kk);    // S^T = K Q^T
-        umma8_ss_kmajor(tmem + kColDP, v_lo, g_lo, idesc_kk);   // dP^T = V g^T
-        umma_commit(&s.s_full);
-        if (!mbar_wait(&s.p_full, it & 1, abort_flag, lim)) { ok = false; break; }
+        umma8_ss_kmajor<true>(tmem + kColS, k_lo, q_lo, idesc_kk);    // S^T = K Q^T
+        umma8_ss_kmajor<true>(tmem + kColDP, v_lo, g_lo, idesc_kk);   // dP^T = V g^T
+        umma_commit<true>(&s.s_full);
+        if (!wait_w(&s.p_full, it & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t q_mn = desc_lo(smem_u32(s.q[b]), kHalf), g_mn = desc_lo(smem_u32(s.g[b]), kHalf);
         // P^T and dS^T of queries 0..63 sit at columns 0..31 of their
         // regions, those of queries 64..127 at columns 64..95 (one half per
         // element warpgroup); B rows 64.. start 4 K-steps (8 KiB) further on.
         if (it == 0) {
-          umma4_ts_mn<0>(tmem + kColDV, tmem + kColS, g_mn, idesc_mn);          // dv  = P^T g
-          umma4_ts_mn<0>(tmem + kColDK, tmem + kColDP, q_mn, idesc_mn);         // dk  = dS^T q
+          umma4_ts_mn<0, true>(tmem + kColDV, tmem + kColS, g_mn, idesc_mn);          // dv  = P^T g
+          umma4_ts_mn<0, true>(tmem + kColDK, tmem + kColDP, q_mn, idesc_mn);         // dk  = dS^T q
         } else {
-          umma4_ts_mn<1>(tmem + kColDV, tmem + kColS, g_mn, idesc_mn);          // dv += P^T g
-          umma4_ts_mn<1>(tmem + kColDK, tmem + kColDP, q_mn, idesc_mn);         // dk += dS^T q
+          umma4_ts_mn<1, true>(tmem + kColDV, tmem + kColS, g_mn, idesc_mn);          // dv += P^T g
+          umma4_ts_mn<1, true>(tmem + kColDK, tmem + kColDP, q_mn, idesc_mn);         // dk += dS^T q
         }
-        umma4_ts_mn<1>(tmem + kColDV, tmem + kColS + 64, g_mn + 512, idesc_mn);
-        umma4_ts_mn<1>(tmem + kColDK, tmem + kColDP + 64, q_mn + 512, idesc_mn);
-        umma_commit(&s.qg_empty[b]);
+        umma4_ts_mn<1, true>(tmem + kColDV, tmem + kColS + 64, g_mn + 512, idesc_mn);
+        umma4_ts_mn<1, true>(tmem + kColDK, tmem + kColDP + 64, q_mn + 512, idesc_mn);
+        umma_commit<true>(&s.qg_empty[b]);
       }
-      if (ok) umma_commit(&s.acc_done);
-      umma_commit(&s.drain);
+      if (ok) umma_commit<true>(&s.acc_done);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }
@@ -484,29 +489,34 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_q, const CUtensorMa
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_steps > 0) {
+    // The whole warp runs the issue loop, converged, and one elected lane
+    // issues each MMA group (waits made warp-uniform).
+    if (n_steps > 0) {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc_kk = idesc_bf16_f32(BM, BN, 0, 0);
       const uint32_t idesc_mn = idesc_bf16_f32(BM, HD, 0, 1);
       const uint32_t q_lo = desc_lo(smem_u32(s.q), 16), g_lo = desc_lo(smem_u32(s.g), 16);
-      bool ok = mbar_wait(&s.qg_full, 0, abort_flag, lim);
+      bool ok = wait_w(&s.qg_full, 0);
       for (int it = 0; it < n_steps && ok; ++it) {
         const int b = it & 1;
-        if (!mbar_wait(&s.kv_full[b], (it >> 1) & 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.kv_full[b], (it >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        umma8_ss_kmajor(tmem + kColS, q_lo, desc_lo(smem_u32(s.k[b]), 16), idesc_kk);    // S = Q K^T
-        umma8_ss_kmajor(tmem + kColDP, g_lo, desc_lo(smem_u32(s.v[b]), 16), idesc_kk);   // dP = g V^T
-        umma_commit(&s.s_full);
-        if (!mbar_wait(&s.p_full, it & 1, abort_flag, lim)) { ok = false; break; }
+        umma8_ss_kmajor<true>(tmem + kColS, q_lo, desc_lo(smem_u32(s.k[b]), 16), idesc_kk);    // S = Q K^T
+        umma8_ss_kmajor<true>(tmem + kColDP, g_lo, desc_lo(smem_u32(s.v[b]), 16), idesc_kk);   // dP = g V^T
+        umma_commit<true>(&s.s_full);
+        if (!wait_w(&s.p_full, it & 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t k_mn = desc_lo(smem_u32(s.k[b]), kHalf);
         // dS of keys 0..63 at columns 0..31, of keys 64..127 at columns 64..95
-        if (it == 0) umma4_ts_mn<0>(tmem + kColDQ, tmem + kColS, k_mn, idesc_mn);   // dq  = dS k
-        else umma4_ts_mn<1>(tmem + kColDQ, tmem + kColS, k_mn, idesc_mn);           // dq += dS k
-        umma4_ts_mn<1>(tmem + kColDQ, tmem + kColS + 64, k_mn + 512, idesc_mn);
-        umma_commit(&s.kv_empty[b]);
+        if (it == 0) umma4_ts_mn<0, true>(tmem + kColDQ, tmem + kColS, k_mn, idesc_mn);   // dq  = dS k
+        else umma4_ts_mn<1, true>(tmem + kColDQ, tmem + kColS, k_mn, idesc_mn);           // dq += dS k
+        umma4_ts_mn<1, true>(tmem + kColDQ, tmem + kColS + 64, k_mn + 512, idesc_mn);
+        umma_commit<true>(&s.kv_empty[b]);
       }
-      if (ok) umma_commit(&s.acc_done);
-      umma_commit(&s.drain);
+      if (ok) umma_commit<true>(&s.acc_done);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }

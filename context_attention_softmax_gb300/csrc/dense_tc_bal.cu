@@ -582,72 +582,77 @@ dense_tc_bal_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // Per piece: S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
     // The first PV of a piece overwrites O_X, so it waits until the softmax
     // warps have read O_X of the previous piece (o_free).
-    if (lane == 0) {
+    // The whole warp runs the issue loop, converged, and one elected lane
+    // issues each MMA group (waits made warp-uniform).
+    {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc_qk = idesc_bf16_f32(BM, BN, 0, 0);
       const uint32_t idesc_pv = idesc_bf16_f32(BM, HD, 0, 1);
       const uint32_t q_lo0 = desc_lo(smem_u32(s.q[0]), 16), q_lo1 = desc_lo(smem_u32(s.q[1]), 16);
       const uint32_t k_lo0 = desc_lo(smem_u32(s.k[0]), 16), k_lo1 = desc_lo(smem_u32(s.k[1]), 16);
       const uint32_t v_lo0 = desc_lo(smem_u32(s.v[0]), kHalf), v_lo1 = desc_lo(smem_u32(s.v[1]), kHalf);
       auto issue_s = [&](int j, int x) {   // S_x = Q_x K_j^T
-        umma8_ss_kmajor(tmem + kColS + x * BN, x ? q_lo1 : q_lo0, (j & 1) ? k_lo1 : k_lo0, idesc_qk);
-        umma_commit(&s.s_full[x]);
+        umma8_ss_kmajor<true>(tmem + kColS + x * BN, x ? q_lo1 : q_lo0, (j & 1) ? k_lo1 : k_lo0, idesc_qk);
+        umma_commit<true>(&s.s_full[x]);
       };
       auto issue_pv = [&](int j, int x, bool first) {  // O_x (+)= P_x V_j
         const uint32_t d = tmem + kColO + x * HD, pa = tmem + kColS + x * BN;
         const uint32_t vb = (j & 1) ? v_lo1 : v_lo0;
-        if (first) umma8_ts_mnmajor<0>(d, pa, vb, idesc_pv);
-        else umma8_ts_mnmajor<1>(d, pa, vb, idesc_pv);
+        if (first) umma8_ts_mnmajor<0, true>(d, pa, vb, idesc_pv);
+        else umma8_ts_mnmajor<1, true>(d, pa, vb, idesc_pv);
       };
       int gj = 0, pc = 0;
       bool ok = true;
       PieceWalk pw{s.pref, nu, S0, S1, 0, 0, 0};
       while (ok && pw.next()) {
         const int n = pw.t1 - pw.t0;
-        if (!mbar_wait(&s.q_full, pc & 1, abort_flag, lim) ||
-            !mbar_wait(&s.k_full[gj % NS], (gj / NS) & 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.q_full, pc & 1) ||
+            !wait_w(&s.k_full[gj % NS], (gj / NS) & 1)) { ok = false; break; }
         tc_fence_after();
         issue_s(gj, 0);
         issue_s(gj, 1);
-        umma_commit(&s.k_empty[gj % NS]);
-        if (n == 1) umma_commit(&s.q_empty);
+        umma_commit<true>(&s.k_empty[gj % NS]);
+        if (n == 1) umma_commit<true>(&s.q_empty);
         for (int jt = 0; jt < n && ok; ++jt) {
           const int j = gj + jt, st = j % NS, st1 = (j + 1) % NS;
           const bool more = jt + 1 < n;
           // block A: PV_A(j), then S_A(j+1)
-          if (!mbar_wait(&s.v_full[st], (j / NS) & 1, abort_flag, lim) ||
-              !mbar_wait(&s.p_full[0], j & 1, abort_flag, lim) ||
-              (jt == 0 && pc > 0 && !mbar_wait(&s.o_free[0], (pc - 1) & 1, abort_flag, lim))) {
+          if (!wait_w(&s.v_full[st], (j / NS) & 1) ||
+              !wait_w(&s.p_full[0], j & 1) ||
+              (jt == 0 && pc > 0 && !wait_w(&s.o_free[0], (pc - 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_pv(j, 0, jt == 0);
-          if (!more) umma_commit(&s.o_ready[0]);
+          if (!more) umma_commit<true>(&s.o_ready[0]);
           if (more) {
-            if (!mbar_wait(&s.k_full[st1], ((j + 1) / NS) & 1, abort_flag, lim)) { ok = false; break; }
+            if (!wait_w(&s.k_full[st1], ((j + 1) / NS) & 1)) { ok = false; break; }
             tc_fence_after();
             issue_s(j + 1, 0);
           }
           // block B: PV_B(j), then S_B(j+1)
-          if (!mbar_wait(&s.p_full[1], j & 1, abort_flag, lim) ||
-              (jt == 0 && pc > 0 && !mbar_wait(&s.o_free[1], (pc - 1) & 1, abort_flag, lim))) {
+          if (!wait_w(&s.p_full[1], j & 1) ||
+              (jt == 0 && pc > 0 && !wait_w(&s.o_free[1], (pc - 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_pv(j, 1, jt == 0);
-          umma_commit(&s.v_empty[st]);
-          if (!more) umma_commit(&s.o_ready[1]);
+          umma_commit<true>(&s.v_empty[st]);
+          if (!more) umma_commit<true>(&s.o_ready[1]);
           if (more) {
             issue_s(j + 1, 1);
-            umma_commit(&s.k_empty[st1]);
-            if (jt + 2 == n) umma_commit(&s.q_empty);   // last S of the piece
+            umma_commit<true>(&s.k_empty[st1]);
+            if (jt + 2 == n) umma_commit<true>(&s.q_empty);   // last S of the piece
           }
         }
         gj += n;
         ++pc;
       }
-      umma_commit(&s.drain);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }

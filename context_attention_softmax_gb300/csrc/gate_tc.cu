@@ -217,7 +217,12 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop, converged, and one elected lane
+    // issues each MMA group (waits made warp-uniform).
+    {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc = idesc_bf16_f32(GM, p.npad, 0, 0);
       uint32_t mlo[3][2], qlo[2][2];
       for (int t = 0; t < 3; ++t)
@@ -229,13 +234,13 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       for (int it = i0; it < i1 && ok; ++it, ++ti) {
         const int h = it / p.n_qtiles, g = h / group;
         if (g != cur_g) {
-          if (!mbar_wait(&s.mu_full, n_mu & 1, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.mu_full, n_mu & 1)) { ok = false; break; }
           cur_g = g;
           ++n_mu;
         }
         const int st = ti & 1;
-        if (!mbar_wait(&s.q_full[st], (ti >> 1) & 1, abort_flag, lim) ||
-            !mbar_wait(&s.acc_free[st], ((ti >> 1) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.q_full[st], (ti >> 1) & 1) ||
+            !wait_w(&s.acc_free[st], ((ti >> 1) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(st * 128);
         // K = 3 x 128: the same query tile against each mean term
@@ -243,13 +248,13 @@ gate_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int t = 0; t < 3; ++t)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_ss_lo(d, qlo[st][kk >> 2] + (kk & 3) * 2, mlo[t][kk >> 2] + (kk & 3) * 2, idesc,
+            umma_ss_lo<true>(d, qlo[st][kk >> 2] + (kk & 3) * 2, mlo[t][kk >> 2] + (kk & 3) * 2, idesc,
                        (t | kk) != 0);
-        umma_commit(&s.acc_full[st]);
+        umma_commit<true>(&s.acc_full[st]);
         const bool last_of_group = it + 1 >= i1 || (it + 1) / p.n_qtiles / group != g;
-        if (last_of_group) umma_commit(&s.mu_empty);
+        if (last_of_group) umma_commit<true>(&s.mu_empty);
       }
-      umma_commit(&s.drain);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }

@@ -77,14 +77,15 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int tile, int& 
   nt = rem - mt * p.n_tiles;
 }
 
-// One stage: four MMAs of K = 16.  A K-major (32 B per step); B K-major
+// One stage: four MMAs of K = 16 (W: issued by the converged warp).  A K-major (32 B per step); B K-major
 // (32 B per step) or MN-major (16 K-rows = 2 KiB per step).
-template <int B_MN>
+template <int B_MN, bool W = false>
 __device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
                                           bool acc_first) {
 #pragma unroll
   for (int k = 0; k < 4; ++k)
-    umma_ss_lo(d, a_lo + 2 * k, b_lo + (B_MN ? 128 * k : 2 * k), idesc, (k > 0 || acc_first) ? 1u : 0u);
+    umma_ss_lo<W>(d, a_lo + 2 * k, b_lo + (B_MN ? 128 * k : 2 * k), idesc,
+                  (k > 0 || acc_first) ? 1u : 0u);
 }
 
 __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
@@ -161,26 +162,31 @@ mla_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant_
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop, converged, and one elected lane
+    // issues each MMA group (waits made warp-uniform).
+    {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc = idesc_bf16_f32(GM, GN, 0, B_MN);
       int it = 0, ti = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < p.n_total_tiles && ok; tile += gridDim.x, ++ti) {
         const int buf = ti & 1;
-        if (!mbar_wait(&s.acc_empty[buf], ((ti >> 1) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.acc_empty[buf], ((ti >> 1) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * GN);
         for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
           const int st = it % kStages;
-          if (!mbar_wait(&s.full[st], (it / kStages) & 1, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.full[st], (it / kStages) & 1)) { ok = false; break; }
           tc_fence_after();
-          mma_stage<B_MN>(d, desc_lo(smem_u32(s.a[st]), 16),
+          mma_stage<B_MN, true>(d, desc_lo(smem_u32(s.a[st]), 16),
                           desc_lo(smem_u32(s.b[st]), B_MN ? kBHalf : 16), idesc, ks > 0);
-          umma_commit(&s.empty[st]);
+          umma_commit<true>(&s.empty[st]);
         }
-        if (ok) umma_commit(&s.acc_full[buf]);
+        if (ok) umma_commit<true>(&s.acc_full[buf]);
       }
-      umma_commit(&s.drain);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }
@@ -320,26 +326,31 @@ mla_kv_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ 
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issue loop, converged, and one elected lane
+    // issues each MMA group (waits made warp-uniform).
+    {
+      auto wait_w = [&](uint64_t* bar, uint32_t ph) {
+        return __all_sync(kFullMask, mbar_wait(bar, ph, abort_flag, lim));
+      };
       const uint32_t idesc = idesc_bf16_f32(GM, KN, 0, 0);
       int it = 0, ti = 0;
       bool ok = true;
       for (int tile = t0; tile < t1 && ok; ++tile, ++ti) {
         const int buf = ti & 1;
-        if (!mbar_wait(&s.acc_empty[buf], ((ti >> 1) & 1) ^ 1, abort_flag, lim)) { ok = false; break; }
+        if (!wait_w(&s.acc_empty[buf], ((ti >> 1) & 1) ^ 1)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * KN);
         for (int ks = 0; ks < p.k_steps; ++ks, ++it) {
           const int st = it % kKvStages;
-          if (!mbar_wait(&s.full[st], (it / kKvStages) & 1, abort_flag, lim)) { ok = false; break; }
+          if (!wait_w(&s.full[st], (it / kKvStages) & 1)) { ok = false; break; }
           tc_fence_after();
-          mma_stage<0>(d, desc_lo(smem_u32(s.a[st]), 16), desc_lo(smem_u32(s.b[st]), 16), idesc, ks > 0);
-          umma_commit(&s.empty[st]);
+          mma_stage<0, true>(d, desc_lo(smem_u32(s.a[st]), 16), desc_lo(smem_u32(s.b[st]), 16), idesc, ks > 0);
+          umma_commit<true>(&s.empty[st]);
         }
         if (!ok) break;
-        umma_commit(&s.acc_full[buf]);
+        umma_commit<true>(&s.acc_full[buf]);
       }
-      umma_commit(&s.drain);
+      umma_commit<true>(&s.drain);
       int no_abort = 0;
       mbar_wait(&s.drain, 0, &no_abort, 1000000000ull);
     }

@@ -68,26 +68,26 @@ L2_NOTE = "flushed by a 256 MiB write before every timed step"
 # dominant kernel from one ncu capture (summarised under profiles/), valid
 # only while the kernel's sources hash to the value they had then.
 TRAFFIC = {
-    "dense_gqa": {"bytes": 21_194_240 + 0, "kernel": "dense_tc_kernel<0>",
+    "dense_gqa": {"bytes": 21_191_424 + 0, "kernel": "dense_tc_kernel<0>",
                   "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                  "sha": "096fba09849c7b44"},
-    "dense_gqa_4chunks": {"bytes": 21_085_440 + 13_801_472, "kernel": "dense_tc_kernel<1>",
+                  "sha": "7c68363959fc5330"},
+    "dense_gqa_4chunks": {"bytes": 21_082_112 + 12_393_984, "kernel": "dense_tc_kernel<1>",
                           "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh",
                                       "common.cuh"],
-                          "sha": "096fba09849c7b44"},
-    "dsa": {"bytes": 662_260_736 + 506_345_216, "kernel": "dsa_attn_kernel",
-            "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "f09990023241a7b9"},
-    "mla_kv": {"bytes": 566_199_296 + 2_627_799_552, "kernel": "mla_kv_kernel",
-               "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "473aca57ddd7ce60"},
-    "mla_v_up": {"bytes": 553_843_456 + 112_686_336, "kernel": "mla_gemm_kernel<1>",
-                 "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "473aca57ddd7ce60"},
-    "dense_gqa_bwd": {"bytes": 30_985_472 + 6_564_608, "kernel": "bwd_kernel",
+                          "sha": "7c68363959fc5330"},
+    "dsa": {"bytes": 661_886_208 + 507_494_400, "kernel": "dsa_attn_kernel",
+            "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "6fea0a102583429c"},
+    "mla_kv": {"bytes": 577_171_712 + 2_627_442_176, "kernel": "mla_kv_kernel",
+               "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "083dccee2bdb63db"},
+    "mla_v_up": {"bytes": 553_840_384 + 112_673_792, "kernel": "mla_gemm_kernel<1>",
+                 "sources": ["mla_gemm.cu", "sm100.cuh", "common.cuh"], "sha": "083dccee2bdb63db"},
+    "dense_gqa_bwd": {"bytes": 30_470_656 + 5_928_960, "kernel": "bwd_kernel",
                       "sources": ["dense_bwd.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                      "sha": "ee19e0b8b42dce2a"},
-    "dsa_indexer": {"bytes": 21_542_912 + 243_081_984, "kernel": "idx_score_kernel",
-                    "sources": ["dsa_indexer.cu", "sm100.cuh", "common.cuh"], "sha": "324f649f320c94c3"},
-    "moba": {"bytes": 1_156_865_536 + 259_025_664, "kernel": "moba_attn_kernel",
-             "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "4bd05f662df3ed35"},
+                      "sha": "5085abcec64ca82e"},
+    "dsa_indexer": {"bytes": 20_698_880 + 243_096_576, "kernel": "idx_score_kernel",
+                    "sources": ["dsa_indexer.cu", "sm100.cuh", "common.cuh"], "sha": "9d98db489b72b21a"},
+    "moba": {"bytes": 1_150_921_984 + 257_916_160, "kernel": "moba_attn_kernel",
+             "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "00d0b2bd05e1f360"},
 }
 
 

@@ -70,11 +70,11 @@ L2_NOTE = "flushed by a 256 MiB write before every timed step"
 TRAFFIC = {
     "dense_gqa": {"bytes": 21_191_424 + 0, "kernel": "dense_tc_kernel<0>",
                   "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
-                  "sha": "7c68363959fc5330"},
+                  "sha": "458a7c9515760e3a"},
     "dense_gqa_4chunks": {"bytes": 21_082_112 + 12_393_984, "kernel": "dense_tc_kernel<1>",
                           "sources": ["dense_tc.cu", "dense_tc_common.cuh", "sm100.cuh",
                                       "common.cuh"],
-                          "sha": "7c68363959fc5330"},
+                          "sha": "458a7c9515760e3a"},
     "dsa": {"bytes": 661_886_208 + 507_494_400, "kernel": "dsa_attn_kernel",
             "sources": ["dsa_tc.cu", "sm100.cuh", "common.cuh"], "sha": "6fea0a102583429c"},
     "mla_kv": {"bytes": 577_171_712 + 2_627_442_176, "kernel": "mla_kv_kernel",
@@ -87,7 +87,7 @@ TRAFFIC = {
     "dsa_indexer": {"bytes": 20_698_880 + 243_096_576, "kernel": "idx_score_kernel",
                     "sources": ["dsa_indexer.cu", "sm100.cuh", "common.cuh"], "sha": "9d98db489b72b21a"},
     "moba": {"bytes": 1_150_921_984 + 257_916_160, "kernel": "moba_attn_kernel",
-             "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "00d0b2bd05e1f360"},
+             "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "be1ba744dc70c6c4"},
 }
 
 

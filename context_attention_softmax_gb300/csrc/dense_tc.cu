@@ -1,7 +1,9 @@
 // Dense CP-chunk attention on the 5th-generation tensor cores (sm_103a).
 //
-// TMA loads Q/K/V tiles into 128-byte-swizzled shared memory; one thread
-// issues tcgen05.mma (bf16 x bf16 -> fp32 accumulators in tensor memory);
+// TMA loads Q/K/V tiles into 128-byte-swizzled shared memory; one elected
+// lane of the converged MMA warp issues tcgen05.mma (bf16 x bf16 -> fp32
+// accumulators in tensor memory; elect.sync of a full warp always picks the
+// same lane, so every MMA comes from one thread);
 // softmax warps read S from TMEM, apply the permitted relation and fold each
 // KV tile into the running summary (m, l, z) of "Context parallel attention:
 // exchange keys and merge softmax globally" para 3: z is the PV accumulator

@@ -313,13 +313,14 @@ __device__ __forceinline__ int unit_tiles(const MobaParams& p, int b) {
   return (keys + BN - 1) / BN;
 }
 
-// Roles (256 threads): warp 0 K/V TMA producer, warp 1 MMA issuer + TMEM
-// owner, warps 2-3 gather the unit's query rows (cp.async),
-// warps 4-7 softmax + epilogue (row = TMEM lane).  Units are taken in a
-// fixed stride (blockIdx.x, + gridDim.x, ...); all roles walk the same
-// sequence, with a global tile counter jt across units.  S is double
-// buffered in TMEM, so S(jt+1) runs while softmax(jt) does; P(jt) goes over
-// S(jt); O is reused across units once the previous epilogue released it.
+// Roles (384 threads): warp 0 K/V TMA producer, warp 1 MMA issuer (the
+// converged warp, one elected lane issuing) + TMEM owner, warps 2-3 gather
+// the unit's query rows (cp.async), warps 4-7 softmax, warps 8-11 epilogue
+// (row = TMEM lane).  Units are taken in a fixed stride (blockIdx.x,
+// + gridDim.x, ...); all roles walk the same sequence, with a global tile
+// counter jt across units.  S and O are double buffered in TMEM: S(jt+1)
+// runs while softmax(jt) does, P(jt) goes over S(jt), and unit u
+// accumulates in O buffer u & 1 while the epilogue warps drain unit u - 1.
 __global__ void __launch_bounds__(kThreads, 1)
 moba_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                  const MobaParams p) {

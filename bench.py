@@ -222,7 +222,7 @@ class DenseBwdRunner(Runner):
 
     name = "dense_gqa_bwd"
     kernel = "cpattn_chunk_bwd (bwd_prep_kernel, then bwd_kernel: dk/dv and dq CTAs in one launch)"
-    launches_per_step = 4   # interval init, prep, dk/dv, dq
+    launches_per_step = 3   # interval init, prep, bwd_kernel (dk/dv and dq CTAs)
 
     def __init__(self, device):
         from context_attention_softmax_gb300 import cpattn_chunk_fwd
@@ -298,7 +298,15 @@ class ZigzagRunner(Runner):
         self.cu = torch.as_tensor(z.cu_seqlens, dtype=torch.int32, device=device)
         self.o = [torch.empty_like(q) for q in self.qs]
         self.lse = [torch.empty(q.shape[:2], dtype=torch.float32, device=device) for q in self.qs]
-        self.ws = torch.empty(64 << 20, dtype=torch.uint8, device=device)   # per-piece summaries
+        # The 8 rank calls are independent (own queries and outputs, shared
+        # read-only K/V), as on 8 GPUs: each gets its own stream, started
+        # after everything already on the caller's stream and joined back
+        # into it, so one call's last CTAs overlap the other calls' work
+        # (0.623 -> 0.446 ms per step against one stream).  Each stream has
+        # its own workspace.
+        self.streams = [torch.cuda.Stream(device) for _ in range(z.cp_size)]
+        self.ws = [torch.empty(64 << 20, dtype=torch.uint8, device=device)
+                   for _ in range(z.cp_size)]   # per-piece summaries
         lens = np.diff(z.cu_seqlens.astype(np.int64))
         pairs = int((lens * (lens + 1) // 2).sum())
         H, D = z.q_global.shape[1], z.q_global.shape[2]
@@ -306,7 +314,7 @@ class ZigzagRunner(Runner):
         self.n_rows = z.q_global.shape[0]
         self.launches_per_step = z.cp_size
         self.config = {"workload": "packed THD varlen, zigzag cp=8, 16384 tokens / 8 seqs, "
-                                   "32 heads, d=128, causal; all 8 rank calls",
+                                   "32 heads, d=128, causal; all 8 rank calls, one stream each",
                        "lengths": lens.tolist(), "permitted_pairs_per_head": pairs, "l2": L2_NOTE}
 
     def device_inputs(self):
@@ -316,11 +324,18 @@ class ZigzagRunner(Runner):
         from context_attention_softmax_gb300 import cpattn_chunk_fwd
         z = self.z
         qs, k, v = ins[:z.cp_size], ins[z.cp_size], ins[z.cp_size + 1]
+        main = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(main)
+        for s in self.streams:
+            s.wait_event(start)
         for r in range(z.cp_size):
             cpattn_chunk_fwd(qs[r], k, v, scale=z.scale, causal=True, cu_seqlens=self.cu,
                              q_chunk_map=self.maps[r], kv_chunk_map=self.kvmap,
                              chunk_len=z.chunk_len, out=self.o[r], lse=self.lse[r],
-                             workspace=self.ws)
+                             workspace=self.ws[r], stream=self.streams[r])
+        for s in self.streams:
+            main.wait_stream(s)
 
     def outputs(self):
         return self.o + self.lse

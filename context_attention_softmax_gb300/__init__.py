@@ -9,6 +9,8 @@ the caller are allocated with torch (device memory plumbing only).
 from __future__ import annotations
 
 import ctypes
+import functools
+import inspect
 import math
 
 import torch
@@ -38,6 +40,25 @@ def _ptr(t):
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _on_call_stream(fn):
+    """Runs the call with its `stream` as torch's current stream, so that the
+    tensors the binding creates (host index arrays copied to the device,
+    outputs and workspaces the caller left out) are copied and allocated on
+    the stream the kernels run on: their copies land before the kernels, and
+    the caching allocator reuses their memory only after them."""
+    pos = list(inspect.signature(fn).parameters).index("stream")
+
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        stream = args[pos] if len(args) > pos else kwargs.get("stream")
+        if stream is None:
+            return fn(*args, **kwargs)
+        with torch.cuda.stream(stream):
+            return fn(*args, **kwargs)
+
+    return wrapper
 
 
 def _device_i32(x, device):
@@ -90,6 +111,7 @@ def _args(q, k, v, scale, causal, causal_offset, cu_seqlens, q_chunk_map, kv_chu
     return a
 
 
+@_on_call_stream
 def cpattn_chunk_fwd(q, k, v, scale=None, causal=True, causal_offset=0, cu_seqlens=None,
                      q_chunk_map=None, kv_chunk_map=None, chunk_len=0, kv_chunk_len=0,
                      out=None, lse=None, partial_o=None, partial_lse=None, dev_status=None,
@@ -127,6 +149,7 @@ def cpattn_chunk_fwd(q, k, v, scale=None, causal=True, causal_offset=0, cu_seqle
     return out, lse
 
 
+@_on_call_stream
 def cpattn_chunk_bwd(q, k, v, out, lse, d_out, scale=None, causal=True, causal_offset=0,
                      cu_seqlens=None, q_chunk_map=None, kv_chunk_map=None, chunk_len=0,
                      dq=None, dk=None, dv=None, dev_status=None, workspace=None, stream=None):
@@ -159,6 +182,7 @@ def cpattn_chunk_bwd(q, k, v, out, lse, d_out, scale=None, causal=True, causal_o
     return dq, dk, dv
 
 
+@_on_call_stream
 def cpattn_lse_merge(part_o, part_lse, out=None, lse=None, out_dtype=torch.bfloat16, stream=None):
     """Merge finalised per-chunk (O_c, LSE_c) [n, Tq, H, Dv] / [n, Tq, H]."""
     n, Tq, H, Dv = part_o.shape
@@ -173,6 +197,7 @@ def cpattn_lse_merge(part_o, part_lse, out=None, lse=None, out_dtype=torch.bfloa
     return out, lse
 
 
+@_on_call_stream
 def cpattn_topk_sparse_fwd(q, k, v, indices, block_size=1, scale=None, causal=True,
                            causal_offset=0, cu_seqlens=None, q_chunk_map=None, kv_chunk_map=None,
                            chunk_len=0, out=None, lse=None, dev_status=None, workspace=None,
@@ -199,6 +224,7 @@ def cpattn_topk_sparse_fwd(q, k, v, indices, block_size=1, scale=None, causal=Tr
     return out, lse
 
 
+@_on_call_stream
 def cpattn_block_gate(q, k, block_size, topk, causal_offset=0, q_chunk_map=None, chunk_len=0,
                       sel=None, workspace=None, stream=None):
     """MoBA block selection: int32 [Tq, Hq, topk + 1], ascending, -1 padded."""
@@ -216,6 +242,7 @@ def cpattn_block_gate(q, k, block_size, topk, causal_offset=0, q_chunk_map=None,
     return sel
 
 
+@_on_call_stream
 def cpattn_dsa_indexer(qI, kI, w, topk, causal=True, causal_offset=0, cu_seqlens=None,
                        q_chunk_map=None, chunk_len=0, out=None, workspace=None, stream=None):
     """DSA indexer top-k: int32 [Tq, topk] key indices, ascending, -1 padded.
@@ -248,6 +275,7 @@ def cpattn_version():
     return _lib.load().cpattn_version()
 
 
+@_on_call_stream
 def cpattn_mla_v_up(o_latent, up_v_weight, out=None, dev_status=None, stream=None):
     """Value up-projection after absorbed attention: out[t, h] = o_latent[t, h] @ W[h].
 
@@ -268,6 +296,7 @@ def cpattn_mla_v_up(o_latent, up_v_weight, out=None, dev_status=None, stream=Non
     return out
 
 
+@_on_call_stream
 def cpattn_mla_kv_materialise(kv_c, k_shared, wkv_b, H, N, V, k_out=None, v_out=None,
                               dev_status=None, stream=None):
     """Per-head K [T, H, N + R] and V [T, H, V] (bf16) from gathered latents.

@@ -166,6 +166,13 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     s.min_lo[0] = s.min_lo[1] = LLONG_MAX;
     s.max_hi[0] = s.max_hi[1] = LLONG_MIN;
     fence_mbar_init();
+    // Q of both blocks needs no tile list: its load overlaps the list's
+    // construction below (rows past Tq read the fill value).
+    mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
+    tma_load_3d(s.q[0], &tm_q, &s.q_full, 0, blk0.head, blk0.q0);
+    tma_load_3d(s.q[0] + kHalf, &tm_q, &s.q_full, 64, blk0.head, blk0.q0);
+    tma_load_3d(s.q[1], &tm_q, &s.q_full, 0, blk1.head, blk1.q0);
+    tma_load_3d(s.q[1] + kHalf, &tm_q, &s.q_full, 64, blk1.head, blk1.q0);
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
@@ -263,17 +270,8 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
-      bool q_issued = false;
       for (int i = 0; i < n_run; ++i) {
         const int kt = s.live_kt[i];
-        if (!q_issued) {
-          mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
-          tma_load_3d(s.q[0], &tm_q, &s.q_full, 0, blk0.head, blk0.q0);
-          tma_load_3d(s.q[0] + kHalf, &tm_q, &s.q_full, 64, blk0.head, blk0.q0);
-          tma_load_3d(s.q[1], &tm_q, &s.q_full, 0, blk1.head, blk1.q0);
-          tma_load_3d(s.q[1] + kHalf, &tm_q, &s.q_full, 64, blk1.head, blk1.q0);
-          q_issued = true;
-        }
         const int jt = k_issued, st = jt % NS;
         const uint32_t ph = (jt / NS) & 1;
         if (!mbar_wait(&s.k_empty[st], ph ^ 1, abort_flag, lim)) break;
@@ -287,9 +285,9 @@ dense_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tma_load_3d(s.v[st] + kHalf, &tm_v, &s.v_full[st], 64, g, kt * BN);
         ++v_issued;
       }
-      if (*abort_flag) {  // let every copy in flight land before the CTA exits
+      if (*abort_flag || n_run == 0) {  // let every copy in flight land before the CTA exits
         int no_abort = 0;
-        if (q_issued) mbar_wait(&s.q_full, 0, &no_abort, 200000000ull);
+        mbar_wait(&s.q_full, 0, &no_abort, 200000000ull);
         for (int j = max(0, k_issued - NS); j < k_issued; ++j)
           mbar_wait(&s.k_full[j % NS], (j / NS) & 1, &no_abort, 200000000ull);
         for (int j = max(0, v_issued - NS); j < v_issued; ++j)

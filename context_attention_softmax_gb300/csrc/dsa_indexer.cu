@@ -473,6 +473,8 @@ size_t dsa_indexer_workspace(const cpattn_attn_args& a, int grid) {
   b += (size_t)round_up4(a.Tk) * 4 + (size_t)round_up4(a.Tq) * 4;   // key norms, query weights
   b = (b + 255) & ~size_t(255);
   b += (size_t)grid * a.Tk * (4 + 8) + 256;            // band lists
+  b = (b + 255) & ~size_t(255);
+  if (dsa_indexer_tc_supported(a)) b += dsa_indexer_tc_workspace(a);   // split operands
   return b;
 }
 
@@ -500,7 +502,14 @@ cudaError_t launch_dsa_indexer(const cpattn_attn_args& a, const float* w, int to
   idx_norm_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, stream>>>(a, w, kn, qa);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (a.Tk > 0) {
+  // scores: on the tensor cores (split operands, wider certified bound) when
+  // the shape allows, else the fp32 SIMT kernel
+  const bool tc = dsa_indexer_tc_supported(a);
+  if (tc) {
+    size_t tc_off = ((off + (size_t)grid * a.Tk * (4 + 8) + 256) + 255) & ~size_t(255);
+    e = launch_dsa_indexer_scores_tc(a, w, S, ldS, p + tc_off, stream);
+    if (e != cudaSuccess) return e;
+  } else if (a.Tk > 0) {
     const dim3 g2((unsigned)((a.Tk + kTK - 1) / kTK), (unsigned)((a.Tq + kTQ - 1) / kTQ));
     idx_score_kernel<<<g2, kScoreThreads, 0, stream>>>(a, w, S, ldS);
     e = cudaGetLastError();
@@ -514,7 +523,7 @@ cudaError_t launch_dsa_indexer(const cpattn_attn_args& a, const float* w, int to
   sp.ldS = ldS;
   sp.kn = kn;
   sp.qa = qa;
-  sp.c = (float)((a.Dqk + a.Hq + 4) * 5.9604644775390625e-8 * 1.02);
+  sp.c = tc ? dsa_indexer_tc_bound(a) : (float)((a.Dqk + a.Hq + 4) * 5.9604644775390625e-8 * 1.02);
   sp.band_idx = band_idx;
   sp.band_key = band_key;
   sp.out = out;

@@ -46,6 +46,15 @@ cudaError_t launch_lse_merge(int32_t n_parts, const float* part_o, const float* 
 // given grid, the grid the launcher uses, and the launch (scores, norms,
 // per-row certified top-k).
 size_t dsa_indexer_workspace(const cpattn_attn_args& a, int grid);
+// Tensor-core indexer scores (dsa_indexer_tc.cu): whether the shape takes
+// them, their extra workspace, the bound factor c of their error
+// (|S - score| <= c a_i ||kI_j||) and the launch (split, tile intervals,
+// score GEMM) writing S [Tq, ldS].
+bool dsa_indexer_tc_supported(const cpattn_attn_args& a);
+size_t dsa_indexer_tc_workspace(const cpattn_attn_args& a);
+float dsa_indexer_tc_bound(const cpattn_attn_args& a);
+cudaError_t launch_dsa_indexer_scores_tc(const cpattn_attn_args& a, const float* w, float* S,
+                                         int64_t ldS, void* tc_ws, cudaStream_t stream);
 int dsa_indexer_grid(const cpattn_attn_args& a);
 cudaError_t launch_dsa_indexer(const cpattn_attn_args& a, const float* w, int topk, int32_t* out,
                                void* ws, cudaStream_t stream);

@@ -609,6 +609,11 @@ def _indexer_case(seed, Tq, Tk, H, D, offset, dup=None, cu=None):
     (37, 700, 4, 64, 600, 50),       # every row has more permitted keys than k
     (40, 300, 3, 32, 0, 64),         # early rows: fewer permitted keys than k
     (9, 2000, 4, 128, 1990, 512),    # large k, D = 128
+    # D = 128 takes the tensor-core scores (one instantiation per head count)
+    (37, 700, 4, 128, 600, 50),
+    (40, 300, 8, 128, 0, 64),        # early rows: fewer permitted keys than k
+    (70, 900, 1, 128, 850, 100),
+    (33, 1000, 2, 128, 960, 300),    # a ragged last query tile, keys not a multiple of 128
 ])
 def test_dsa_indexer_matches_float64_oracle(Tq, Tk, H, D, offset, topk):
     qI, kI, w, lay = _indexer_case(31 + Tq, Tq, Tk, H, D, offset)
@@ -618,12 +623,14 @@ def test_dsa_indexer_matches_float64_oracle(Tq, Tk, H, D, offset, topk):
     np.testing.assert_array_equal(got.cpu().numpy(), ref)
 
 
-def test_dsa_indexer_ties_and_packed_sequences():
+@pytest.mark.parametrize("D", [32, 128])
+def test_dsa_indexer_ties_and_packed_sequences(D):
     """Keys 3, 130, 150, 300 and 390 are equal and favoured by every query: with
     k = 2 the two lowest permitted ones (130, 150) win - key 3 lies in the
-    first packed sequence, which the queries of the second never see."""
+    first packed sequence, which the queries of the second never see (D = 32
+    scores on the SIMT path, D = 128 on the tensor cores)."""
     cu = np.array([0, 120, 400], dtype=np.int32)
-    qI, kI, w, lay = _indexer_case(5, 50, 400, 2, 32, 350, dup=(130, 3, 150, 300, 390), cu=cu)
+    qI, kI, w, lay = _indexer_case(5, 50, 400, 2, D, 350, dup=(130, 3, 150, 300, 390), cu=cu)
     ref = orc.dsa_indexer_topk(qI, kI, w, lay, 2)[:, 0, :]
     got = cpattn_dsa_indexer(torch.from_numpy(qI).cuda(), torch.from_numpy(kI).cuda(),
                              torch.from_numpy(w).cuda(), 2, causal_offset=350,

@@ -338,6 +338,31 @@ __device__ double exact_score(const cpattn_attn_args& a, const float* w, int64_t
   return sc;
 }
 
+// fp32 score of key j for query i by one thread, in the arithmetic the SIMT
+// score kernel uses (fma over d in order, relu, fma over the heads in
+// order), so that its error is within (D + H + 4) 2^-24 a_i ||kI_j||.  Rows
+// are read as float4 (the tensor-core path, its only user, requires rows
+// aligned to 16 bytes and D a multiple of 4).
+__device__ float fp32_score(const cpattn_attn_args& a, const float* w, int64_t i, int64_t j) {
+  const float* qI = reinterpret_cast<const float*>(a.q) + i * a.q_stride_t;
+  const float4* k4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.k) + j * a.k_stride_t);
+  float sc = 0.f;
+  for (int h = 0; h < a.Hq; ++h) {
+    const float4* q4 = reinterpret_cast<const float4*>(qI + (int64_t)h * a.q_stride_h);
+    float acc = 0.f;
+#pragma unroll 8
+    for (int d4 = 0; d4 < a.Dqk / 4; ++d4) {
+      const float4 q = __ldg(q4 + d4), k = __ldg(k4 + d4);
+      acc = fmaf(q.x, k.x, acc);
+      acc = fmaf(q.y, k.y, acc);
+      acc = fmaf(q.z, k.z, acc);
+      acc = fmaf(q.w, k.w, acc);
+    }
+    sc = fmaf(w[h], fmaxf(acc, 0.f), sc);
+  }
+  return sc;
+}
+
 struct SelParams {
   cpattn_attn_args a;
   const float* w;
@@ -346,7 +371,8 @@ struct SelParams {
   int64_t ldS;
   const float* kn;
   const float* qa;
-  float c;                 // bound factor (D + H + 4) 2^-24 * 1.02
+  float c;                 // bound factor of the scores S
+  float c2;                // > 0: S came from the tensor cores; bound factor of fp32_score
   int32_t* band_idx;       // per CTA: Tk entries
   uint64_t* band_key;      // per CTA: Tk entries (ordered float64 bits)
   int32_t* out;            // [Tq, topk]
@@ -400,7 +426,55 @@ __global__ void __launch_bounds__(kSelThreads) idx_select_kernel(const SelParams
     }
     atomicAdd(&sm.n_in, my_in);
     __syncthreads();
-    const int n_band = sm.n_band, need = p.topk - sm.n_in;
+    int n_band = sm.n_band, need = p.topk - sm.n_in;
+    if (p.c2 > 0.f && need > 0 && n_band > need) {
+      // The scores S carry the wide tensor-core bound: narrow the band first
+      // with fp32 scores of its members (fma over d in order, relu, fma over
+      // the heads in order) and their own bound c2.  Within the band, a key
+      // whose lower bound beats the (need+1)-th largest upper bound is in, a
+      // key whose upper bound is below the need-th largest lower bound is
+      // out; only the rest is ranked in float64.
+      for (int m = tid; m < n_band; m += kSelThreads)
+        bkey[m] = (uint64_t)__float_as_uint(fp32_score(a, p.w, i, bidx[m]));
+      __syncthreads();
+      const float es2 = __fmul_ru(p.c2, p.qa[i]);
+      auto lkey2 = [&](int64_t m) {
+        return ord32(__fsub_rd(__uint_as_float((uint32_t)bkey[m]), __fmul_ru(es2, p.kn[bidx[m]])));
+      };
+      auto ukey2 = [&](int64_t m) {
+        return ord32(__fadd_ru(__uint_as_float((uint32_t)bkey[m]), __fmul_ru(es2, p.kn[bidx[m]])));
+      };
+      const uint32_t T2 = select32(sm, 0, n_band - 1, need, lkey2);
+      const uint32_t U2 = select32(sm, 0, n_band - 1, need + 1, ukey2);
+      // classify, compacting the undecided members to the front of the list
+      // (a member is written at or before its own position, after every
+      // member of its pass has been read)
+      int n_keep = 0, my_in2 = 0;
+      for (int base = 0; base < n_band; base += kSelThreads) {
+        const int m = base + tid;
+        bool keep = false;
+        int32_t j = 0;
+        if (m < n_band) {
+          j = bidx[m];
+          const uint32_t l = lkey2(m), u = ukey2(m);
+          if (l > U2) {
+            atomicOr(&sel[(j - lo) >> 5], 1u << ((j - lo) & 31));
+            ++my_in2;
+          } else if (u >= T2) {
+            keep = true;
+          }
+        }
+        int kept = 0;
+        const int pos = block_excl_scan(keep ? 1 : 0, sm, kept);
+        if (keep) bidx[n_keep + pos] = j;
+        n_keep += kept;
+        __syncthreads();
+      }
+      int in2 = 0;
+      block_excl_scan(my_in2, sm, in2);
+      need -= in2;
+      n_band = n_keep;
+    }
     if (need > 0) {
       // float64 scores of the band, one warp per member
       for (int m = warp; m < n_band; m += kSelThreads / 32) {
@@ -523,7 +597,9 @@ cudaError_t launch_dsa_indexer(const cpattn_attn_args& a, const float* w, int to
   sp.ldS = ldS;
   sp.kn = kn;
   sp.qa = qa;
-  sp.c = tc ? dsa_indexer_tc_bound(a) : (float)((a.Dqk + a.Hq + 4) * 5.9604644775390625e-8 * 1.02);
+  const float c_simt = (float)((a.Dqk + a.Hq + 4) * 5.9604644775390625e-8 * 1.02);
+  sp.c = tc ? dsa_indexer_tc_bound(a) : c_simt;
+  sp.c2 = tc ? c_simt : 0.f;
   sp.band_idx = band_idx;
   sp.band_key = band_key;
   sp.out = out;

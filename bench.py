@@ -18,7 +18,7 @@ end-to-end figure:
   dsa                DSA top-2048 sparse attention, absorbed MLA (TFLOP/s and
                      gathered GB/s)
   moba               MoBA gate + block-sparse attention (compulsory GB/s)
-  dsa_indexer        the DSA indexer's exact top-2048 (fp32 TFLOP/s)
+  dsa_indexer        the DSA indexer's exact top-2048 (TFLOP/s of its fp32 scores)
   mla_v_up           absorbed-MLA value up-projection of the DSA output (GB/s)
   mla_kv             MLA K/V materialisation from gathered latents (TFLOP/s)
 `--workload NAME` times one of them alone as the top-level record.
@@ -84,8 +84,9 @@ TRAFFIC = {
     "dense_gqa_bwd": {"bytes": 30_470_656 + 5_928_960, "kernel": "bwd_kernel",
                       "sources": ["dense_bwd.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
                       "sha": "5085abcec64ca82e"},
-    "dsa_indexer": {"bytes": 20_698_880 + 243_096_576, "kernel": "idx_score_kernel",
-                    "sources": ["dsa_indexer.cu", "sm100.cuh", "common.cuh"], "sha": "9d98db489b72b21a"},
+    "dsa_indexer": {"bytes": 0 + 0, "kernel": "idx_select_kernel",
+                    "sources": ["dsa_indexer.cu", "dsa_indexer_tc.cu", "sm100.cuh", "common.cuh"],
+                    "sha": "0000000000000000"},
     "moba": {"bytes": 1_150_921_984 + 257_916_160, "kernel": "moba_attn_kernel",
              "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "be1ba744dc70c6c4"},
 }
@@ -498,8 +499,9 @@ class IndexerRunner(Runner):
 
     name = "dsa_indexer"
     bound = "alu"
-    kernel = "cpattn_dsa_indexer (norms, scores, selection)"
-    launches_per_step = 3   # norms, scores, selection
+    kernel = ("cpattn_dsa_indexer (norms, operand split, tile intervals, tensor-core scores, "
+              "selection)")
+    launches_per_step = 5   # norms, split, tile intervals, scores, selection
 
     def __init__(self, device):
         self.w = w = dsa_inputs(device)
@@ -879,7 +881,9 @@ def roofline(runner, mean_ms, dev):
         peak = n_sm * 128 * 2 * sm_mhz * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": None,
-                "peak_source": f"fp32 FMA: {n_sm} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz"}
+                "peak_source": f"fp32 FMA: {n_sm} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz "
+                               "(the ceiling of these fp32 scores on the FMA pipes; the scores "
+                               "run on the tensor cores and the selection dominates the step)"}
     else:
         achieved = runner.work / sec / 1e9
         peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))

@@ -215,6 +215,7 @@ idx_score_kernel(const cpattn_attn_args a, const float* __restrict__ w, float* _
 // Block-wide helpers for 512 threads (16 warps).
 struct SelSmem {
   uint32_t hist[kBins];
+  uint32_t hist2[kBins];           // the second histogram of select32_pair
   int wsum[kSelThreads / 32];
   int found_digit, found_above;
   int n_in, n_band;
@@ -245,9 +246,9 @@ __device__ __forceinline__ int block_excl_scan(int v, SelSmem& sm, int& total) {
 
 // The digit holding the kk-th largest key of a histogram of kBins bins, and
 // the number of keys in higher digits.  Thread t owns bins 4t .. 4t + 3.
-__device__ __forceinline__ void find_digit(SelSmem& sm, int kk) {
+__device__ __forceinline__ void find_digit(SelSmem& sm, int kk, const uint32_t* hist) {
   const int t = threadIdx.x;
-  const int c0 = sm.hist[4 * t], c1 = sm.hist[4 * t + 1], c2 = sm.hist[4 * t + 2], c3 = sm.hist[4 * t + 3];
+  const int c0 = hist[4 * t], c1 = hist[4 * t + 1], c2 = hist[4 * t + 2], c3 = hist[4 * t + 3];
   const int local = c0 + c1 + c2 + c3;
   // suffix sum over threads above t: reverse the order and scan
   const int lane = t & 31, warp = t >> 5;
@@ -274,29 +275,42 @@ __device__ __forceinline__ void find_digit(SelSmem& sm, int kk) {
   __syncthreads();
 }
 
-// The kk-th largest (with multiplicity) of key(j) over j in [lo, hi], for
-// 32-bit keys: three radix passes of 11, 11 and 10 bits.
-template <typename KeyFn>
-__device__ uint32_t select32(SelSmem& sm, int64_t lo, int64_t hi, int kk, KeyFn key) {
-  uint32_t prefix = 0u, pmask = 0u;
+// Selections over j in [lo, hi] of 32-bit keys take three radix passes of 11,
+// 11 and 10 bits.  Two of them run at once: the kk1-th largest of key1 and
+// the kk2-th largest (with multiplicity) of key2, every pass reading each j
+// once and filling both histograms.
+template <typename KeyFn1, typename KeyFn2>
+__device__ void select32_pair(SelSmem& sm, int64_t lo, int64_t hi, int kk1, KeyFn1 key1, int kk2,
+                              KeyFn2 key2, uint32_t& out1, uint32_t& out2) {
+  uint32_t p1 = 0u, p2 = 0u, pmask = 0u;
   const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = shifts[pass];
     const uint32_t dmask = (1u << widths[pass]) - 1u;
-    for (int b = threadIdx.x; b < kBins; b += kSelThreads) sm.hist[b] = 0u;
-    __syncthreads();
-    for (int64_t j = lo + threadIdx.x; j <= hi; j += kSelThreads) {
-      const uint32_t x = key(j);
-      if ((x & pmask) == prefix) atomicAdd(&sm.hist[(x >> shift) & dmask], 1u);
+    for (int b = threadIdx.x; b < kBins; b += kSelThreads) {
+      sm.hist[b] = 0u;
+      sm.hist2[b] = 0u;
     }
     __syncthreads();
-    find_digit(sm, kk);
-    kk -= sm.found_above;
-    prefix |= (uint32_t)sm.found_digit << shift;
+    for (int64_t j = lo + threadIdx.x; j <= hi; j += kSelThreads) {
+      const uint32_t x1 = key1(j), x2 = key2(j);
+      if ((x1 & pmask) == p1) atomicAdd(&sm.hist[(x1 >> shift) & dmask], 1u);
+      if ((x2 & pmask) == p2) atomicAdd(&sm.hist2[(x2 >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    find_digit(sm, kk1, sm.hist);
+    const int d1 = sm.found_digit, a1 = sm.found_above;
+    __syncthreads();   // every thread has read the first result
+    find_digit(sm, kk2, sm.hist2);
+    kk1 -= a1;
+    p1 |= (uint32_t)d1 << shift;
+    kk2 -= sm.found_above;
+    p2 |= (uint32_t)sm.found_digit << shift;
     pmask |= dmask << shift;
     __syncthreads();
   }
-  return prefix;
+  out1 = p1;
+  out2 = p2;
 }
 
 // The same for 64-bit keys of the band members bk[0 .. n): eight 8-bit passes.
@@ -311,7 +325,7 @@ __device__ uint64_t select64(SelSmem& sm, const uint64_t* bk, int n, int kk) {
       if ((x & pmask) == prefix) atomicAdd(&sm.hist[(x >> shift) & 0xffu], 1u);
     }
     __syncthreads();
-    find_digit(sm, kk);
+    find_digit(sm, kk, sm.hist);
     kk -= sm.found_above;
     prefix |= (uint64_t)sm.found_digit << shift;
     pmask |= 0xffull << shift;
@@ -406,8 +420,8 @@ __global__ void __launch_bounds__(kSelThreads) idx_select_kernel(const SelParams
       return ord32(__fadd_ru(srow[j], __fmul_ru(es, p.kn[j])));
     };
     // T: the k-th largest lower bound; U*: the (k+1)-th largest upper bound
-    const uint32_t T = select32(sm, lo, hi, p.topk, lkey);
-    const uint32_t Us = select32(sm, lo, hi, p.topk + 1, ukey);
+    uint32_t T, Us;
+    select32_pair(sm, lo, hi, p.topk, lkey, p.topk + 1, ukey, T, Us);
     const int nw = (int)((n + 31) >> 5);
     for (int x = tid; x < nw; x += kSelThreads) { sel[x] = 0u; eq[x] = 0u; }
     if (tid == 0) { sm.n_in = 0; sm.n_band = 0; }
@@ -444,8 +458,8 @@ __global__ void __launch_bounds__(kSelThreads) idx_select_kernel(const SelParams
       auto ukey2 = [&](int64_t m) {
         return ord32(__fadd_ru(__uint_as_float((uint32_t)bkey[m]), __fmul_ru(es2, p.kn[bidx[m]])));
       };
-      const uint32_t T2 = select32(sm, 0, n_band - 1, need, lkey2);
-      const uint32_t U2 = select32(sm, 0, n_band - 1, need + 1, ukey2);
+      uint32_t T2, U2;
+      select32_pair(sm, 0, n_band - 1, need, lkey2, need + 1, ukey2, T2, U2);
       // classify, compacting the undecided members to the front of the list
       // (a member is written at or before its own position, after every
       // member of its pass has been read)

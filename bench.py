@@ -84,9 +84,9 @@ TRAFFIC = {
     "dense_gqa_bwd": {"bytes": 30_470_656 + 5_928_960, "kernel": "bwd_kernel",
                       "sources": ["dense_bwd.cu", "dense_tc_common.cuh", "sm100.cuh", "common.cuh"],
                       "sha": "5085abcec64ca82e"},
-    "dsa_indexer": {"bytes": 331_847_424 + 28_760_320, "kernel": "idx_select_kernel",
+    "dsa_indexer": {"bytes": 331_365_632 + 28_990_208, "kernel": "idx_select_kernel",
                     "sources": ["dsa_indexer.cu", "dsa_indexer_tc.cu", "sm100.cuh", "common.cuh"],
-                    "sha": "87b919ff2e7ce424"},
+                    "sha": "63fddb7a129a018f"},
     "moba": {"bytes": 1_150_921_984 + 257_916_160, "kernel": "moba_attn_kernel",
              "sources": ["moba_tc.cu", "sm100.cuh", "common.cuh"], "sha": "be1ba744dc70c6c4"},
 }

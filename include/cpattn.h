@@ -298,16 +298,19 @@ cpattn_status cpattn_block_gate_static(const cpattn_attn_args* args, int32_t blo
  * Output indices: device int32 [Tq, topk] contiguous, each row ascending and
  * padded with -1 - directly usable as `indices` of cpattn_topk_sparse_fwd
  * with index_heads = 1 and block_size = 1.  The selection equals the one an
- * exact (float64) evaluation of the scores makes: fp32 scores carry a
- * certified error bound, and only keys whose bound reaches the k-th
- * boundary are ranked again in float64.
+ * exact (float64) evaluation of the scores makes: the scores (fp32 fmas, or
+ * for Dqk = 128 a split bf16 GEMM on the tensor cores) carry a certified
+ * error bound, and only keys whose bound reaches the k-th boundary are
+ * ranked again (first in fp32 under the tighter fp32 bound when the scores
+ * came from the tensor cores, then in float64).
  * Uses args->dtype (CPATTN_FP32), q = qI [Tq, Hq, Dqk] (Hq = indexer heads),
  * k = kI [Tk, 1, Dqk] (Hkv = 1), causal, causal_offset, cu_seqlens and
  * q_chunk_map/chunk_len for positions; keys are in logical order
  * (kv_chunk_map NULL).  w: device fp32 [Hq].  Limits: Dqk <= 256, Hq <= 16,
  * 1 <= topk <= Tk.
  * Workspace: cpattn_workspace_size(CPATTN_OP_DSA_INDEXER, ...) bytes (the
- * fp32 scores of every query and permitted key, key norms, scratch).
+ * fp32 scores of every query and permitted key, key norms, scratch and, for
+ * Dqk = 128, the bf16 split operands).
  */
 cpattn_status cpattn_dsa_indexer(const cpattn_attn_args* args, const float* w, int32_t topk,
                                  int32_t* indices, void* workspace, size_t workspace_bytes,

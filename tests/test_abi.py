@@ -173,6 +173,21 @@ def test_indexer_needs_weights_outputs_and_its_workspace(lib):
     assert lib.cpattn_workspace_size(_lib.OP_DSA_INDEXER, ctypes.byref(a), 16, 1) == 0
 
 
+def test_indexer_workspace_holds_the_tensor_core_operands(lib):
+    """D = 128 (the tensor-core scores) needs, beyond what D = 64 needs, the
+    bf16 split operands [Tq * H, 256] and [Tk, 256] and one 16-byte key
+    interval per 128-row tile, each region 256-byte aligned."""
+    def need(D):
+        a = _indexer_args()
+        a.Dqk, a.q_stride_h, a.q_stride_t, a.k_stride_t, a.k_stride_h = D, D, 4 * D, D, D
+        return lib.cpattn_workspace_size(_lib.OP_DSA_INDEXER, ctypes.byref(a), 16, 1)
+
+    up = lambda x: (x + 255) // 256 * 256
+    rows, Tk = 64 * 4, 256
+    split = up(up(rows * 256 * 2) + Tk * 256 * 2) + (rows + 127) // 128 * 16 + 256
+    assert need(128) - need(64) == split
+
+
 def _bwd_call(lib, a, d_out=0x90000, dq=0xA0000, dk=0xB0000, dv=0xC0000):
     return lib.cpattn_chunk_bwd(ctypes.byref(a), d_out, 16 * 128, 128, dq, 16 * 128, 128,
                                 dk, 4 * 128, 128, dv, 4 * 128, 128, None, 0, None)
